@@ -1,0 +1,121 @@
+"""CPU oracle for multi-LoRA SGMV -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, the package's smoke check and the benchmark's CPU-baseline
+leg may import this package.  The product path (the CUDA library and its
+binding) never imports, links or calls it, and this package never imports
+the product.
+
+The arithmetic lives in ``sgmv_oracle.c`` (plain C, one IEEE operation at a
+time, built with ``-ffp-contract=off``); this module compiles it with gcc and
+marshals numpy arrays to it.  What it computes and the readings it takes are
+stated in the C file's header.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import tempfile
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sgmv_oracle.c")
+_LIB = os.path.join(_HERE, "libsgmv_oracle.so")
+_loaded = {}
+
+CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-fPIC", "-shared", "-std=c11"]
+
+
+def build(out: Optional[str] = None, mutant: int = 0) -> str:
+    """Compile the oracle; returns the path of the shared library."""
+    out = out or _LIB
+    cmd = ["gcc", *CFLAGS, f"-DORACLE_MUTANT={int(mutant)}", _SRC, "-o", out + ".tmp"]
+    subprocess.run(cmd, check=True)
+    os.replace(out + ".tmp", out)
+    return out
+
+
+def _needs_build(path: str) -> bool:
+    return (not os.path.exists(path)) or os.path.getmtime(path) < os.path.getmtime(_SRC)
+
+
+def load(mutant: int = 0) -> ctypes.CDLL:
+    """Load (building first if stale) the oracle, or a planted-mistake variant."""
+    if mutant in _loaded:
+        return _loaded[mutant]
+    if mutant == 0:
+        path = _LIB
+        if _needs_build(path):
+            build(path)
+    else:
+        path = os.path.join(tempfile.gettempdir(), f"libsgmv_oracle_mutant{mutant}_{os.getpid()}.so")
+        build(path, mutant)
+    lib = ctypes.CDLL(path)
+    i32, i64, p = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+    lib.oracle_lora_segment.restype = i32
+    lib.oracle_lora_segment.argtypes = [p, i32, i32, i32, p, p, p, p]
+    lib.oracle_sgmv_f32.restype = i32
+    lib.oracle_sgmv_f32.argtypes = [p, i64, p, p, p, i32, i32, i32, i32, i32, ctypes.c_float, p, i64, p, p, i32]
+    lib.oracle_sgmv_f64.restype = i32
+    lib.oracle_sgmv_f64.argtypes = [p, i64, p, p, p, i32, i32, i32, i32, i32, ctypes.c_double, p, i64, p, p, i32]
+    lib.oracle_mutant.restype = i32
+    assert lib.oracle_mutant() == mutant
+    _loaded[mutant] = lib
+    return lib
+
+
+def bits(a) -> np.ndarray:
+    """bf16 data as a C-contiguous uint16 array of bit patterns. Accepts a
+    uint16 numpy array or a CPU torch.bfloat16 tensor."""
+    if isinstance(a, np.ndarray):
+        assert a.dtype == np.uint16, a.dtype
+        return np.ascontiguousarray(a)
+    import torch  # local: the oracle's C path does not need torch
+
+    assert a.dtype == torch.bfloat16, a.dtype
+    return np.ascontiguousarray(a.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def lora_segment_ref(ids, P: int, max_segments: Optional[int] = None, mutant: int = 0) -> dict:
+    """Stable segmentation of token indices by adapter id (see the C file)."""
+    ids = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    n = int(ids.size)
+    ms = min(n, P) if max_segments is None else int(max_segments)
+    perm = np.empty(n, np.int32)
+    offs = np.empty(ms + 1, np.int32)
+    sad = np.empty(max(ms, 1), np.int32)
+    ns = np.zeros(1, np.int32)
+    n_bad = load(mutant).oracle_lora_segment(_ptr(ids), n, int(P), ms, _ptr(perm), _ptr(offs), _ptr(sad), _ptr(ns))
+    return dict(perm=perm, seg_offsets=offs, seg_adapter=sad[:ms], num_segments=int(ns[0]), n_invalid=int(n_bad))
+
+
+def sgmv_ref(x, A_pool, B_pool, ids, s: float, y0, *, threads: int = 1, f64: bool = False,
+             want_v: bool = False, mutant: int = 0):
+    """y = y0 + s*((x.A[a_i]).B[a_i]) per token, unrounded.
+
+    x: [n, >=h_in] bf16; A_pool: [P, h_in, r]; B_pool: [P, r, h_out];
+    ids: int32 [n]; y0: [n, >=h_out].  Returns y ([n, h_out], fp32 or fp64)
+    and, with want_v, v ([n, r]) as well."""
+    xb, Ab, Bb, yb = bits(x), bits(A_pool), bits(B_pool), bits(y0)
+    ids = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    P, h_in, r = Ab.shape
+    P2, r2, h_out = Bb.shape
+    assert P2 == P and r2 == r
+    n = int(ids.size)
+    assert xb.ndim == 2 and xb.shape[0] == n and xb.shape[1] >= h_in
+    assert yb.ndim == 2 and yb.shape[0] == n and yb.shape[1] >= h_out
+    dt = np.float64 if f64 else np.float32
+    y = np.empty((n, h_out), dt)
+    v = np.zeros((n, r), dt) if want_v else None
+    lib = load(mutant)
+    fn = lib.oracle_sgmv_f64 if f64 else lib.oracle_sgmv_f32
+    fn(_ptr(xb), xb.shape[1], _ptr(Ab), _ptr(Bb), _ptr(ids), n, P, h_in, h_out, r, float(s),
+       _ptr(yb), yb.shape[1], _ptr(y), _ptr(v) if want_v else None, int(threads))
+    return (y, v) if want_v else y
