@@ -1,0 +1,27 @@
+"""B300 (sm_103a) multi-LoRA SGMV: y[i] += s * (x[i] . A[a_i]) . B[a_i] for a
+batch whose tokens name adapters of an HBM-resident pool.
+
+The compute lives in liblora_sgmv.so (hand-written CUDA kernels behind a C
+ABI, declared in include/lora_sgmv.h); this package is its thin binding.
+"""
+
+from .lora_sgmv import (  # noqa: F401
+    LIB_PATH,
+    LORA_MAX_PROJ,
+    STATUS,
+    SYMBOLS,
+    Segments,
+    load_library,
+    lora_segment,
+    lora_segment_workspace_bytes,
+    make_projs,
+    sgmv_expand,
+    sgmv_fused,
+    sgmv_multi,
+    sgmv_shrink,
+)
+
+__all__ = [
+    "Segments", "load_library", "lora_segment", "lora_segment_workspace_bytes", "sgmv_shrink", "sgmv_expand",
+    "sgmv_fused", "sgmv_multi", "make_projs",
+]

@@ -1,0 +1,60 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/lora_sgmv.h"
+
+namespace lsg {
+
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+inline int round_up(int a, int b) { return ceil_div(a, b) * b; }
+
+// ---- segmentation
+struct SegPlan {
+  int nw;             // warps (each owns one histogram row and one chunk of tokens)
+  bool gmem;          // histograms in the workspace instead of shared memory
+  size_t ws_bytes;    // workspace bytes required
+  size_t smem_bytes;  // dynamic shared memory bytes
+};
+SegPlan seg_plan(int n, int P);
+lora_status launch_segment(const int32_t* ids, int n, int P, int32_t* perm, int32_t* seg_offsets,
+                           int32_t* seg_adapter, int32_t* num_segments, int32_t* hist, int32_t* err_flag,
+                           cudaStream_t stream);
+
+// ---- SGMV (CUDA-core split-K path)
+constexpr int kMaxProj = LORA_MAX_PROJ;
+
+struct ProjArgs {
+  const uint16_t* x;
+  const uint16_t* A;
+  const uint16_t* B;
+  uint16_t* y;
+  int64_t ldx, ldy;
+  int32_t h_in, h_out;
+  float scale;
+};
+
+enum Mode : int { kModeShrink = 1, kModeExpand = 2, kModeFused = 3 };
+
+struct SgmvCall {
+  Mode mode;
+  ProjArgs proj[kMaxProj];
+  int n_proj;
+  int r;
+  int n_adapters;
+  lora_segments seg;
+  float* v_out;       // shrink output [n][r]
+  const float* v_in;  // expand input [n][r]
+  int32_t* err_flag;
+};
+
+lora_status launch_sgmv_cc(const SgmvCall& call, cudaStream_t stream);
+
+// Records a CUDA error from a runtime call; returns LORA_ERR_CUDA on failure.
+lora_status cuda_status(cudaError_t e);
+
+}  // namespace lsg

@@ -1,0 +1,168 @@
+// C ABI of liblora_sgmv.so: argument checks on the host, then one launch per
+// call on the caller's stream.  Declarations and contracts: include/lora_sgmv.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "internal.h"
+
+namespace lsg {
+
+lora_status cuda_status(cudaError_t e) { return e == cudaSuccess ? LORA_OK : LORA_ERR_CUDA; }
+
+namespace {
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool al4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool rank_ok(int r) { return r == 8 || r == 16 || r == 32 || r == 64; }
+bool width_ok(int h) { return h >= 8 && (h % 8) == 0; }
+
+lora_status check_seg(const lora_segments* seg, int n_adapters) {
+  if (seg == nullptr || n_adapters < 1) return LORA_ERR_INVALID_ARG;
+  if (seg->n_tokens < 0) return LORA_ERR_INVALID_ARG;
+  if (seg->n_tokens == 0) return LORA_OK;
+  if (!seg->perm || !seg->seg_offsets || !seg->seg_adapter || !seg->num_segments) return LORA_ERR_INVALID_ARG;
+  if (seg->max_segments < 1 || seg->max_segments > seg->n_tokens) return LORA_ERR_INVALID_ARG;
+  if (!al4(seg->perm) || !al4(seg->seg_offsets) || !al4(seg->seg_adapter) || !al4(seg->num_segments))
+    return LORA_ERR_MISALIGNED;
+  return LORA_OK;
+}
+
+lora_status check_proj(const lora_bf16* x, int64_t ldx, const lora_bf16* A, const lora_bf16* B, lora_bf16* y,
+                       int64_t ldy, int h_in, int h_out, bool need_x, bool need_y) {
+  if (need_x) {
+    if (!x || !A) return LORA_ERR_INVALID_ARG;
+    if (!width_ok(h_in)) return LORA_ERR_UNSUPPORTED;
+    if (ldx < h_in) return LORA_ERR_INVALID_ARG;
+    if (!al16(x) || !al16(A) || (ldx % 8) != 0) return LORA_ERR_MISALIGNED;
+  }
+  if (need_y) {
+    if (!y || !B) return LORA_ERR_INVALID_ARG;
+    if (!width_ok(h_out)) return LORA_ERR_UNSUPPORTED;
+    if (ldy < h_out) return LORA_ERR_INVALID_ARG;
+    if (!al16(y) || !al16(B) || (ldy % 8) != 0) return LORA_ERR_MISALIGNED;
+  }
+  return LORA_OK;
+}
+
+}  // namespace
+}  // namespace lsg
+
+using namespace lsg;
+
+extern "C" {
+
+const char* lora_status_str(int s) {
+  switch (s) {
+    case LORA_OK: return "LORA_OK";
+    case LORA_ERR_INVALID_ARG: return "LORA_ERR_INVALID_ARG: invalid argument";
+    case LORA_ERR_MISALIGNED: return "LORA_ERR_MISALIGNED: pointer or leading dimension not 16-byte aligned";
+    case LORA_ERR_UNSUPPORTED: return "LORA_ERR_UNSUPPORTED: rank or width not supported";
+    case LORA_ERR_BAD_ADAPTER_ID: return "LORA_ERR_BAD_ADAPTER_ID: adapter id or permutation entry out of range";
+    case LORA_ERR_WORKSPACE: return "LORA_ERR_WORKSPACE: workspace missing or too small";
+    case LORA_ERR_CUDA: return "LORA_ERR_CUDA: CUDA runtime error";
+    case LORA_ERR_TIMEOUT: return "LORA_ERR_TIMEOUT: a bounded wait in a kernel ran out";
+    default: return "unknown status";
+  }
+}
+
+int lora_abi_version(void) { return LORA_SGMV_ABI_VERSION; }
+
+size_t lora_segment_workspace_bytes(int32_t n_tokens, int32_t n_adapters) {
+  if (n_tokens < 0 || n_adapters < 1) return 0;
+  return seg_plan(n_tokens, n_adapters).ws_bytes;
+}
+
+lora_status lora_segment(const int32_t* ids, int32_t n_tokens, int32_t n_adapters, int32_t* perm,
+                         int32_t* seg_offsets, int32_t* seg_adapter, int32_t* num_segments, void* workspace,
+                         size_t workspace_bytes, int32_t* err_flag, lora_stream_t stream) {
+  if (n_tokens < 0 || n_adapters < 1) return LORA_ERR_INVALID_ARG;
+  if (!seg_offsets || !num_segments) return LORA_ERR_INVALID_ARG;
+  if (n_tokens > 0 && (!ids || !perm || !seg_adapter)) return LORA_ERR_INVALID_ARG;
+  const SegPlan pl = seg_plan(n_tokens, n_adapters);
+  if (pl.gmem && (workspace == nullptr || workspace_bytes < pl.ws_bytes)) return LORA_ERR_WORKSPACE;
+  if (pl.gmem && !al4(workspace)) return LORA_ERR_MISALIGNED;
+  return launch_segment(ids, n_tokens, n_adapters, perm, seg_offsets, seg_adapter, num_segments,
+                        static_cast<int32_t*>(workspace), err_flag, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lora_status sgmv_shrink(const lora_bf16* x, int64_t ldx, const lora_bf16* A_pool, int32_t n_adapters,
+                        int32_t h_in, int32_t r, const lora_segments* seg, float* v, int32_t* err_flag,
+                        lora_stream_t stream) {
+  lora_status s = check_seg(seg, n_adapters);
+  if (s != LORA_OK) return s;
+  if (!rank_ok(r)) return LORA_ERR_UNSUPPORTED;
+  if (seg->n_tokens == 0) return LORA_OK;
+  s = check_proj(x, ldx, A_pool, nullptr, nullptr, 0, h_in, 0, true, false);
+  if (s != LORA_OK) return s;
+  if (!v) return LORA_ERR_INVALID_ARG;
+  if (!al16(v)) return LORA_ERR_MISALIGNED;
+  SgmvCall c{};
+  c.mode = kModeShrink;
+  c.proj[0] = ProjArgs{x, A_pool, nullptr, nullptr, ldx, 0, h_in, 0, 1.0f};
+  c.n_proj = 1;
+  c.r = r;
+  c.n_adapters = n_adapters;
+  c.seg = *seg;
+  c.v_out = v;
+  c.err_flag = err_flag;
+  return launch_sgmv_cc(c, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lora_status sgmv_expand(const float* v, const lora_bf16* B_pool, int32_t n_adapters, int32_t r, int32_t h_out,
+                        float scale, const lora_segments* seg, lora_bf16* y, int64_t ldy, int32_t* err_flag,
+                        lora_stream_t stream) {
+  lora_status s = check_seg(seg, n_adapters);
+  if (s != LORA_OK) return s;
+  if (!rank_ok(r)) return LORA_ERR_UNSUPPORTED;
+  if (seg->n_tokens == 0) return LORA_OK;
+  s = check_proj(nullptr, 0, nullptr, B_pool, y, ldy, 0, h_out, false, true);
+  if (s != LORA_OK) return s;
+  if (!v) return LORA_ERR_INVALID_ARG;
+  if (!al16(v)) return LORA_ERR_MISALIGNED;
+  SgmvCall c{};
+  c.mode = kModeExpand;
+  c.proj[0] = ProjArgs{nullptr, nullptr, B_pool, y, 0, ldy, 0, h_out, scale};
+  c.n_proj = 1;
+  c.r = r;
+  c.n_adapters = n_adapters;
+  c.seg = *seg;
+  c.v_in = v;
+  c.err_flag = err_flag;
+  return launch_sgmv_cc(c, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lora_status sgmv_multi(const lora_proj* projs, int32_t n_proj, int32_t n_adapters, int32_t r,
+                       const lora_segments* seg, int32_t* err_flag, lora_stream_t stream) {
+  if (!projs || n_proj < 1) return LORA_ERR_INVALID_ARG;
+  if (n_proj > LORA_MAX_PROJ) return LORA_ERR_UNSUPPORTED;
+  lora_status s = check_seg(seg, n_adapters);
+  if (s != LORA_OK) return s;
+  if (!rank_ok(r)) return LORA_ERR_UNSUPPORTED;
+  if (seg->n_tokens == 0) return LORA_OK;
+  SgmvCall c{};
+  c.mode = kModeFused;
+  for (int i = 0; i < n_proj; ++i) {
+    const lora_proj& q = projs[i];
+    s = check_proj(q.x, q.ldx, q.A_pool, q.B_pool, q.y, q.ldy, q.h_in, q.h_out, true, true);
+    if (s != LORA_OK) return s;
+    c.proj[i] = ProjArgs{q.x, q.A_pool, q.B_pool, q.y, q.ldx, q.ldy, q.h_in, q.h_out, q.scale};
+  }
+  c.n_proj = n_proj;
+  c.r = r;
+  c.n_adapters = n_adapters;
+  c.seg = *seg;
+  c.err_flag = err_flag;
+  return launch_sgmv_cc(c, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lora_status sgmv_fused(const lora_bf16* x, int64_t ldx, const lora_bf16* A_pool, const lora_bf16* B_pool,
+                       int32_t n_adapters, int32_t h_in, int32_t h_out, int32_t r, float scale,
+                       const lora_segments* seg, lora_bf16* y, int64_t ldy, int32_t* err_flag,
+                       lora_stream_t stream) {
+  lora_proj q{x, A_pool, B_pool, y, ldx, ldy, h_in, h_out, scale};
+  return sgmv_multi(&q, 1, n_adapters, r, seg, err_flag, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,215 @@
+// lora_segment: group a batch's tokens by adapter.
+//
+// Punica: Multi-Tenant LoRA Serving (research.elamur.ai summary),
+// "Interesting ideas" I2: sort the batch by adapter so that same-adapter
+// requests sit next to each other and form dense segments; "Summary":
+// requests of the same adapter are grouped.
+//
+// One CTA runs a stable counting sort.  Warp w owns the w-th contiguous chunk
+// of tokens and one histogram row H[w][0..P] (bucket P collects invalid ids,
+// so they land after every valid token).  Steps: per-warp counts (warp-match
+// aggregated, no atomics: the row is private to the warp), per-key exclusive
+// scan over warps, block-wide exclusive scan over keys (giving segment starts)
+// fused with the compaction of the non-empty adapters, then a stable scatter
+// where each warp walks its chunk in order and ranks equal keys inside a
+// 32-token group by warp match.  Rows live in shared memory unless the pool is
+// too large, in which case they live in the caller's workspace.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace lsg {
+
+constexpr size_t kSegSmemBudget = 200 * 1024;
+constexpr int kSegScratchInts = 128;  // block-scan partials, in shared memory
+
+SegPlan seg_plan(int n, int P) {
+  SegPlan pl{};
+  const int want = std::clamp(std::max(ceil_div(std::max(n, 1), 64), ceil_div(P + 1, 256)), 1, 32);
+  const size_t row = static_cast<size_t>(P + 1) * sizeof(int32_t);
+  const size_t scratch = kSegScratchInts * sizeof(int32_t);
+  auto need = [&](int w) { return static_cast<size_t>(w + 1) * row + scratch; };
+  pl.nw = want;
+  if (need(1) <= kSegSmemBudget) {
+    while (pl.nw > 1 && need(pl.nw) > kSegSmemBudget) pl.nw /= 2;
+    pl.gmem = false;
+    pl.ws_bytes = 0;
+    pl.smem_bytes = need(pl.nw);
+  } else {
+    pl.gmem = true;
+    pl.ws_bytes = static_cast<size_t>(pl.nw + 1) * row;
+    pl.smem_bytes = scratch;
+  }
+  return pl;
+}
+
+__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    int o = __shfl_up_sync(0xffffffffu, v, d);
+    if (lane >= d) v += o;
+  }
+  return v;
+}
+
+__global__ void __launch_bounds__(1024)
+    lora_segment_kernel(const int32_t* __restrict__ ids, int n, int P, int max_segments,
+                        int32_t* __restrict__ perm, int32_t* __restrict__ seg_offsets,
+                        int32_t* __restrict__ seg_adapter, int32_t* __restrict__ num_segments,
+                        int32_t* gbuf, int32_t* err_flag) {
+  extern __shared__ __align__(16) int32_t sbuf[];
+  // The SGMV launch that follows may start its prologue now; it reads our
+  // outputs only after griddepcontrol.wait, i.e. after this grid completes.
+  pdl_launch_dependents();
+  // Our own inputs (ids) and outputs may be in use by the previous launch.
+  pdl_wait();
+
+  const int nt = blockDim.x, nw = nt >> 5, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int Pp = P + 1;
+  int32_t* H = gbuf ? gbuf : sbuf;                    // [nw][Pp]
+  int32_t* TOT = H + static_cast<size_t>(nw) * Pp;    // [Pp]
+  int32_t* scratch = gbuf ? sbuf : (TOT + Pp);        // kSegScratchInts
+
+  const size_t hsize = static_cast<size_t>(nw) * Pp;
+  for (size_t i = tid; i < hsize; i += nt) H[i] = 0;
+  __syncthreads();
+
+  // 1. per-warp histogram of its chunk
+  const int chunk = (n + nw - 1) / nw;
+  const int lo = min(n, warp * chunk), hi = min(n, lo + chunk);
+  int32_t* Hw = H + static_cast<size_t>(warp) * Pp;
+  bool bad_seen = false;
+  for (int base = lo; base < hi; base += 32) {
+    const int i = base + lane;
+    const bool act = i < hi;
+    const unsigned am = __ballot_sync(0xffffffffu, act);
+    if (act) {
+      const int a = ids[i];
+      const int key = (a >= 0 && a < P) ? a : P;
+      bad_seen |= (key == P);
+      const unsigned peers = __match_any_sync(am, key);
+      if (lane == __ffs(peers) - 1) Hw[key] += __popc(peers);
+    }
+    __syncwarp();
+  }
+  if (bad_seen) set_err(err_flag, LORA_ERR_BAD_ADAPTER_ID);
+  __syncthreads();
+
+  // 2. per key: exclusive scan across warps, column total into TOT
+  for (int a = tid; a < Pp; a += nt) {
+    int run = 0;
+    for (int w = 0; w < nw; ++w) {
+      const size_t idx = static_cast<size_t>(w) * Pp + a;
+      const int c = H[idx];
+      H[idx] = run;
+      run += c;
+    }
+    TOT[a] = run;
+  }
+  __syncthreads();
+
+  // 3. block exclusive scan over keys of (count, non-empty flag); writes the
+  //    segment start of every key and compacts non-empty adapters.
+  const int per = (Pp + nt - 1) / nt;
+  const int a0 = min(Pp, tid * per), a1 = min(Pp, a0 + per);
+  int sum = 0, cnt = 0;
+  for (int a = a0; a < a1; ++a) {
+    const int c = TOT[a];
+    sum += c;
+    cnt += (a < P && c > 0);
+  }
+  const int xs = warp_incl_scan(sum, lane), xc = warp_incl_scan(cnt, lane);
+  if (lane == 31) {
+    scratch[warp] = xs;
+    scratch[32 + warp] = xc;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int s = lane < nw ? scratch[lane] : 0;
+    const int c = lane < nw ? scratch[32 + lane] : 0;
+    const int is = warp_incl_scan(s, lane), ic = warp_incl_scan(c, lane);
+    __syncwarp();
+    scratch[lane] = is - s;
+    scratch[32 + lane] = ic - c;
+    if (lane == 31) {
+      scratch[64] = is;
+      scratch[65] = ic;
+    }
+  }
+  __syncthreads();
+  int run_s = scratch[warp] + xs - sum;
+  int run_c = scratch[32 + warp] + xc - cnt;
+  for (int a = a0; a < a1; ++a) {
+    const int c = TOT[a];
+    TOT[a] = run_s;
+    if (a < P && c > 0) {
+      seg_adapter[run_c] = a;
+      seg_offsets[run_c] = run_s;
+      ++run_c;
+    }
+    run_s += c;
+  }
+  __syncthreads();
+  const int S = scratch[65];
+  const int n_valid = TOT[P];
+  if (tid == 0) *num_segments = S;
+  for (int s = S + tid; s <= max_segments; s += nt) seg_offsets[s] = n_valid;
+  for (int s = S + tid; s < max_segments; s += nt) seg_adapter[s] = -1;
+
+  // 4. cursors: first output slot of (warp, key)
+  for (size_t i = tid; i < hsize; i += nt) H[i] += TOT[i % Pp];
+  __syncthreads();
+
+  // 5. stable scatter: warps walk their chunks in token order
+  for (int base = lo; base < hi; base += 32) {
+    const int i = base + lane;
+    const bool act = i < hi;
+    const unsigned am = __ballot_sync(0xffffffffu, act);
+    if (act) {
+      const int a = ids[i];
+      const int key = (a >= 0 && a < P) ? a : P;
+      const unsigned peers = __match_any_sync(am, key);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      const int b = Hw[key];
+      perm[b + rank] = i;
+      __syncwarp(am);
+      if (lane == __ffs(peers) - 1) Hw[key] = b + __popc(peers);
+    }
+    __syncwarp();
+  }
+}
+
+lora_status launch_segment(const int32_t* ids, int n, int P, int32_t* perm, int32_t* seg_offsets,
+                           int32_t* seg_adapter, int32_t* num_segments, int32_t* hist, int32_t* err_flag,
+                           cudaStream_t stream) {
+  static std::once_flag once[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
+  cudaError_t attr_err = cudaSuccess;
+  std::call_once(once[dev & 63], [&] {
+    attr_err = cudaFuncSetAttribute(lora_segment_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(kSegSmemBudget));
+  });
+  if (attr_err != cudaSuccess) return LORA_ERR_CUDA;
+  const SegPlan pl = seg_plan(n, P);
+  const int max_segments = std::min(n, P);
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute at[1];
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(pl.nw * 32);
+  cfg.dynamicSmemBytes = pl.smem_bytes;
+  cfg.stream = stream;
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int32_t* gbuf = pl.gmem ? hist : nullptr;
+  return cuda_status(cudaLaunchKernelEx(&cfg, lora_segment_kernel, ids, n, P, max_segments, perm, seg_offsets,
+                                        seg_adapter, num_segments, gbuf, err_flag));
+}
+
+}  // namespace lsg

@@ -1,0 +1,240 @@
+"""Python binding of liblora_sgmv.so (argument marshalling only).
+
+Every function has the name of the C entry point it calls and passes
+torch tensors' device pointers and the current CUDA stream.  All arithmetic
+runs in the library's CUDA kernels; there is no fallback: a missing library
+raises at import of the first call, a non-OK status raises RuntimeError.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "liblora_sgmv.so")
+_lib: Optional[ctypes.CDLL] = None
+
+LORA_MAX_PROJ = 8
+STATUS = {
+    0: "LORA_OK", -1: "LORA_ERR_INVALID_ARG", -2: "LORA_ERR_MISALIGNED", -3: "LORA_ERR_UNSUPPORTED",
+    -4: "LORA_ERR_BAD_ADAPTER_ID", -5: "LORA_ERR_WORKSPACE", -6: "LORA_ERR_CUDA", -7: "LORA_ERR_TIMEOUT",
+}
+# exported symbols declared in include/lora_sgmv.h
+SYMBOLS = ("lora_status_str", "lora_abi_version", "lora_segment_workspace_bytes", "lora_segment",
+           "sgmv_shrink", "sgmv_expand", "sgmv_fused", "sgmv_multi")
+
+
+class LoraSegments(ctypes.Structure):
+    _fields_ = [("perm", ctypes.c_void_p), ("seg_offsets", ctypes.c_void_p), ("seg_adapter", ctypes.c_void_p),
+                ("num_segments", ctypes.c_void_p), ("n_tokens", ctypes.c_int32), ("max_segments", ctypes.c_int32)]
+
+
+class LoraProj(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("A_pool", ctypes.c_void_p), ("B_pool", ctypes.c_void_p),
+                ("y", ctypes.c_void_p), ("ldx", ctypes.c_int64), ("ldy", ctypes.c_int64),
+                ("h_in", ctypes.c_int32), ("h_out", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load liblora_sgmv.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing; build it with `python -m adapter_gemm_02_b300.build`")
+    lib = ctypes.CDLL(path)
+    p, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    lib.lora_status_str.restype = ctypes.c_char_p
+    lib.lora_status_str.argtypes = [ctypes.c_int]
+    lib.lora_abi_version.restype = ctypes.c_int
+    lib.lora_abi_version.argtypes = []
+    lib.lora_segment_workspace_bytes.restype = sz
+    lib.lora_segment_workspace_bytes.argtypes = [i32, i32]
+    lib.lora_segment.restype = ctypes.c_int
+    lib.lora_segment.argtypes = [p, i32, i32, p, p, p, p, p, sz, p, p]
+    lib.sgmv_shrink.restype = ctypes.c_int
+    lib.sgmv_shrink.argtypes = [p, i64, p, i32, i32, i32, ctypes.POINTER(LoraSegments), p, p, p]
+    lib.sgmv_expand.restype = ctypes.c_int
+    lib.sgmv_expand.argtypes = [p, p, i32, i32, i32, ctypes.c_float, ctypes.POINTER(LoraSegments), p, i64, p, p]
+    lib.sgmv_fused.restype = ctypes.c_int
+    lib.sgmv_fused.argtypes = [p, i64, p, p, i32, i32, i32, i32, ctypes.c_float, ctypes.POINTER(LoraSegments),
+                               p, i64, p, p]
+    lib.sgmv_multi.restype = ctypes.c_int
+    lib.sgmv_multi.argtypes = [ctypes.POINTER(LoraProj), i32, i32, i32, ctypes.POINTER(LoraSegments), p, p]
+    _lib = lib
+    return lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        msg = load_library().lora_status_str(status).decode()
+        raise RuntimeError(f"{what} failed: {msg} ({status})")
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _req(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+
+
+def _rows(t: torch.Tensor, name: str) -> int:
+    """Leading dimension of a row-major [n, width] matrix with unit column stride."""
+    if t.stride(1) != 1 and t.shape[1] > 1:
+        raise ValueError(f"{name} must have unit column stride")
+    return t.stride(0) if t.shape[0] > 1 else max(t.stride(0), t.shape[1])
+
+
+def _pool(t: torch.Tensor, name: str) -> None:
+    _req(t, name, torch.bfloat16, 3)
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous [n_adapters, ., .]")
+
+
+@dataclass
+class Segments:
+    """Device-side segmentation (output of lora_segment)."""
+    perm: torch.Tensor          # int32 [n]
+    seg_offsets: torch.Tensor   # int32 [max_segments + 1]
+    seg_adapter: torch.Tensor   # int32 [max_segments]
+    num_segments: torch.Tensor  # int32 [1]
+    n_tokens: int
+    max_segments: int
+    n_adapters: int
+
+    def __post_init__(self):
+        self._c = LoraSegments(self.perm.data_ptr(), self.seg_offsets.data_ptr(), self.seg_adapter.data_ptr(),
+                               self.num_segments.data_ptr(), self.n_tokens, self.max_segments)
+
+    @property
+    def c_struct(self) -> LoraSegments:
+        return self._c
+
+    @staticmethod
+    def empty(n_tokens: int, n_adapters: int, device="cuda") -> "Segments":
+        ms = min(n_tokens, n_adapters)
+        i32 = dict(dtype=torch.int32, device=device)
+        return Segments(torch.empty(max(n_tokens, 1), **i32), torch.empty(ms + 1, **i32),
+                        torch.empty(max(ms, 1), **i32), torch.empty(1, **i32), n_tokens, ms, n_adapters)
+
+
+def lora_segment_workspace_bytes(n_tokens: int, n_adapters: int) -> int:
+    return int(load_library().lora_segment_workspace_bytes(n_tokens, n_adapters))
+
+
+def lora_segment(ids: torch.Tensor, n_adapters: int, *, out: Optional[Segments] = None,
+                 workspace: Optional[torch.Tensor] = None, err_flag: Optional[torch.Tensor] = None,
+                 stream=None) -> Segments:
+    """Stable grouping of tokens by adapter id (see include/lora_sgmv.h)."""
+    lib = load_library()
+    _req(ids, "ids", torch.int32, 1)
+    n = ids.shape[0]
+    seg = out if out is not None else Segments.empty(n, n_adapters, ids.device)
+    if seg.n_tokens != n or seg.n_adapters != n_adapters:
+        raise ValueError("out was sized for another batch")
+    need = lora_segment_workspace_bytes(n, n_adapters)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=ids.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.lora_segment(_ptr(ids.contiguous()), n, n_adapters, _ptr(seg.perm), _ptr(seg.seg_offsets),
+                            _ptr(seg.seg_adapter), _ptr(seg.num_segments), _ptr(workspace), ws_bytes,
+                            _ptr(err_flag), _stream(stream)), "lora_segment")
+    return seg
+
+
+def sgmv_shrink(x: torch.Tensor, A_pool: torch.Tensor, seg: Segments, *, v: Optional[torch.Tensor] = None,
+                err_flag: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """v[i] = x[i] . A[a_i] in fp32."""
+    lib = load_library()
+    _req(x, "x", torch.bfloat16, 2)
+    _pool(A_pool, "A_pool")
+    P, h_in, r = A_pool.shape
+    if x.shape[1] != h_in:
+        raise ValueError("x width != h_in")
+    if v is None:
+        v = torch.zeros(x.shape[0], r, dtype=torch.float32, device=x.device)
+    _req(v, "v", torch.float32, 2)
+    _check(lib.sgmv_shrink(_ptr(x), _rows(x, "x"), _ptr(A_pool), P, h_in, r, ctypes.byref(seg.c_struct),
+                           _ptr(v), _ptr(err_flag), _stream(stream)), "sgmv_shrink")
+    return v
+
+
+def sgmv_expand(v: torch.Tensor, B_pool: torch.Tensor, seg: Segments, y: torch.Tensor, scale: float, *,
+                err_flag: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """y[i] += scale * v[i] . B[a_i] (in place)."""
+    lib = load_library()
+    _req(v, "v", torch.float32, 2)
+    _pool(B_pool, "B_pool")
+    _req(y, "y", torch.bfloat16, 2)
+    P, r, h_out = B_pool.shape
+    if y.shape[1] != h_out or v.shape[1] != r:
+        raise ValueError("shape mismatch")
+    if not v.is_contiguous():
+        raise ValueError("v must be contiguous")
+    _check(lib.sgmv_expand(_ptr(v), _ptr(B_pool), P, r, h_out, float(scale), ctypes.byref(seg.c_struct),
+                           _ptr(y), _rows(y, "y"), _ptr(err_flag), _stream(stream)), "sgmv_expand")
+    return y
+
+
+def sgmv_fused(x: torch.Tensor, A_pool: torch.Tensor, B_pool: torch.Tensor, seg: Segments, y: torch.Tensor,
+               scale: float, *, err_flag: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """y[i] += scale * (x[i] . A[a_i]) . B[a_i] in one launch (in place)."""
+    lib = load_library()
+    _req(x, "x", torch.bfloat16, 2)
+    _req(y, "y", torch.bfloat16, 2)
+    _pool(A_pool, "A_pool")
+    _pool(B_pool, "B_pool")
+    P, h_in, r = A_pool.shape
+    _, r2, h_out = B_pool.shape
+    if r2 != r or x.shape[1] != h_in or y.shape[1] != h_out or B_pool.shape[0] != P:
+        raise ValueError("shape mismatch")
+    _check(lib.sgmv_fused(_ptr(x), _rows(x, "x"), _ptr(A_pool), _ptr(B_pool), P, h_in, h_out, r, float(scale),
+                          ctypes.byref(seg.c_struct), _ptr(y), _rows(y, "y"), _ptr(err_flag), _stream(stream)),
+           "sgmv_fused")
+    return y
+
+
+def make_projs(projs: Sequence) -> "ctypes.Array":
+    """Host array of lora_proj from (x, A_pool, B_pool, y, scale) tuples."""
+    arr = (LoraProj * len(projs))()
+    for i, (x, A, B, y, s) in enumerate(projs):
+        _req(x, "x", torch.bfloat16, 2)
+        _req(y, "y", torch.bfloat16, 2)
+        _pool(A, "A_pool")
+        _pool(B, "B_pool")
+        if A.shape[2] != B.shape[1] or x.shape[1] != A.shape[1] or y.shape[1] != B.shape[2]:
+            raise ValueError(f"projection {i}: shape mismatch")
+        arr[i] = LoraProj(x.data_ptr(), A.data_ptr(), B.data_ptr(), y.data_ptr(), _rows(x, "x"), _rows(y, "y"),
+                          A.shape[1], B.shape[2], float(s))
+    return arr
+
+
+def sgmv_multi(projs: Sequence, seg: Segments, *, err_flag: Optional[torch.Tensor] = None, stream=None,
+               c_projs=None) -> None:
+    """sgmv_fused over up to 8 projections sharing `seg`, in one launch.
+    projs: sequence of (x, A_pool, B_pool, y, scale)."""
+    lib = load_library()
+    if not 1 <= len(projs) <= LORA_MAX_PROJ:
+        raise ValueError("1..8 projections")
+    arr = c_projs if c_projs is not None else make_projs(projs)
+    P, _, r = projs[0][1].shape
+    _check(lib.sgmv_multi(arr, len(projs), P, r, ctypes.byref(seg.c_struct), _ptr(err_flag), _stream(stream)),
+           "sgmv_multi")

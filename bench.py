@@ -1,0 +1,500 @@
+#!/usr/bin/env python
+"""Benchmark of the multi-LoRA SGMV hot path on one B300 per process.
+
+One step = lora_segment (per-token adapter ids -> segments) + sgmv_fused (or
+sgmv_multi) over one batch, inputs resident in HBM.  Default workload:
+Llama2-7B decode projection 4096 -> 4096, r = 16, 32 tokens, each token a
+different adapter of a 64-adapter pool (mixed adapters), s = 1.
+
+Prints one JSON line.  `value` is microseconds per step (lower is better),
+timed with CUDA events around a CUDA graph of K steps that rotates over
+input copies whose touched bytes exceed twice the L2, so every step reads
+HBM.  `roofline` grades the fused kernel against measured HBM bandwidth;
+`e2e` times the same step through the Python API from pinned host buffers;
+`cpu_baseline` times the CPU oracle (test infrastructure) on host cores.
+
+--impl reference times the CPU oracle as the reference arm.
+Multi-GPU (torchrun): every rank runs its own replica of the workload
+(independent batches, no data-path collective); timing is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from workloads import WORKLOADS, make_inputs  # noqa: E402
+
+DEFAULT_WORKLOAD = "7b_proj_distinct"
+METRIC = "fused SGMV µs & % HBM roofline, Llama2-7B dims r=16 bs32 mixed adapters"
+L2_BYTES = 126 * 2 ** 20
+FALLBACK_HBM_GBS = 6400.0
+
+
+# ----------------------------------------------------------------- accounting
+
+def algorithmic_bytes(wl, ids: np.ndarray) -> int:
+    """Unique bytes one call must move: A and B slabs of every distinct valid
+    adapter of every projection, each distinct x once, y read and written."""
+    valid = ids[(ids >= 0) & (ids < wl.P)]
+    D = int(np.unique(valid).size)
+    n = int(ids.size)
+    w = sum((p.h_in * wl.r + wl.r * p.h_out) * 2 for p in wl.projs) * D
+    xs = {}
+    for p in wl.projs:
+        xs[p.x_key] = p.h_in
+    x = sum(n * h * 2 for h in xs.values())
+    y = sum(n * p.h_out * 2 * 2 for p in wl.projs)
+    return w + x + y
+
+
+def flops(wl, ids: np.ndarray) -> int:
+    n = int(((ids >= 0) & (ids < wl.P)).sum())
+    return sum(2 * n * wl.r * (p.h_in + p.h_out) for p in wl.projs)
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "adapter_gemm_02_b300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = source_hash()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) == 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == workload \
+                and parts[2] == want:
+            return int(parts[3])
+    return None
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 10:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        pw = [float(r[4]) for r in rows if r[4].replace(".", "", 1).isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for nm, val in zip(names, r[6:10]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        loaded = [s for s, p in zip(sm, pw)] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+# ----------------------------------------------------------------- distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(x: float, world: int) -> float:
+    """Max over ranks (gloo or nccl); identity for one process."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- oracle timing
+
+def time_oracle(wl, inp_cpu, seconds: float, threads: int, max_calls: int = 10 ** 9):
+    """Seconds per full call of the CPU oracle (segmentation + per-token
+    SGMV over every projection) on this host; returns (s_per_call, calls)."""
+    import oracle  # test infrastructure: the CPU baseline leg only
+
+    ids = inp_cpu.ids.numpy()
+    x = {k: oracle.bits(v) for k, v in inp_cpu.x.items()}
+    A = [oracle.bits(a) for a in inp_cpu.A]
+    B = [oracle.bits(b) for b in inp_cpu.B]
+    Y = [oracle.bits(y) for y in inp_cpu.y0]
+    calls = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.lora_segment_ref(ids, wl.P)
+        for i, p in enumerate(wl.projs):
+            oracle.sgmv_ref(x[p.x_key], A[i], B[i], ids, wl.scale, Y[i], threads=threads)
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or calls >= max_calls:
+            return el / calls, calls
+
+
+def run_reference(args) -> None:
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import torch
+
+    wl = WORKLOADS[args.workload]
+    threads = os.cpu_count() or 1
+    inp = make_inputs(wl, "cpu")
+    for _ in range(args.warmup):
+        time_oracle(wl, inp, 0.0, threads, max_calls=1)
+    per, calls = time_oracle(wl, inp, 0.0, threads, max_calls=max(1, args.steps))
+    us = per * 1e6
+    out = {
+        "impl": "reference", "metric": METRIC, "value": round(us, 3), "unit": "us", "n_gpus": args.gpus,
+        "steps": calls, "warmup": args.warmup, "ms_per_step": round(per * 1e3, 4), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.description, "name": wl.name, "n_tokens": wl.n, "rank": wl.r,
+                   "pool": wl.P, "projections": len(wl.projs)},
+        "cpu_baseline": {"value": round(us, 3), "unit": "us", "cores": threads, "kind": "oracle",
+                         "sample": f"{calls} full calls (segmentation + per-token fp32 SGMV, all tokens)"},
+        "e2e": {"value": round(us, 3), "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "torch": torch.__version__,
+    }
+    print(json.dumps(out), flush=True)
+
+
+# ----------------------------------------------------------------- our arm
+
+def run_ours(args) -> None:
+    import torch
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    import adapter_gemm_02_b300 as lsg
+
+    wl = WORKLOADS[args.workload]
+    K, Wm = args.steps, args.warmup
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+
+    ids_np = wl.ids()
+    abytes = algorithmic_bytes(wl, ids_np)
+    nflop = flops(wl, ids_np)
+    copy_bytes = abytes  # bytes one step touches
+    NB = max(2, min(args.max_copies, int(np.ceil(2.2 * L2_BYTES / copy_bytes))))
+
+    copies = []
+    for c in range(NB):
+        inp = make_inputs(wl, dev, copy=c)
+        seg = lsg.Segments.empty(wl.n, wl.P, dev)
+        projs = [(inp.x[p.x_key], inp.A[i], inp.B[i], inp.y0[i], wl.scale) for i, p in enumerate(wl.projs)]
+        copies.append((inp, seg, projs, lsg.make_projs(projs)))
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(k):
+        inp, seg, projs, cproj = copies[k % NB]
+        lsg.lora_segment(inp.ids, wl.P, out=seg, err_flag=err)
+        if len(projs) == 1:
+            x, A, B, y, s = projs[0]
+            lsg.sgmv_fused(x, A, B, seg, y, s, err_flag=err)
+        else:
+            lsg.sgmv_multi(projs, seg, err_flag=err, c_projs=cproj)
+
+    def fused_only(k):
+        inp, seg, projs, cproj = copies[k % NB]
+        if len(projs) == 1:
+            x, A, B, y, s = projs[0]
+            lsg.sgmv_fused(x, A, B, seg, y, s, err_flag=err)
+        else:
+            lsg.sgmv_multi(projs, seg, err_flag=err, c_projs=cproj)
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for k in range(max(Wm, NB)):
+            step(k)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, f"device error flag {int(err.item())}"
+
+    # graph of K steps (value) ...
+    g_step = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step, stream=side):
+        for k in range(K):
+            step(k)
+    # ... and graph of K fused launches with events around each (kernel time)
+    ev_a = [_timing_event() for _ in range(K)]
+    ev_b = [_timing_event() for _ in range(K)]
+    g_kern = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_kern, stream=side):
+        for k in range(K):
+            ev_a[k].record()
+            fused_only(k)
+            ev_b[k].record()
+    torch.cuda.synchronize()
+
+    # settle clocks under load (untimed), then the timed region
+    t_end = time.perf_counter() + args.settle
+    while time.perf_counter() < t_end:
+        g_step.replay()
+        torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g_step.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_total = e0.elapsed_time(e1)
+    ms_step = reduce_max(ms_total / K, world)
+
+    g_kern.replay()
+    torch.cuda.synchronize()
+    kern_ms = [ev_a[k].elapsed_time(ev_b[k]) for k in range(K)]
+    kern_avg_ms = float(np.mean(kern_ms))
+    clocks = sampler.stop()
+    assert int(err.item()) == 0, f"device error flag {int(err.item())}"
+
+    # end to end through the Python API from pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        inp0, seg0, projs0, cproj0 = copies[0]
+        h_ids = inp0.ids.cpu().pin_memory()
+        h_x = {k: v.cpu().pin_memory() for k, v in inp0.x.items()}
+        h_y = [y.cpu().pin_memory() for y in inp0.y0]
+        h_out = [torch.empty_like(y).pin_memory() for y in h_y]
+        d_ids = torch.empty_like(inp0.ids)
+        d_x = {k: torch.empty_like(v) for k, v in inp0.x.items()}
+        d_y = [torch.empty_like(y) for y in inp0.y0]
+        seg_e = lsg.Segments.empty(wl.n, wl.P, dev)
+        dprojs = [(d_x[p.x_key], inp0.A[i], inp0.B[i], d_y[i], wl.scale) for i, p in enumerate(wl.projs)]
+        cdp = lsg.make_projs(dprojs)
+        bi = h_ids.numel() * 4 + sum(v.numel() * 2 for v in h_x.values()) + sum(y.numel() * 2 for y in h_y)
+        bo = sum(y.numel() * 2 for y in h_out)
+
+        def e2e_step():
+            d_ids.copy_(h_ids, non_blocking=True)
+            for k in d_x:
+                d_x[k].copy_(h_x[k], non_blocking=True)
+            for d, h in zip(d_y, h_y):
+                d.copy_(h, non_blocking=True)
+            lsg.lora_segment(d_ids, wl.P, out=seg_e, err_flag=err)
+            if len(dprojs) == 1:
+                x, A, B, y, s = dprojs[0]
+                lsg.sgmv_fused(x, A, B, seg_e, y, s, err_flag=err)
+            else:
+                lsg.sgmv_multi(dprojs, seg_e, err_flag=err, c_projs=cdp)
+            for h, d in zip(h_out, d_y):
+                h.copy_(d, non_blocking=True)
+
+        for _ in range(Wm):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record()
+        for _ in range(K):
+            e2e_step()
+        f1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_us = reduce_max(f0.elapsed_time(f1) / K * 1e3, world)
+        e2e = {"value": round(e2e_us, 3), "unit": "us", "h2d_bytes_per_step": int(bi),
+               "d2h_bytes_per_step": int(bo), "path": "python API, pinned host buffers, stream-ordered copies"}
+
+    # mixed vs single adapter on the same shape (Punica: almost no difference)
+    mixed = None
+    if args.workload.startswith("7b_proj_") and not args.no_mixed:
+        mixed = {}
+        for pat in ("same", "zipf", "distinct"):
+            mixed[pat] = round(_time_variant(f"7b_proj_{pat}", K, Wm, dev, lsg, args.max_copies), 3)
+        mixed["distinct_over_same"] = round(mixed["distinct"] / mixed["same"], 3)
+
+    peak, peak_kind = hbm_peak()
+    achieved = abytes / (kern_avg_ms * 1e-3) / 1e9
+    kname = "sgmv_cc_kernel"
+    traffic = recorded_traffic(kname, wl.name)
+    out = {
+        "metric": METRIC, "value": round(ms_step * 1e3, 3), "unit": "us", "n_gpus": world, "steps": K,
+        "warmup": Wm, "ms_per_step": round(ms_step, 5), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.description, "name": wl.name, "n_tokens": wl.n, "rank": wl.r, "pool": wl.P,
+                   "distinct_adapters": int(np.unique(ids_np).size), "projections": len(wl.projs),
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": f"rotating {NB} input copies (x, ids, y, pool); {NB * copy_bytes / L2_BYTES:.1f}x L2 "
+                         "touched per cycle",
+                   "timing": "CUDA graph of K steps, CUDA events around the replay"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_kind,
+                     "kernel": kname, "kernel_us": round(kern_avg_ms * 1e3, 3),
+                     "algorithmic_bytes_per_launch": int(abytes), "flops_per_launch": int(nflop),
+                     "tflops": round(nflop / (kern_avg_ms * 1e-3) / 1e12, 4)},
+        "gpu_launches": 2 * K,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if mixed is not None:
+        out["mixed_vs_single_us"] = mixed
+    if rank == 0 and world == 1 and not args.no_cpu:
+        threads = os.cpu_count() or 1
+        inp_cpu = make_inputs(wl, "cpu")
+        per, calls = time_oracle(wl, inp_cpu, args.cpu_seconds, threads)
+        out["cpu_baseline"] = {"value": round(per * 1e6, 3), "unit": "us", "cores": threads, "kind": "oracle",
+                               "sample": f"{calls} full calls of the workload in {args.cpu_seconds:.0f} s "
+                                         "(segmentation + per-token fp32 SGMV, all tokens)"}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def _timing_event():
+    """A timing event whose record inside a graph capture is an event-record
+    node (external), so its timestamp can be read after the replay."""
+    import torch
+
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return torch.cuda.Event(enable_timing=True)
+
+
+def _time_variant(name, K, Wm, dev, lsg, max_copies):
+    """Microseconds per step (segment + fused) of another id pattern."""
+    import torch
+
+    wl = WORKLOADS[name]
+    ids_np = wl.ids()
+    NB = max(2, min(max_copies, int(np.ceil(2.2 * L2_BYTES / algorithmic_bytes(wl, ids_np)))))
+    copies = []
+    for c in range(NB):
+        inp = make_inputs(wl, dev, copy=c)
+        copies.append((inp, lsg.Segments.empty(wl.n, wl.P, dev)))
+    side = torch.cuda.Stream(dev)
+
+    def step(k):
+        inp, seg = copies[k % NB]
+        lsg.lora_segment(inp.ids, wl.P, out=seg)
+        lsg.sgmv_fused(inp.x["x"], inp.A[0], inp.B[0], seg, inp.y0[0], wl.scale)
+
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for k in range(max(Wm, NB)):
+            step(k)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for k in range(K):
+            step(k)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / K * 1e3
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--settle", type=float, default=0.5, help="seconds of untimed replays before timing")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--max-copies", type=int, default=256)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-mixed", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

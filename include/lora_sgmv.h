@@ -1,0 +1,193 @@
+/*
+ * lora_sgmv.h -- C ABI of the B300 (sm_103a) multi-LoRA SGMV library
+ * (liblora_sgmv.so).
+ *
+ * The operation.  Punica: Serving Multiple LoRA Finetuned LLM as One
+ * (vecbase.com), "How It Works": a LoRA finetune adds two small matrices A and
+ * B to a pretrained weight W, and the output is produced with Segmented Gather
+ * Matrix-Vector multiplication (SGMV) in a CUDA kernel.  Punica: Multi-Tenant
+ * LoRA Serving (research.elamur.ai summary), "Summary": one batch mixes
+ * requests of many adapters; the backbone runs as an ordinary GEMM and the
+ * per-adapter low-rank additions are computed together, requests of the same
+ * adapter grouped; "Interesting ideas" I2: sort the batch by adapter so that
+ * same-adapter rows form dense segments.  For token i with adapter a_i:
+ *
+ *     y[i,:] += s * ((x[i,:] . A[a_i]) . B[a_i])
+ *
+ * computed as a shrink v = x.A (rank r, fp32) followed by an expand
+ * y += s * v.B.
+ *
+ * Conventions shared by every call.
+ *  - bf16 data is passed as raw 16-bit patterns (lora_bf16).
+ *  - Every pointer argument named as device memory must be device memory of
+ *    the current CUDA device; host memory is never read by a kernel.  The
+ *    caller owns and allocates every buffer (including workspaces); the
+ *    library allocates no device memory and keeps no per-call state.
+ *  - Calls are ordered on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and never synchronise the host.
+ *  - The return value reports errors found on the host before any launch
+ *    (bad sizes, null or misaligned pointers, too small workspace) and launch
+ *    failures (LORA_ERR_CUDA).  Nothing is launched when it is not LORA_OK.
+ *  - Errors found on the device (an adapter id outside [0, n_adapters), a
+ *    permutation entry outside [0, n_tokens), a wait that ran out of time) are
+ *    recorded in *err_flag (device int32, may be NULL) with the first error's
+ *    code winning (atomic compare-and-swap from 0); the offending token or
+ *    segment is skipped and its output rows are left untouched.  The caller
+ *    clears *err_flag and reads it after its own synchronisation.
+ *  - Layouts (a reading: the pages give none): x is [n_tokens][ldx] row-major,
+ *    y is [n_tokens][ldy] row-major, the adapter pools are contiguous slabs
+ *    A_pool[n_adapters][h_in][r] and B_pool[n_adapters][r][h_out], row-major,
+ *    so that the adapter id is the slab index.
+ *  - Supported shapes: r in {8, 16, 32, 64}; h_in, h_out >= 8 and multiples
+ *    of 8; ldx, ldy multiples of 8; x, y, A_pool, B_pool, v 16-byte aligned.
+ *    Other shapes return LORA_ERR_UNSUPPORTED, other alignments
+ *    LORA_ERR_MISALIGNED.
+ */
+#ifndef LORA_SGMV_H_
+#define LORA_SGMV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LORA_SGMV_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define LORA_API __attribute__((visibility("default")))
+#else
+#define LORA_API
+#endif
+
+typedef uint16_t lora_bf16;                /* bfloat16 bit pattern */
+typedef struct CUstream_st* lora_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  LORA_OK = 0,
+  LORA_ERR_INVALID_ARG = -1,    /* null pointer, negative size, ld < width ... */
+  LORA_ERR_MISALIGNED = -2,     /* pointer or leading dimension not 16-byte aligned */
+  LORA_ERR_UNSUPPORTED = -3,    /* rank or width outside the supported set */
+  LORA_ERR_BAD_ADAPTER_ID = -4, /* device: adapter id or permutation entry out of range */
+  LORA_ERR_WORKSPACE = -5,      /* workspace missing or smaller than required */
+  LORA_ERR_CUDA = -6,           /* a CUDA runtime call or launch failed */
+  LORA_ERR_TIMEOUT = -7         /* device: a bounded wait inside a kernel ran out */
+} lora_status;
+
+/* Static string naming a status code (unknown codes give "unknown status"). */
+LORA_API const char* lora_status_str(int status);
+
+/* LORA_SGMV_ABI_VERSION of the loaded library. */
+LORA_API int lora_abi_version(void);
+
+/*
+ * Segmentation record produced by lora_segment and read by every SGMV call
+ * (all pointers device memory, owned by the caller).
+ *   perm[n_tokens]             perm[k] = original index of the k-th token in
+ *                              adapter order (stable: ties in token order).
+ *   seg_offsets[max_segments+1]  segment s covers perm[seg_offsets[s] ..
+ *                              seg_offsets[s+1]); entries past the last segment
+ *                              hold the number of valid tokens.
+ *   seg_adapter[max_segments]  adapter id of segment s, ascending; -1 past the
+ *                              last segment.
+ *   num_segments               device scalar: number of non-empty segments.
+ *   max_segments               min(n_tokens, n_adapters) (capacity of the arrays).
+ */
+typedef struct {
+  const int32_t* perm;
+  const int32_t* seg_offsets;
+  const int32_t* seg_adapter;
+  const int32_t* num_segments;
+  int32_t n_tokens;
+  int32_t max_segments;
+} lora_segments;
+
+/*
+ * Bytes of device workspace lora_segment needs for (n_tokens, n_adapters).
+ * 0 when the per-warp histograms fit in shared memory (pools of up to ~25k
+ * adapters); otherwise the histograms live in the workspace.
+ */
+LORA_API size_t lora_segment_workspace_bytes(int32_t n_tokens, int32_t n_adapters);
+
+/*
+ * Group tokens by adapter: Punica: Multi-Tenant LoRA Serving, "Interesting
+ * ideas" I2 (sort the batch by adapter) and "Summary" (requests of the same
+ * adapter grouped).  A stable counting sort: histogram of ids over
+ * [0, n_adapters), exclusive scan into segment offsets, compaction of the
+ * non-empty adapters (ascending id), stable scatter of token indices.
+ *   ids[n_tokens]      device int32 adapter ids.
+ *   perm, seg_offsets, seg_adapter, num_segments: outputs as described for
+ *                      lora_segments, sized with max_segments =
+ *                      min(n_tokens, n_adapters).
+ *   workspace          device memory of lora_segment_workspace_bytes() bytes
+ *                      (may be NULL when that is 0); contents on entry are
+ *                      ignored, contents on exit are unspecified.
+ * Ids outside [0, n_adapters) join no segment: they are counted out of
+ * seg_offsets[num_segments] and listed in perm after every valid token, in
+ * token order; *err_flag gets LORA_ERR_BAD_ADAPTER_ID.
+ * n_tokens == 0 writes num_segments = 0 and seg_offsets[0] = 0.
+ */
+LORA_API lora_status lora_segment(const int32_t* ids, int32_t n_tokens, int32_t n_adapters,
+                         int32_t* perm, int32_t* seg_offsets, int32_t* seg_adapter,
+                         int32_t* num_segments, void* workspace, size_t workspace_bytes,
+                         int32_t* err_flag, lora_stream_t stream);
+
+/*
+ * Shrink: v[i,:] = x[i,:] . A[a_i]  (fp32 accumulate, fp32 output).
+ * Punica: Multi-Tenant LoRA Serving, "Summary" (the low-rank part of the
+ * per-adapter addition).  x [n][ldx] bf16; A_pool [n_adapters][h_in][r] bf16;
+ * v [n][r] fp32 in original token order (rows of skipped tokens untouched).
+ */
+LORA_API lora_status sgmv_shrink(const lora_bf16* x, int64_t ldx, const lora_bf16* A_pool,
+                        int32_t n_adapters, int32_t h_in, int32_t r, const lora_segments* seg,
+                        float* v, int32_t* err_flag, lora_stream_t stream);
+
+/*
+ * Expand: y[i,:] += s * v[i,:] . B[a_i]  (fp32 accumulate, one round-to-
+ * nearest-even to bf16 at the store).  v [n][r] fp32; B_pool
+ * [n_adapters][r][h_out] bf16; y [n][ldy] bf16, updated in place.
+ */
+LORA_API lora_status sgmv_expand(const float* v, const lora_bf16* B_pool, int32_t n_adapters, int32_t r,
+                        int32_t h_out, float scale, const lora_segments* seg, lora_bf16* y,
+                        int64_t ldy, int32_t* err_flag, lora_stream_t stream);
+
+/*
+ * Shrink and expand in one launch, v kept on chip (never written to device
+ * memory): y[i,:] += s * ((x[i,:] . A[a_i]) . B[a_i]).  Arguments as for
+ * sgmv_shrink / sgmv_expand.  The tensor-core path for long segments rounds v
+ * to bf16 before the expand product (its error, about 2^-9 relative to |v|,
+ * is far inside the parity tolerance); the CUDA-core path keeps v in fp32.
+ */
+LORA_API lora_status sgmv_fused(const lora_bf16* x, int64_t ldx, const lora_bf16* A_pool,
+                       const lora_bf16* B_pool, int32_t n_adapters, int32_t h_in, int32_t h_out,
+                       int32_t r, float scale, const lora_segments* seg, lora_bf16* y,
+                       int64_t ldy, int32_t* err_flag, lora_stream_t stream);
+
+/* One projection of a multi-projection call (device pointers, host struct). */
+typedef struct {
+  const lora_bf16* x;      /* [n][ldx] */
+  const lora_bf16* A_pool; /* [n_adapters][h_in][r] */
+  const lora_bf16* B_pool; /* [n_adapters][r][h_out] */
+  lora_bf16* y;            /* [n][ldy], updated in place */
+  int64_t ldx, ldy;
+  int32_t h_in, h_out;
+  float scale;
+} lora_proj;
+
+#define LORA_MAX_PROJ 8
+
+/*
+ * sgmv_fused for up to LORA_MAX_PROJ projections (e.g. q,k,v,o,gate,up,down
+ * of one transformer layer) sharing one segmentation and one rank, in one
+ * launch.  `projs` is a host array of n_proj descriptors (read during the
+ * call only).  Projections may share x; their y must not overlap.
+ */
+LORA_API lora_status sgmv_multi(const lora_proj* projs, int32_t n_proj, int32_t n_adapters, int32_t r,
+                       const lora_segments* seg, int32_t* err_flag, lora_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LORA_SGMV_H_ */

@@ -1,0 +1,120 @@
+"""The C ABI library loads and exports every symbol its header declares, and
+its host-side argument checks answer without touching a GPU (CPU only)."""
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import adapter_gemm_02_b300 as lsg
+from adapter_gemm_02_b300 import build as lbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        for m in re.finditer(r"LORA_API\s+[\w\s\*]+?\b(\w+)\s*\(", src):
+            names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if lbuild.stale():
+        lbuild.build()
+    return lsg.load_library()
+
+
+def test_header_declares_the_boundary():
+    assert _declared_symbols() == set(lsg.SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.lora_abi_version() == 1
+    for code, name in lsg.STATUS.items():
+        assert lib.lora_status_str(code).decode().startswith(name)
+    assert lib.lora_status_str(12345) == b"unknown status"
+
+
+def test_segment_workspace_sizes(lib):
+    # histograms fit shared memory for pools up to ~25k adapters
+    assert lsg.lora_segment_workspace_bytes(256, 1000) == 0
+    assert lsg.lora_segment_workspace_bytes(6224, 32) == 0
+    big = lsg.lora_segment_workspace_bytes(100, 60000)
+    assert big >= 2 * 60001 * 4 and big % 4 == 0
+    assert lsg.lora_segment_workspace_bytes(-1, 10) == 0
+
+
+def _seg_struct(n=4, ms=4, ptrs=True):
+    p = 256 if ptrs else 0
+    return lsg.lora_sgmv.LoraSegments(p, p, p, p, n, ms)
+
+
+def test_host_validation_without_gpu(lib):
+    """Every check below fails before any CUDA call is made."""
+    P = ctypes.c_void_p
+    s = _seg_struct()
+    # lora_segment: negative n, no adapters, null outputs
+    assert lib.lora_segment(P(16), -1, 4, P(16), P(16), P(16), P(16), None, 0, None, None) == -1
+    assert lib.lora_segment(P(16), 4, 0, P(16), P(16), P(16), P(16), None, 0, None, None) == -1
+    assert lib.lora_segment(P(16), 4, 4, P(16), None, P(16), P(16), None, 0, None, None) == -1
+    # huge pool: workspace required
+    assert lib.lora_segment(P(16), 4, 60000, P(16), P(16), P(16), P(16), None, 0, None, None) == -5
+    # sgmv_*: null segmentation, unsupported rank, bad widths, misalignment, ld < width
+    assert lib.sgmv_fused(P(256), 64, P(256), P(256), 4, 64, 64, 16, 1.0, None, P(256), 64, None, None) == -1
+    assert lib.sgmv_fused(P(256), 64, P(256), P(256), 4, 64, 64, 12, 1.0, ctypes.byref(s), P(256), 64, None,
+                          None) == -3
+    assert lib.sgmv_fused(P(256), 64, P(256), P(256), 4, 60, 64, 16, 1.0, ctypes.byref(s), P(256), 64, None,
+                          None) == -3
+    assert lib.sgmv_fused(P(258), 64, P(256), P(256), 4, 64, 64, 16, 1.0, ctypes.byref(s), P(256), 64, None,
+                          None) == -2
+    assert lib.sgmv_fused(P(256), 68, P(256), P(256), 4, 64, 64, 16, 1.0, ctypes.byref(s), P(256), 64, None,
+                          None) == -2
+    assert lib.sgmv_fused(P(256), 32, P(256), P(256), 4, 64, 64, 16, 1.0, ctypes.byref(s), P(256), 64, None,
+                          None) == -1
+    assert lib.sgmv_fused(P(256), 64, P(256), P(256), 0, 64, 64, 16, 1.0, ctypes.byref(s), P(256), 64, None,
+                          None) == -1
+    bad = _seg_struct(ptrs=False)
+    assert lib.sgmv_fused(P(256), 64, P(256), P(256), 4, 64, 64, 16, 1.0, ctypes.byref(bad), P(256), 64, None,
+                          None) == -1
+    # n_tokens == 0 is a no-op
+    zero = _seg_struct(n=0, ms=0, ptrs=False)
+    assert lib.sgmv_fused(P(256), 64, P(256), P(256), 4, 64, 64, 16, 1.0, ctypes.byref(zero), P(256), 64, None,
+                          None) == 0
+    assert lib.sgmv_shrink(P(256), 64, P(256), 4, 64, 16, ctypes.byref(s), None, None, None) == -1
+    assert lib.sgmv_shrink(P(256), 64, P(256), 4, 64, 16, ctypes.byref(s), P(260), None, None) == -2
+    assert lib.sgmv_expand(P(256), P(256), 4, 16, 64, 1.0, ctypes.byref(s), P(256), 63, None, None) == -1
+    # multi: too many projections
+    arr = (lsg.lora_sgmv.LoraProj * 9)()
+    assert lib.sgmv_multi(arr, 9, 4, 16, ctypes.byref(s), None, None) == -3
+    assert lib.sgmv_multi(arr, 0, 4, 16, ctypes.byref(s), None, None) == -1
+
+
+def test_product_path_fails_loudly_without_library(tmp_path):
+    from adapter_gemm_02_b300 import lora_sgmv
+
+    saved = lora_sgmv._lib
+    try:
+        lora_sgmv._lib = None
+        with pytest.raises(RuntimeError, match="missing"):
+            lora_sgmv.load_library(str(tmp_path / "nope.so"))
+    finally:
+        lora_sgmv._lib = saved
+
+
+def test_product_never_imports_the_oracle():
+    for path in glob.glob(os.path.join(ROOT, "adapter_gemm_02_b300", "**", "*"), recursive=True):
+        if path.endswith((".py", ".cu", ".cuh", ".h")):
+            src = open(path).read()
+            assert "import oracle" not in src and "from oracle" not in src, path
+            assert "sgmv_oracle" not in src, path
