@@ -13,6 +13,7 @@ from .lora_sgmv import (  # noqa: F401
     Segments,
     load_library,
     lora_segment,
+    lora_segment_noalloc,
     lora_segment_workspace_bytes,
     make_projs,
     sgmv_expand,
@@ -22,6 +23,6 @@ from .lora_sgmv import (  # noqa: F401
 )
 
 __all__ = [
-    "Segments", "load_library", "lora_segment", "lora_segment_workspace_bytes", "sgmv_shrink", "sgmv_expand",
+    "Segments", "load_library", "lora_segment", "lora_segment_noalloc", "lora_segment_workspace_bytes", "sgmv_shrink", "sgmv_expand",
     "sgmv_fused", "sgmv_multi", "make_projs",
 ]

@@ -26,7 +26,8 @@ STATUS = {
 }
 # exported symbols declared in include/lora_sgmv.h
 SYMBOLS = ("lora_status_str", "lora_abi_version", "lora_segment_workspace_bytes", "lora_segment",
-           "sgmv_shrink", "sgmv_expand", "sgmv_fused", "sgmv_multi")
+           "lora_segment_noalloc", "sgmv_shrink", "sgmv_expand", "sgmv_fused", "sgmv_multi")
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class LoraSegments(ctypes.Structure):
@@ -57,6 +58,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lora_segment_workspace_bytes.argtypes = [i32, i32]
     lib.lora_segment.restype = ctypes.c_int
     lib.lora_segment.argtypes = [p, i32, i32, p, p, p, p, p, sz, p, p]
+    lib.lora_segment_noalloc.restype = ctypes.c_int
+    lib.lora_segment_noalloc.argtypes = [p, i32, i32, p, p, p, p, p, p]
     lib.sgmv_shrink.restype = ctypes.c_int
     lib.sgmv_shrink.argtypes = [p, i64, p, i32, i32, i32, ctypes.POINTER(LoraSegments), p, p, p]
     lib.sgmv_expand.restype = ctypes.c_int
@@ -158,6 +161,22 @@ def lora_segment(ids: torch.Tensor, n_adapters: int, *, out: Optional[Segments] 
                             _ptr(seg.seg_adapter), _ptr(seg.num_segments), _ptr(workspace), ws_bytes,
                             _ptr(err_flag), _stream(stream)), "lora_segment")
     return seg
+
+
+def lora_segment_noalloc(ids: torch.Tensor, n_adapters: int, out: Segments, *,
+                         err_flag: Optional[torch.Tensor] = None, stream=None) -> Segments:
+    """lora_segment without a workspace: large pools use the library's own
+    8 MiB device scratch array, so the call allocates nothing (the outputs
+    `out` are the caller's).  Calls that overlap on the GPU race on that array."""
+    lib = load_library()
+    _req(ids, "ids", torch.int32, 1)
+    n = ids.shape[0]
+    if out.n_tokens != n or out.n_adapters != n_adapters:
+        raise ValueError("out was sized for another batch")
+    _check(lib.lora_segment_noalloc(_ptr(ids), n, n_adapters, _ptr(out.perm), _ptr(out.seg_offsets),
+                                    _ptr(out.seg_adapter), _ptr(out.num_segments), _ptr(err_flag),
+                                    _stream(stream)), "lora_segment_noalloc")
+    return out
 
 
 def sgmv_shrink(x: torch.Tensor, A_pool: torch.Tensor, seg: Segments, *, v: Optional[torch.Tensor] = None,

@@ -134,6 +134,31 @@ LORA_API lora_status lora_segment(const int32_t* ids, int32_t n_tokens, int32_t 
                          int32_t* err_flag, lora_stream_t stream);
 
 /*
+ * lora_segment for callers that cannot allocate device memory (no cudaMalloc
+ * and no allocator of their own at hand: code running under a framework that
+ * owns the allocator, a real-time loop whose memory was planned up front, a
+ * plugin handed only its input and output buffers).  The paper has no
+ * counterpart; this is a packaging variant of lora_segment.
+ *
+ * Same arguments, outputs and device-side errors as lora_segment, without the
+ * workspace: when the pool is too large for shared-memory histograms the
+ * scratch comes from a library-owned device array of
+ * LORA_SEGMENT_NOALLOC_SCRATCH_BYTES (8 MiB) that every GPU which loads the
+ * library holds until the process exits.  Pools needing more scratch than that
+ * (more than about 63,500 adapters) return LORA_ERR_WORKSPACE without a launch.
+ * The call allocates nothing.
+ *  - The first call on a device (with that device current) looks up the
+ *    array's device address; make that first call before any stream capture.
+ *  - All calls share the array and it keeps the last call's contents (each
+ *    kernel clears the part it uses), so calls whose kernels overlap on the
+ *    GPU (different streams, or concurrent graphs) race on it: order them.
+ */
+#define LORA_SEGMENT_NOALLOC_SCRATCH_BYTES (8u << 20)
+LORA_API lora_status lora_segment_noalloc(const int32_t* ids, int32_t n_tokens, int32_t n_adapters,
+                                          int32_t* perm, int32_t* seg_offsets, int32_t* seg_adapter,
+                                          int32_t* num_segments, int32_t* err_flag, lora_stream_t stream);
+
+/*
  * Shrink: v[i,:] = x[i,:] . A[a_i]  (fp32 accumulate, fp32 output).
  * Punica: Multi-Tenant LoRA Serving, "Summary" (the low-rank part of the
  * per-adapter addition).  x [n][ldx] bf16; A_pool [n_adapters][h_in][r] bf16;
