@@ -1,6 +1,7 @@
 // Host-side declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -53,6 +54,11 @@ struct SgmvCall {
 };
 
 lora_status launch_sgmv_cc(const SgmvCall& call, cudaStream_t stream);
+
+// TMA tensor map over bf16 data: `rank` dims (innermost first), byte strides
+// of dims 1.., box extents in elements, swizzle span in bytes (0 = none).
+lora_status encode_tmap_bf16(CUtensorMap* out, const void* base, int rank, const uint64_t* dims,
+                             const uint64_t* strides_bytes, const uint32_t* box, int swizzle_bytes);
 
 // Records a CUDA error from a runtime call; returns LORA_ERR_CUDA on failure.
 lora_status cuda_status(cudaError_t e);

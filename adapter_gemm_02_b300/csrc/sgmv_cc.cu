@@ -1,30 +1,40 @@
-// SGMV on CUDA cores for short segments (decode), the HBM-bound regime.
+// SGMV for short segments (decode), the HBM-bound regime.
 //
 // Punica: Multi-Tenant LoRA Serving (research.elamur.ai summary), "Summary":
 // the per-adapter low-rank additions of a mixed batch are computed together,
-// requests of one adapter grouped into segments; "Key points": rank is far
-// below the hidden size (16 vs 4096).  For a decode segment the work is a few
-// rank-r dot products per token, so time goes to streaming the adapter's A
-// and B slabs from HBM; this kernel is built to keep HBM busy:
+// requests of one adapter grouped into segments; "Key points": SGMV runs on
+// the GPU's tensor cores, and rank is far below the hidden size (16 vs 4096).
+// For a decode segment the work is a few rank-r dot products per token, so
+// time goes to streaming the adapter's A and B slabs from HBM; this kernel is
+// built to keep HBM busy with as few instructions per byte as possible:
 //
 //  * Work item = (token tile of <= T tokens of one segment, projection).  A
 //    cluster of C CTAs takes one item: CTA `rank` streams rows
 //    [rank*k_chunk, +k_chunk) of A (split-K of the shrink) and columns
 //    [rank*n_chunk, +n_chunk) of B (split-N of the expand).
-//  * Partial v = x.A of each CTA is summed across the cluster through
-//    distributed shared memory (fixed order, so every CTA holds identical v);
-//    v never leaves the chip in the fused mode.
-//  * One producer warp issues bulk (TMA) copies of A rows, gathered x rows,
-//    B row pieces and gathered y rows into a 4-stage shared-memory ring
-//    (16 KiB stages, mbarrier transaction counts); it runs ahead across items
-//    so the next item's A slab streams while the current item is expanded.
-//  * Four consumer warps: shrink with 16-byte A loads and fp32 FMAs, warp
-//    shuffle + shared-memory split-K reduction; expand with 16-byte B loads,
-//    a k-split over lanes reduced by shuffles, fp32 accumulate, one
-//    round-to-nearest-even bf16 store of y (16-byte stores).
+//  * One producer warp fills a shared-memory ring of 2-3 stages of 24-28 KiB
+//    (mbarrier transaction counts) with 2-D TMA tensor copies of the A rows
+//    (swizzled to the row width, so the fragment loads below are free of bank
+//    conflicts) and of the B block [r][columns], and with one bulk copy per
+//    token for the gathered x / y row pieces.  It runs ahead across items, so
+//    the next item's slabs stream while the current item is reduced.
+//  * Four consumer warps run warp-level tensor-core MMAs (m16n8k16, bf16 in,
+//    fp32 accumulate) with the tile's tokens as the M rows: the shrink splits
+//    the stage's k-steps over the warps, the warps' partial v are summed in
+//    shared memory, and each CTA pushes its partial v into every peer's shared
+//    memory with st.async (completing as transaction bytes on the peer's
+//    mbarrier) and sums the C partials in a fixed order, so every CTA holds
+//    the identical fp32 v, which never leaves the chip in the fused mode.  The
+//    expand takes v as a pair of bf16 MMA operands (v = hi + lo, hi = bf16(v),
+//    lo = bf16(v - hi); the pair carries 16 bits of v's mantissa), adds
+//    s * v.B to y in fp32 and stores y rounded once to bf16.
 //  * Persistent grid: as many clusters as are co-resident; cluster g takes
 //    items g, g+G, ... in tile-major order (all projections of a tile in a
 //    row), read from the device-side segmentation without a host round trip.
+//
+// Partial-v buffers are double-buffered by item parity and need no extra
+// synchronisation: a peer can push item j+2 only after it received our
+// partial of item j+1, which we send after we finished reading item j.
 //
 // Modes: shrink (v -> device memory), expand (v from device memory, no
 // cluster), fused (v on chip).
@@ -39,11 +49,28 @@
 
 namespace lsg {
 
+// Ring shape per rank (build-time knobs, chosen by measurement on B300):
+// ranks 8-32 use two 24 KiB stages, so that one CTA's share of a decode item
+// (A rows + B columns + x/y pieces) is in flight at once and three to four
+// CTAs share an SM; r = 64, whose CTAs registers hold to two per SM, keeps
+// three 28 KiB stages in flight.
+#ifndef LSG_CC_STAGES_SMALL
+#define LSG_CC_STAGES_SMALL 2
+#endif
+#ifndef LSG_CC_KB_SMALL
+#define LSG_CC_KB_SMALL 24
+#endif
+#ifndef LSG_CC_STAGES_BIG
+#define LSG_CC_STAGES_BIG 3
+#endif
+#ifndef LSG_CC_KB_BIG
+#define LSG_CC_KB_BIG 28
+#endif
 constexpr int kCW = 4;                 // consumer warps
 constexpr int kCThreads = kCW * 32;    // consumer threads
 constexpr int kThreads = kCThreads + 32;
-constexpr int kStages = 4;
-constexpr int kStageBytes = 16384;
+constexpr int kMaxC = 8;               // CTAs per cluster (portable limit)
+constexpr int kXB = 2;                 // partial-v exchange buffers
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
 enum : int { kStShrink = 1, kStExpand = 2, kStFirst = 4, kStLast = 8, kStEnd = 16 };
@@ -55,11 +82,15 @@ struct CCProj {
   uint16_t* y;
   int64_t ldx, ldy;
   int32_t h_in, h_out;
-  int32_t k_chunk, n_chunk;  // rows of A / columns of B per rank (multiples of 8)
+  int32_t k_chunk, n_chunk;  // rows of A / columns of B per rank (k_chunk: multiple of 16)
+  int32_t bw;                // TMA box width of B (columns, an odd multiple of 8)
+  int32_t nb;                // B boxes per expand stage
   float scale;
 };
 
-struct CCParams {
+// Everything but the tensor maps; copied to shared memory at kernel start so
+// that no later access waits on a constant-cache miss.
+struct CCTail {
   CCProj proj[kMaxProj];
   const int32_t* perm;
   const int32_t* seg_offsets;
@@ -75,16 +106,32 @@ struct CCParams {
   int32_t csplit;  // C
 };
 
+struct CCParams {
+  CUtensorMap tmA[kMaxProj];  // A_pool of projection p as 2-D [n_adapters*h_in][r], box {r, BA}
+  CUtensorMap tmB[kMaxProj];  // B_pool of projection p as 2-D [n_adapters*r][h_out], box {bw, r}
+  CCTail t;
+};
+
 template <int R, int T>
 struct CCCfg {
-  // rows (shrink) or columns (expand) per stage: A/B part + x/y part fit a stage
-  static constexpr int W = ((kStageBytes / ((R + T) * 2)) / 8) * 8;
-  static constexpr int kPartBytes = W * R * 2;
-  static constexpr int G = R / 8;           // shrink: 16-byte k-groups per A row
-  static constexpr int L = kCThreads / G;   // shrink: row lanes
-  static constexpr int KQ = R / 4;          // expand: lanes sharing one output vector (4 k each)
-  static_assert(W >= 8, "stage too small");
-  static_assert(kPartBytes + T * W * 2 <= kStageBytes, "stage overflow");
+  static constexpr int kStages = R >= 64 ? LSG_CC_STAGES_BIG : LSG_CC_STAGES_SMALL;
+  static constexpr int kStageBytes = (R >= 64 ? LSG_CC_KB_BIG : LSG_CC_KB_SMALL) * 1024;
+  // shrink: A rows per stage (A part + x part fit a stage), whole k-steps of
+  // 16, made of NBA TMA boxes of BA rows (a box extent is at most 256)
+  static constexpr int WS0 = (((kStageBytes - T * 16) / ((R + T) * 2)) / 16) * 16;
+  static constexpr int NBA = (WS0 + 255) / 256;
+  static constexpr int BA = ((WS0 / NBA) / 16) * 16;
+  static constexpr int WS = NBA * BA;
+  static constexpr int XP = WS + 8;              // x / y row pitch: an odd number of 16-byte chunks
+  static constexpr int kPartBytes = WS * R * 2;  // x / y part starts here
+  static constexpr int SWA = R >= 16 ? R * 2 : 0;  // A-part swizzle span in bytes (0: none)
+  static constexpr uint32_t SWM = SWA ? SWA / 16 - 1 : 0;
+  static constexpr int NT = R / 8;               // 8-rank n-tiles of the shrink
+  static constexpr int KS = R / 16;              // 16-rank k-steps of the expand (0 for r = 8)
+  static_assert(WS >= 16 && BA >= 16, "stage too small");
+  static_assert(kPartBytes + T * XP * 2 <= kStageBytes, "stage overflow");
+  static_assert(T * R % 4 == 0, "exchange layout");
+  static_assert(T <= 16, "one MMA row block");
 };
 
 template <int T>
@@ -92,122 +139,173 @@ struct StageHdr {
   int32_t kind;
   int32_t proj;
   int32_t tlen;
-  int32_t len;  // rows (shrink) or columns (expand) in this stage
-  int32_t off;  // first row / column
+  int32_t len;    // rows (shrink) or columns (expand) in this stage
+  int32_t off;    // first row / column
+  int32_t pitch;  // expand: box width (columns) of the B part
   int32_t tok[T];
 };
 
 template <int R, int T>
 struct CCSmem {
-  alignas(128) uint8_t ring[kStages][kStageBytes];
+  static constexpr int kStages = CCCfg<R, T>::kStages;
+  alignas(1024) uint8_t ring[kStages][CCCfg<R, T>::kStageBytes];
+  alignas(16) CCTail t;
   StageHdr<T> hdr[kStages];
   alignas(8) uint64_t full[kStages];
   uint64_t empty[kStages];
-  float red[kCW][T][R];
-  alignas(16) float vpart[T][R];
+  uint64_t xbar[kXB];
+  alignas(16) float red[kCW][T][R];
+  alignas(16) float xbuf[kXB][kMaxC][T][R];
   alignas(16) float vfull[T][R];
+  alignas(16) uint16_t zero_row[8];  // fragment rows past the tile's tokens read this
 };
-
-__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 t = __bfloat1622float2(h[i]);
-    f[2 * i] = t.x;
-    f[2 * i + 1] = t.y;
-  }
-}
-
-__device__ __forceinline__ float bf16_at(const uint16_t* p) {
-  return __uint_as_float(static_cast<uint32_t>(*p) << 16);
-}
 
 __device__ __forceinline__ void consumer_sync() { named_bar_sync(1, kCThreads); }
 
-// Locate token tile `tile` (tiles of <= T tokens, segment by segment) with a
-// forward-only cursor over the segments (tile indices a CTA visits only grow).
-// Executed by a full warp; returns false when `tile` is past the last tile.
-template <int T>
-__device__ bool find_tile(int& seg_base, int& tiles_before, int tile, int S, const int32_t* offs, int n,
-                          int lane, int& seg, int& t0, int& tlen) {
-  while (seg_base < S) {
-    const int s = seg_base + lane;
-    int off = 0, len = 0;
-    if (s < S) {
-      off = offs[s];
-      const int end = offs[s + 1];
-      len = (off >= 0 && end <= n && end >= off) ? end - off : 0;
-    }
-    const int tl = (len + T - 1) / T;
-    int inc = tl;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, inc, d);
-      if (lane >= d) inc += o;
-    }
-    const int total = __shfl_sync(0xffffffffu, inc, 31);
-    if (tile < tiles_before + total) {
-      const unsigned m = __ballot_sync(0xffffffffu, tiles_before + inc > tile);
-      const int Ls = __ffs(m) - 1;
-      const int excl = __shfl_sync(0xffffffffu, inc - tl, Ls);
-      const int o = __shfl_sync(0xffffffffu, off, Ls);
-      const int l = __shfl_sync(0xffffffffu, len, Ls);
-      seg = seg_base + Ls;
-      t0 = o + (tile - tiles_before - excl) * T;
-      tlen = min(T, o + l - t0);
-      return true;
-    }
-    tiles_before += total;
-    seg_base += 32;
-  }
-  return false;
+// TMA swizzle (16-byte chunk index XOR address bits 7..) of a shared-memory
+// byte address; SWM = span/16 - 1 (0: no swizzle).
+template <uint32_t SWM>
+__device__ __forceinline__ uint32_t swz(uint32_t addr) {
+  return addr ^ (((addr >> 7) & SWM) << 4);
 }
+
+__device__ __forceinline__ uint32_t ld_shared_u32(const void* p) {
+  return *reinterpret_cast<const uint32_t*>(p);
+}
+
+// bf16x2 {lo: a, hi: b} from two floats (round to nearest even)
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Cursor over the segments, 32 at a time (one per lane), finding token tile
+// `tile` (tiles of <= T tokens, segment by segment).  Tile indices a CTA asks
+// for only grow.  The first window is loaded together with num_segments, so
+// locating the first tile costs one round trip.  Executed by a full warp.
+template <int T>
+struct SegCursor {
+  int base = 0, tiles_before = 0, S = 0;
+  int off = 0, len = 0, ad = -1;  // segment base + lane
+
+  __device__ void load(const CCTail& q, int lane, int bound) {
+    const int s = base + lane;
+    off = 0;
+    len = 0;
+    ad = -1;
+    if (s < bound) {
+      const int o = q.seg_offsets[s];
+      const int e = q.seg_offsets[s + 1];
+      ad = q.seg_adapter[s];
+      off = o;
+      len = (o >= 0 && e <= q.n_tokens && e >= o) ? e - o : 0;
+    }
+  }
+
+  __device__ void init(const CCTail& q, int lane) {
+    const int s_raw = *q.num_segments;
+    load(q, lane, min(32, q.max_segments));  // speculative: issued alongside num_segments
+    S = min(max(s_raw, 0), q.max_segments);
+    if (lane >= S) len = 0;
+  }
+
+  __device__ bool find(const CCTail& q, int lane, int tile, int& t0, int& tlen, int& a) {
+    while (base < S) {
+      const int tl = (len + T - 1) / T;
+      int inc = tl;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, inc, d);
+        if (lane >= d) inc += o;
+      }
+      const int total = __shfl_sync(0xffffffffu, inc, 31);
+      if (tile < tiles_before + total) {
+        const unsigned m = __ballot_sync(0xffffffffu, tiles_before + inc > tile);
+        const int ls = __ffs(m) - 1;
+        const int excl = __shfl_sync(0xffffffffu, inc - tl, ls);
+        const int o = __shfl_sync(0xffffffffu, off, ls);
+        const int l = __shfl_sync(0xffffffffu, len, ls);
+        a = __shfl_sync(0xffffffffu, ad, ls);
+        t0 = o + (tile - tiles_before - excl) * T;
+        tlen = min(T, o + l - t0);
+        return true;
+      }
+      tiles_before += total;
+      base += 32;
+      load(q, lane, S);
+    }
+    return false;
+  }
+};
 
 template <int R, int T, int MODE>
 __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant__ CCParams p) {
   using Cfg = CCCfg<R, T>;
-  constexpr int W = Cfg::W;
+  constexpr int kStages = Cfg::kStages;
+  constexpr int WS = Cfg::WS;
+  constexpr int NT = Cfg::NT;
   constexpr bool kHasShrink = (MODE & kModeShrink) != 0;
   constexpr bool kHasExpand = (MODE & kModeExpand) != 0;
-  extern __shared__ __align__(128) uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   auto& sm = *reinterpret_cast<CCSmem<R, T>*>(smem_raw);
+  const CCTail& q = sm.t;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int C = p.csplit;
+  const int C = p.t.csplit;
   const int rank = static_cast<int>(blockIdx.x) % C;
   const int group = static_cast<int>(blockIdx.x) / C;
   const int ngroups = static_cast<int>(gridDim.x) / C;
-  const bool do_cluster = kHasShrink && C > 1;
+  const bool xchg = kHasShrink && C > 1;
 
+  // Per-call parameters to shared memory: every word in flight at once.
+  {
+    static_assert(sizeof(CCTail) % 4 == 0, "tail size");
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(&p.t);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.t);
+    for (int i = tid; i < static_cast<int>(sizeof(CCTail) / 4); i += kThreads) dst[i] = src[i];
+  }
+  if (warp == kCW && lane < kMaxProj) {
+    if (kHasShrink) prefetch_tmap(&p.tmA[lane]);
+    if (kHasExpand) prefetch_tmap(&p.tmB[lane]);
+  }
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], kCW);
     }
+    for (int b = 0; b < kXB; ++b) mbar_init(&sm.xbar[b], 1);
     fence_mbar_init();
   }
+  if (tid < 8) sm.zero_row[tid] = 0;
   __syncthreads();
+  // Our mbarriers exist before any peer pushes into this CTA: every thread
+  // arrives now and waits before its first push (or at the end).
+  if (xchg) cluster_arrive_relaxed();
   // The next launch may begin its prologue; it waits for our completion before
   // touching memory.  We wait for the launch that wrote the segmentation (and
   // v in the expand mode) before reading anything.
   pdl_launch_dependents();
   pdl_wait();
+  // The swizzle below is computed on absolute shared addresses, which agrees
+  // with the TMA's when the ring starts on a 1 KiB boundary (all CTAs alike).
+  const bool ring_ok = (smem_u32(sm.ring) & 1023u) == 0;
 
   if (warp == kCW) {
     // ============================== producer warp
     int slot = 0;
     uint32_t phase = 0;
-    bool any = false, failed = false;
-    const int S = min(max(*p.num_segments, 0), p.max_segments);
-    int seg_base = 0, tiles_before = 0;
-    int last_tile = -1, a = -1, t0 = 0, tlen = 0, tok = -1, ntok = 0;
-    bool tile_ok = false;
+    bool failed = !ring_ok;
+    if (!ring_ok && lane == 0) set_err(q.err_flag, LORA_ERR_UNSUPPORTED);
+    SegCursor<T> cur;
+    cur.init(q, lane);
+    int last_tile = -1, a = -1, t0 = 0, tlen = 0, tok = -1, ntok = 0, tk = -1;
+    bool tile_ok = false, tok_ready = false;
 
     auto acquire = [&]() -> bool {
       bool ok = true;
       if (lane == 0) ok = mbar_wait(&sm.empty[slot], phase ^ 1u, kWaitLimitNs);
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok && lane == 0) set_err(p.err_flag, LORA_ERR_TIMEOUT);
+      if (!ok && lane == 0) set_err(q.err_flag, LORA_ERR_TIMEOUT);
       return ok;
     };
     auto advance = [&]() {
@@ -216,147 +314,149 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
         phase ^= 1u;
       }
     };
+    // validate the tile's token indices (loaded when the tile was found)
+    auto resolve_tok = [&]() {
+      tok = tk;
+      if (lane < tlen && (tok < 0 || tok >= q.n_tokens)) {
+        set_err(q.err_flag, LORA_ERR_BAD_ADAPTER_ID);
+        tok = -1;
+      }
+      ntok = __popc(__ballot_sync(0xffffffffu, tok >= 0));
+      tok_ready = true;
+    };
+    auto header = [&](int kind, int pj, int len, int off, int pitch) {
+      StageHdr<T>& h = sm.hdr[slot];
+      if (lane < T) h.tok[lane] = tok;
+      if (lane == 0) {
+        h.kind = kind;
+        h.proj = pj;
+        h.tlen = tlen;
+        h.len = len;
+        h.off = off;
+        h.pitch = pitch;
+      }
+      __syncwarp();
+    };
 
     for (int item = group; !failed; item += ngroups) {
-      const int tile = item / p.n_proj;
-      const int pj = item - tile * p.n_proj;
+      const int tile = item / q.n_proj;
+      const int pj = item - tile * q.n_proj;
       if (tile != last_tile) {
-        int seg;
-        if (!find_tile<T>(seg_base, tiles_before, tile, S, p.seg_offsets, p.n_tokens, lane, seg, t0, tlen)) break;
+        if (!cur.find(q, lane, tile, t0, tlen, a)) break;
         last_tile = tile;
-        a = __shfl_sync(0xffffffffu, lane == 0 ? p.seg_adapter[seg] : 0, 0);
-        tok = -1;
-        if (lane < tlen) {
-          tok = p.perm[t0 + lane];
-          if (tok < 0 || tok >= p.n_tokens) {
-            set_err(p.err_flag, LORA_ERR_BAD_ADAPTER_ID);
-            tok = -1;
-          }
-        }
-        ntok = __popc(__ballot_sync(0xffffffffu, tok >= 0));
-        tile_ok = (a >= 0 && a < p.n_adapters);
-        if (!tile_ok && lane == 0) set_err(p.err_flag, LORA_ERR_BAD_ADAPTER_ID);
+        tk = -1;
+        if (lane < tlen) tk = q.perm[t0 + lane];  // consumed after the first A copy is issued
+        tok_ready = false;
+        tile_ok = (a >= 0 && a < q.n_adapters);
+        if (!tile_ok && lane == 0) set_err(q.err_flag, LORA_ERR_BAD_ADAPTER_ID);
       }
       if (!tile_ok) continue;  // every CTA of the cluster skips it alike
-      const CCProj& pr = p.proj[pj];
+      const CCProj& pr = q.proj[pj];
 
       if (kHasShrink) {
-        if (do_cluster) {
-          if (any) cluster_wait_acquire();  // peers finished reading the previous partial v
-          cluster_arrive_relaxed();
-        }
         const int k0 = rank * pr.k_chunk;
         const int klen = max(0, min(pr.h_in, k0 + pr.k_chunk) - k0);
-        const int nst = max(1, (klen + W - 1) / W);
-        const int per = ((klen + nst - 1) / nst + 7) & ~7;
-        const uint16_t* Aslab = pr.A + static_cast<int64_t>(a) * pr.h_in * R;
-        for (int st = 0; st < nst && !failed; ++st) {
+        const int nst = max(1, (klen + WS - 1) / WS);
+        const int per = ((klen + nst - 1) / nst + 15) & ~15;
+        const int arow = a * pr.h_in;  // first pool row of the adapter
+        for (int st = 0; st < nst; ++st) {
           const int r0 = k0 + st * per;
           const int rl = max(0, min(per, k0 + klen - r0));
+          const int nbx = (rl + Cfg::BA - 1) / Cfg::BA;  // A boxes in this stage
           if (!acquire()) {
             failed = true;
             break;
           }
-          StageHdr<T>& h = sm.hdr[slot];
-          if (lane < T) h.tok[lane] = tok;
-          if (lane == 0) {
-            h.kind = kStShrink | (st == 0 ? kStFirst : 0) | (st == nst - 1 ? kStLast : 0);
-            h.proj = pj;
-            h.tlen = tlen;
-            h.len = rl;
-            h.off = r0;
-          }
-          __syncwarp();
-          const uint32_t bytes = static_cast<uint32_t>(rl) * 2u * (R + ntok);
-          if (lane == 0) {
-            if (bytes) mbar_arrive_expect_tx(&sm.full[slot], bytes);
-            else mbar_arrive(&sm.full[slot]);
-          }
-          __syncwarp();
-          if (rl > 0) {
-            uint8_t* st_base = sm.ring[slot];
-            if (lane == 0) bulk_g2s(st_base, Aslab + static_cast<int64_t>(r0) * R, rl * R * 2, &sm.full[slot]);
-            if (tok >= 0)
-              bulk_g2s(st_base + Cfg::kPartBytes + lane * W * 2, pr.x + static_cast<int64_t>(tok) * pr.ldx + r0,
-                       rl * 2, &sm.full[slot]);
-          }
+          uint8_t* st_base = sm.ring[slot];
+          if (lane == 0 && nbx) mbar_expect_tx(&sm.full[slot], static_cast<uint32_t>(nbx) * Cfg::BA * R * 2u);
+          if (lane < nbx)
+            tma_load_2d(st_base + lane * Cfg::BA * R * 2, &p.tmA[pj], 0, arow + r0 + lane * Cfg::BA,
+                        &sm.full[slot]);
+          if (!tok_ready) resolve_tok();
+          header(kStShrink | (st == 0 ? kStFirst : 0) | (st == nst - 1 ? kStLast : 0), pj, rl, r0, 0);
+          if (lane == 0) mbar_arrive_expect_tx(&sm.full[slot], static_cast<uint32_t>(rl) * 2u * ntok);
+          if (rl > 0 && tok >= 0)
+            bulk_g2s(st_base + Cfg::kPartBytes + lane * Cfg::XP * 2, pr.x + static_cast<int64_t>(tok) * pr.ldx + r0,
+                     rl * 2, &sm.full[slot]);
           advance();
         }
       }
       if (kHasExpand && !failed) {
         const int c0 = rank * pr.n_chunk;
         const int clen = max(0, min(pr.h_out, c0 + pr.n_chunk) - c0);
-        const int nst = (clen + W - 1) / W;
-        const int per = nst ? ((clen + nst - 1) / nst + 7) & ~7 : 0;
-        const uint16_t* Bslab = pr.B + static_cast<int64_t>(a) * R * pr.h_out;
+        const int bw = pr.bw;
+        const int sc = bw * pr.nb;  // columns per stage
+        const int nst = (clen + sc - 1) / sc;
+        if (!tok_ready) resolve_tok();
         for (int st = 0; st < nst; ++st) {
-          const int cc = c0 + st * per;
-          const int cl = max(0, min(per, c0 + clen - cc));
+          const int cc = c0 + st * sc;
+          const int cl = min(sc, c0 + clen - cc);
+          const int nbs = (cl + bw - 1) / bw;  // boxes in this stage
           if (!acquire()) {
             failed = true;
             break;
           }
-          StageHdr<T>& h = sm.hdr[slot];
-          if (lane < T) h.tok[lane] = tok;
-          if (lane == 0) {
-            h.kind = kStExpand | (st == 0 ? kStFirst : 0) | (st == nst - 1 ? kStLast : 0);
-            h.proj = pj;
-            h.tlen = tlen;
-            h.len = cl;
-            h.off = cc;
-          }
-          __syncwarp();
-          const uint32_t bytes = static_cast<uint32_t>(cl) * 2u * (R + ntok);
-          if (lane == 0) {
-            if (bytes) mbar_arrive_expect_tx(&sm.full[slot], bytes);
-            else mbar_arrive(&sm.full[slot]);
-          }
-          __syncwarp();
-          if (cl > 0) {
-            uint8_t* st_base = sm.ring[slot];
-            for (int k = lane; k < R; k += 32)
-              bulk_g2s(st_base + k * W * 2, Bslab + static_cast<int64_t>(k) * pr.h_out + cc, cl * 2,
-                       &sm.full[slot]);
-            if (tok >= 0)
-              bulk_g2s(st_base + Cfg::kPartBytes + lane * W * 2, pr.y + static_cast<int64_t>(tok) * pr.ldy + cc,
-                       cl * 2, &sm.full[slot]);
-          }
+          uint8_t* st_base = sm.ring[slot];
+          if (lane == 0) mbar_expect_tx(&sm.full[slot], static_cast<uint32_t>(nbs) * bw * R * 2u);
+          if (lane < nbs)
+            tma_load_2d(st_base + lane * bw * R * 2, &p.tmB[pj], cc + lane * bw, a * R, &sm.full[slot]);
+          header(kStExpand | (st == 0 ? kStFirst : 0) | (st == nst - 1 ? kStLast : 0), pj, cl, cc, bw);
+          if (lane == 0) mbar_arrive_expect_tx(&sm.full[slot], static_cast<uint32_t>(cl) * 2u * ntok);
+          if (tok >= 0)
+            bulk_g2s(st_base + Cfg::kPartBytes + lane * Cfg::XP * 2, pr.y + static_cast<int64_t>(tok) * pr.ldy + cc,
+                     cl * 2, &sm.full[slot]);
           advance();
         }
       }
-      if (do_cluster && !failed) {
-        cluster_wait_acquire();   // all shrink partials of this item are published
-        cluster_arrive_relaxed(); // (ours: nothing to publish)
-      }
-      any = true;
     }
     if (!failed && acquire()) {
       if (lane == 0) {
         sm.hdr[slot].kind = kStEnd;
         mbar_arrive(&sm.full[slot]);
       }
+    } else if (!ring_ok) {
+      // nothing was issued: tell the consumers to stop
+      if (lane == 0) {
+        sm.hdr[0].kind = kStEnd;
+        mbar_arrive(&sm.full[0]);
+      }
     }
-    if (do_cluster && any) cluster_wait_acquire();
+    if (xchg) {
+      cluster_wait_acquire();   // start barrier
+      cluster_arrive_relaxed();  // end barrier: no CTA leaves while a peer may still push to it
+      cluster_wait_acquire();
+    }
     return;
   }
 
   // ============================== consumer warps
   const int ct = tid;  // 0 .. kCThreads-1
+  const int g = lane >> 2, tig = lane & 3;  // MMA fragment coordinates
+  const int lm = lane >> 3, lr = lane & 7;  // ldmatrix: matrix lm, row lr of it
   int slot = 0;
   uint32_t phase = 0;
-  bool any = false;
-  float acc[T][8];
+  int nx = 0;  // partial-v exchanges done
+  bool start_waited = false;
+  float acc[NT][4];  // this warp's partial v: rows g, g+8 of every 8-rank n-tile
+  // expand operands: v as bf16 hi/lo MMA A fragments (per 16-rank k-step)
+  constexpr int KSA = Cfg::KS > 0 ? Cfg::KS : 1;
+  uint32_t vah[KSA][4], val[KSA][4];
+  uint32_t v8h[2] = {0u, 0u}, v8l[2] = {0u, 0u};  // r = 8: one m16n8k8 A fragment
 #pragma unroll
-  for (int t = 0; t < T; ++t)
+  for (int ks = 0; ks < KSA; ++ks)
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[t][e] = 0.f;
+    for (int e = 0; e < 4; ++e) vah[ks][e] = val[ks][e] = 0u;
+#pragma unroll
+  for (int n = 0; n < NT; ++n)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
 
   for (;;) {
     bool ok = true;
     if (lane == 0) ok = mbar_wait(&sm.full[slot], phase, kWaitLimitNs);
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok) {
-      if (lane == 0) set_err(p.err_flag, LORA_ERR_TIMEOUT);
+      if (lane == 0) set_err(q.err_flag, LORA_ERR_TIMEOUT);
       return;
     }
     const StageHdr<T>& h = sm.hdr[slot];
@@ -366,140 +466,292 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
     const uint8_t* st_base = sm.ring[slot];
 
     if (kind & kStShrink) {
+      const int b = nx & 1;
       if (kind & kStFirst) {
 #pragma unroll
-        for (int t = 0; t < T; ++t)
+        for (int n = 0; n < NT; ++n)
 #pragma unroll
-          for (int e = 0; e < 8; ++e) acc[t][e] = 0.f;
+          for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
+        if (xchg && ct == 0)
+          mbar_arrive_expect_tx(&sm.xbar[b], static_cast<uint32_t>(C - 1) * T * R * 4u);
       }
-      const int g = ct % Cfg::G, l = ct / Cfg::G;
-      const uint16_t* As = reinterpret_cast<const uint16_t*>(st_base);
-      const uint16_t* Xs = reinterpret_cast<const uint16_t*>(st_base + Cfg::kPartBytes);
-      for (int j = l; j < len; j += Cfg::L) {
-        const uint4 av = *reinterpret_cast<const uint4*>(As + j * R + g * 8);
-        float af[8];
-        unpack8(av, af);
-#pragma unroll
-        for (int t = 0; t < T; ++t) {
-          if (t < tlen) {
-            const float xv = bf16_at(Xs + t * W + j);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[t][e] = fmaf(xv, af[e], acc[t][e]);
-          }
-        }
-      }
-      if (kind & kStLast) {
-        // ---- reduce partial v over this CTA: lanes (same g), then warps
-#pragma unroll
-        for (int t = 0; t < T; ++t) {
-          if (t < tlen) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              float v = acc[t][e];
-#pragma unroll
-              for (int o = Cfg::G; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-              acc[t][e] = v;
-            }
-          }
-        }
-        if (lane < Cfg::G) {
-#pragma unroll
-          for (int t = 0; t < T; ++t)
-            if (t < tlen)
-#pragma unroll
-              for (int e = 0; e < 8; ++e) sm.red[warp][t][lane * 8 + e] = acc[t][e];
-        }
-        if (do_cluster && any) cluster_wait_acquire();  // peers done reading our previous vpart
-        consumer_sync();
-        for (int idx = ct; idx < tlen * R; idx += kCThreads) {
-          const int t = idx / R, k = idx % R;
-          float s = 0.f;
-#pragma unroll
-          for (int w = 0; w < kCW; ++w) s += sm.red[w][t][k];
-          sm.vpart[t][k] = s;
-        }
-        consumer_sync();
-        if (do_cluster) {
-          cluster_arrive_release();
-          cluster_wait_acquire();
-          const uint32_t base = smem_u32(&sm.vpart[0][0]);
-          for (int idx = ct; idx < tlen * R; idx += kCThreads) {
-            float s = 0.f;
-            for (int q = 0; q < C; ++q) s += ld_dsmem_f32(mapa_shared(base + idx * 4, q));
-            (&sm.vfull[0][0])[idx] = s;
-          }
-          consumer_sync();
-          cluster_arrive_relaxed();
+      // ---- v[t, :] += x[t, k-range] . A[k-range, :]  (tokens = MMA rows)
+      const uint32_t a_base = smem_u32(st_base);
+      const uint32_t x_base = a_base + Cfg::kPartBytes;
+      const int nk16 = len >> 4;
+      // x fragment (A operand): lane L gives row (L/8 & 1)*8 + L%8, k offset (L/16)*8 of the
+      // 16x16 block; rows past the tile read the zero row
+      const int xrow = (lm & 1) * 8 + lr;
+      const uint32_t xaddr0 = xrow < tlen ? x_base + static_cast<uint32_t>(xrow * Cfg::XP + (lm >> 1) * 8) * 2
+                                          : smem_u32(sm.zero_row);
+      const uint32_t xstep = xrow < tlen ? 32u : 0u;  // bytes per k-step of 16
+      // A fragment (B operand, swizzled rows of R ranks): per-lane offset, independent of the k-step
+      const int krow = (lm & 1) * 8 + lr;
+      auto step = [&](int ks, float (&ac)[NT][4]) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(xaddr0 + static_cast<uint32_t>(ks) * xstep, a0, a1, a2, a3);
+        const uint32_t kbase = a_base + static_cast<uint32_t>(ks) * (16 * R * 2);
+        if constexpr (NT == 1) {
+          // r = 8: matrices (k 0-7), (k 8-15) of the single n-tile; lanes 16+ repeat 0-15
+          uint32_t b0, b1;
+          ldsm_x2_trans(kbase + static_cast<uint32_t>(krow) * (R * 2), b0, b1);
+          mma_bf16_16816(ac[0], a0, a1, a2, a3, b0, b1);
         } else {
-          for (int idx = ct; idx < tlen * R; idx += kCThreads) (&sm.vfull[0][0])[idx] = (&sm.vpart[0][0])[idx];
-          consumer_sync();
+#pragma unroll
+          for (int np = 0; np < NT / 2; ++np) {
+            // matrices: (k 0-7, n 0-7), (k 8-15, n 0-7), (k 0-7, n 8-15), (k 8-15, n 8-15) of the pair
+            const uint32_t off = swz<Cfg::SWM>(static_cast<uint32_t>(krow) * (R * 2) +
+                                               static_cast<uint32_t>(np * 16 + (lm >> 1) * 8) * 2);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_trans(kbase + off, b0, b1, b2, b3);
+            mma_bf16_16816(ac[2 * np], a0, a1, a2, a3, b0, b1);
+            mma_bf16_16816(ac[2 * np + 1], a0, a1, a2, a3, b2, b3);
+          }
         }
-        any = true;
+      };
+      {
+        // two k-steps per iteration into independent accumulators (overlaps the MMA latency)
+        float ac2[NT][4];
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) ac2[n][e] = 0.f;
+        int ks = warp;
+        for (; ks + kCW < nk16; ks += 2 * kCW) {
+          step(ks, acc);
+          step(ks + kCW, ac2);
+        }
+        if (ks < nk16) step(ks, acc);
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[n][e] += ac2[n][e];
+      }
+      if ((len & 8) && warp == (nk16 % kCW)) {
+        // tail of 8 rows (h_in is a multiple of 8): m16n8k8
+        const int kb = nk16 * 16;
+        const uint16_t* Xs = reinterpret_cast<const uint16_t*>(st_base + Cfg::kPartBytes);
+        const uint32_t a0 = g < tlen ? ld_shared_u32(Xs + g * Cfg::XP + kb + 2 * tig) : 0u;
+        const uint32_t a1 = g + 8 < tlen ? ld_shared_u32(Xs + (g + 8) * Cfg::XP + kb + 2 * tig) : 0u;
+        if constexpr (NT == 1) {
+          uint32_t b0, b1;  // b1 (lanes 8-15's rows) is not used
+          ldsm_x2_trans(a_base + static_cast<uint32_t>(kb + lr) * (R * 2), b0, b1);
+          mma_bf16_1688(acc[0], a0, a1, b0);
+        } else {
+#pragma unroll
+          for (int np = 0; np < NT / 2; ++np) {
+            // matrices: (k 0-7, n 0-7), (k 0-7, n 8-15) of the pair
+            const uint32_t addr = swz<Cfg::SWM>(a_base + static_cast<uint32_t>(kb + lr) * (R * 2) +
+                                                static_cast<uint32_t>(np * 16 + (lm & 1) * 8) * 2);
+            uint32_t b0, b1;
+            ldsm_x2_trans(addr, b0, b1);
+            mma_bf16_1688(acc[2 * np], a0, a1, b0);
+            mma_bf16_1688(acc[2 * np + 1], a0, a1, b1);
+          }
+        }
+      }
+      if (!(kind & kStLast)) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[slot]);  // header and data of this slot no longer read
+      } else {
+        // the slot is released before the exchange, so the producer keeps streaming
+        int tokr[T];
+#pragma unroll
+        for (int t = 0; t < T; ++t) tokr[t] = h.tok[t];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[slot]);
+        // ---- this warp's partial v to shared memory, then the sum over warps
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          if (g < T) {
+            sm.red[warp][g][n * 8 + 2 * tig] = acc[n][0];
+            sm.red[warp][g][n * 8 + 2 * tig + 1] = acc[n][1];
+          }
+          if (g + 8 < T) {
+            sm.red[warp][g + 8][n * 8 + 2 * tig] = acc[n][2];
+            sm.red[warp][g + 8][n * 8 + 2 * tig + 1] = acc[n][3];
+          }
+        }
+        consumer_sync();
+        constexpr int kV4 = T * R / 4;  // float4 elements of one partial v
+        auto red_sum = [&](int i) {
+          float4 vp = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int w = 0; w < kCW; ++w) {
+            const float4 u = reinterpret_cast<const float4*>(&sm.red[w][0][0])[i];
+            vp.x += u.x;
+            vp.y += u.y;
+            vp.z += u.z;
+            vp.w += u.w;
+          }
+          return vp;
+        };
+        if (xchg) {
+          if (!start_waited) {
+            cluster_wait_acquire();  // every peer's mbarriers are initialised
+            start_waited = true;
+          }
+          const uint32_t bar = smem_u32(&sm.xbar[b]);
+          for (int i = ct; i < kV4; i += kCThreads) {
+            const float4 vp = red_sum(i);
+            reinterpret_cast<float4*>(&sm.xbuf[b][rank][0][0])[i] = vp;
+            const uint32_t src = smem_u32(&sm.xbuf[b][rank][0][0]) + i * 16;
+            for (int qq = 0; qq < C; ++qq)
+              if (qq != rank) st_async_v4(mapa_shared(src, qq), vp, mapa_shared(bar, qq));
+          }
+          bool got = true;
+          if (lane == 0) got = mbar_wait(&sm.xbar[b], (nx >> 1) & 1, kWaitLimitNs);
+          got = __shfl_sync(0xffffffffu, got, 0);
+          if (!got) {
+            if (lane == 0) set_err(q.err_flag, LORA_ERR_TIMEOUT);
+            return;
+          }
+          consumer_sync();  // our own partial (plain stores) is visible to every consumer
+          for (int i = ct; i < kV4; i += kCThreads) {
+            float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int qq = 0; qq < C; ++qq) {  // fixed order: identical v in every CTA
+              const float4 u = reinterpret_cast<const float4*>(&sm.xbuf[b][qq][0][0])[i];
+              sum.x += u.x;
+              sum.y += u.y;
+              sum.z += u.z;
+              sum.w += u.w;
+            }
+            reinterpret_cast<float4*>(&sm.vfull[0][0])[i] = sum;
+          }
+        } else {
+          for (int i = ct; i < kV4; i += kCThreads) reinterpret_cast<float4*>(&sm.vfull[0][0])[i] = red_sum(i);
+        }
+        consumer_sync();
+        ++nx;
         if (MODE == kModeShrink && rank == 0) {
           for (int idx = ct; idx < tlen * R; idx += kCThreads) {
             const int t = idx / R, k = idx % R;
-            const int tk = h.tok[t];
-            if (tk >= 0) p.v_out[static_cast<int64_t>(tk) * R + k] = sm.vfull[t][k];
+            int tkv = -1;
+#pragma unroll
+            for (int u = 0; u < T; ++u)
+              if (u == t) tkv = tokr[u];
+            if (tkv >= 0) q.v_out[static_cast<int64_t>(tkv) * R + k] = sm.vfull[t][k];
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.empty[slot]);  // header and data of this slot no longer read
     } else {
       // ---- expand stage: y[tok, off .. off+len) += s * vfull[t] . B[:, off .. off+len)
-      if (MODE == kModeExpand && (kind & kStFirst)) {
-        consumer_sync();  // every warp is done with the previous item's v
-        for (int idx = ct; idx < tlen * R; idx += kCThreads) {
-          const int t = idx / R, k = idx % R;
-          const int tk = h.tok[t];
-          sm.vfull[t][k] = tk >= 0 ? p.v_in[static_cast<int64_t>(tk) * R + k] : 0.f;
+      if (kind & kStFirst) {
+        if (MODE == kModeExpand) {
+          consumer_sync();  // every warp is done with the previous item's v
+          for (int idx = ct; idx < T * R; idx += kCThreads) {
+            const int t = idx / R, k = idx % R;
+            const int tk = t < tlen ? h.tok[t] : -1;
+            sm.vfull[t][k] = tk >= 0 ? q.v_in[static_cast<int64_t>(tk) * R + k] : 0.f;
+          }
+          consumer_sync();
         }
-        consumer_sync();
+        // v as bf16 hi/lo MMA A fragments (rows >= tlen are zero)
+        auto split = [&](int row, int col, uint32_t& hi, uint32_t& lo) {
+          const bool ok = row < tlen;
+          const float x0 = ok ? sm.vfull[row][col] : 0.f, x1 = ok ? sm.vfull[row][col + 1] : 0.f;
+          hi = pack_bf16(x0, x1);
+          const float2 hf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi));
+          lo = pack_bf16(x0 - hf.x, x1 - hf.y);
+        };
+        if constexpr (Cfg::KS == 0) {
+          split(g, 2 * tig, v8h[0], v8l[0]);
+          split(g + 8, 2 * tig, v8h[1], v8l[1]);
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < Cfg::KS; ++ks) {
+            split(g, ks * 16 + 2 * tig, vah[ks][0], val[ks][0]);
+            split(g + 8, ks * 16 + 2 * tig, vah[ks][1], val[ks][1]);
+            split(g, ks * 16 + 8 + 2 * tig, vah[ks][2], val[ks][2]);
+            split(g + 8, ks * 16 + 8 + 2 * tig, vah[ks][3], val[ks][3]);
+          }
+        }
       }
-      const CCProj& pr = p.proj[pj];
-      const uint16_t* Bs = reinterpret_cast<const uint16_t*>(st_base);
-      const uint16_t* Ys = reinterpret_cast<const uint16_t*>(st_base + Cfg::kPartBytes);
-      const int nv = len >> 3;
-      const int units = nv * tlen * Cfg::KQ;
-      for (int ub = warp * 32; ub < units; ub += kCThreads) {
-        const int u = ub + lane;
-        const bool act = u < units;
-        const int kq = u % Cfg::KQ;
-        const int rest = u / Cfg::KQ;
-        const int cv = act ? rest % nv : 0;
-        const int t = act ? rest / nv : 0;
-        float o[8];
+      const CCProj& pr = q.proj[pj];
+      const float scale = pr.scale;
+      uint16_t* const yg = pr.y;
+      const int64_t ldy = pr.ldy;
+      const int bw = h.pitch;  // box width (columns) of the B part; box = [R][bw]
+      const uint32_t b_base = smem_u32(st_base);
+      uint16_t* const Ys = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(st_base) + Cfg::kPartBytes);
+      const int ntl = len >> 3;  // 8-column n-tiles in the stage
+      const int tpb = bw >> 3;   // n-tiles per box (odd)
+      const uint32_t mtpb = 65536u / static_cast<uint32_t>(tpb) + 1u;  // i / tpb == (i * mtpb) >> 16 here
+      // element offset in the B part of column 0 of n-tile i (box-major layout [box][R][bw])
+      auto tile_off = [&](int i) -> int {
+        const int bx = static_cast<int>((static_cast<uint32_t>(i) * mtpb) >> 16);
+        return bx * (R * bw) + (i - bx * tpb) * 8;
+      };
+      // y += s * products, in place in the stage's y rows (rows g, g+8 of a tile pair)
+      auto upd = [&](int row, int col, float e0, float e1) {
+        uint32_t* yp = reinterpret_cast<uint32_t*>(Ys + row * Cfg::XP + col);
+        const float2 yf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(yp));
+        *yp = pack_bf16(yf.x + scale * e0, yf.y + scale * e1);
+      };
+      auto pair = [&](int j, float (&d0)[4], float (&d1)[4]) {
+        // n-tiles j and j+1 (a missing second tile repeats the first)
+        const int oa = tile_off(j), ob = j + 1 < ntl ? tile_off(j + 1) : oa;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = 0.f;
-        if (act) {
+        for (int e = 0; e < 4; ++e) d0[e] = d1[e] = 0.f;
+        if constexpr (Cfg::KS == 0) {
+          // r = 8: matrices (k 0-7, tile a), (k 0-7, tile b); lanes 16+ repeat 0-15
+          const int o = (lm & 1) ? ob : oa;
+          uint32_t b0, b1;
+          ldsm_x2_trans(b_base + static_cast<uint32_t>(o + lr * bw) * 2, b0, b1);
+          mma_bf16_1688(d0, v8h[0], v8h[1], b0);
+          mma_bf16_1688(d0, v8l[0], v8l[1], b0);
+          mma_bf16_1688(d1, v8h[0], v8h[1], b1);
+          mma_bf16_1688(d1, v8l[0], v8l[1], b1);
+        } else {
+          const int o = (lm >> 1) ? ob : oa;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const int k = kq * 4 + kk;
-            const uint4 bv = *reinterpret_cast<const uint4*>(Bs + k * W + cv * 8);
-            float bf[8];
-            unpack8(bv, bf);
-            const float vv = sm.vfull[t][k];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = fmaf(vv, bf[e], o[e]);
+          for (int ks = 0; ks < Cfg::KS; ++ks) {
+            // matrices: (k 0-7, a), (k 8-15, a), (k 0-7, b), (k 8-15, b)
+            const int krow = ks * 16 + (lm & 1) * 8 + lr;
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_trans(b_base + static_cast<uint32_t>(o + krow * bw) * 2, b0, b1, b2, b3);
+            mma_bf16_16816(d0, vah[ks][0], vah[ks][1], vah[ks][2], vah[ks][3], b0, b1);
+            mma_bf16_16816(d0, val[ks][0], val[ks][1], val[ks][2], val[ks][3], b0, b1);
+            mma_bf16_16816(d1, vah[ks][0], vah[ks][1], vah[ks][2], vah[ks][3], b2, b3);
+            mma_bf16_16816(d1, val[ks][0], val[ks][1], val[ks][2], val[ks][3], b2, b3);
           }
         }
-#pragma unroll
-        for (int s = 1; s < Cfg::KQ; s <<= 1)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) o[e] += __shfl_xor_sync(0xffffffffu, o[e], s);
-        if (act && kq == 0) {
-          const int tk = h.tok[t];
-          if (tk >= 0) {
-            const uint4 yv = *reinterpret_cast<const uint4*>(Ys + t * W + cv * 8);
-            float yf[8];
-            unpack8(yv, yf);
-            uint4 outv;
-            __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&outv);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              ob[i] = __floats2bfloat162_rn(yf[2 * i] + pr.scale * o[2 * i], yf[2 * i + 1] + pr.scale * o[2 * i + 1]);
-            *reinterpret_cast<uint4*>(pr.y + static_cast<int64_t>(tk) * pr.ldy + off + cv * 8) = outv;
-          }
+      };
+      auto store = [&](int j, const float (&d0)[4], const float (&d1)[4]) {
+        const bool has_b = j + 1 < ntl;
+        const int col_a = 8 * j + 2 * tig, col_b = col_a + 8;
+        if (g < tlen) {
+          upd(g, col_a, d0[0], d0[1]);
+          if (has_b) upd(g, col_b, d1[0], d1[1]);
+        }
+        if (g + 8 < tlen) {
+          upd(g + 8, col_a, d0[2], d0[3]);
+          if (has_b) upd(g + 8, col_b, d1[2], d1[3]);
+        }
+      };
+      // this warp's tile pairs: j = 2*warp + 2*kCW*i, two pairs per iteration
+      int j = 2 * warp;
+      for (; j + 2 * kCW < ntl; j += 4 * kCW) {
+        float d0[4], d1[4], d2[4], d3[4];
+        pair(j, d0, d1);
+        pair(j + 2 * kCW, d2, d3);
+        store(j, d0, d1);
+        store(j + 2 * kCW, d2, d3);
+      }
+      if (j < ntl) {
+        float d0[4], d1[4];
+        pair(j, d0, d1);
+        store(j, d0, d1);
+      }
+      fence_proxy_async_smem();  // our y updates, visible to the bulk stores below
+      consumer_sync();
+      // ---- the tile's updated y rows back to global memory, one bulk copy per token
+      if (ct < tlen) {
+        const int tkv = h.tok[ct];
+        if (tkv >= 0) {
+          bulk_s2g(yg + static_cast<int64_t>(tkv) * ldy + off, Ys + ct * Cfg::XP, static_cast<uint32_t>(len) * 2u);
+          bulk_commit();
+          bulk_wait_read0();  // the slot may be refilled once the copy has read it
         }
       }
       __syncwarp();
@@ -510,7 +762,12 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
       phase ^= 1u;
     }
   }
-  if (do_cluster && any) cluster_wait_acquire();
+  if (ct < T) bulk_wait0();  // our y stores have landed
+  if (xchg) {
+    if (!start_waited) cluster_wait_acquire();
+    cluster_arrive_relaxed();
+    cluster_wait_acquire();
+  }
 }
 
 // ------------------------------------------------------------------ host side
@@ -522,14 +779,53 @@ struct KernelInfo {
 };
 
 template <int R, int T, int MODE>
-lora_status launch_rtm(const CCParams& prm, int items_bound, cudaStream_t stream) {
+lora_status launch_rtm(CCParams& prm, int items_bound, cudaStream_t stream) {
+  using Cfg = CCCfg<R, T>;
   auto kern = sgmv_cc_kernel<R, T, MODE>;
   const size_t smem = sizeof(CCSmem<R, T>);
-  const int C = prm.csplit;
+  const int C = prm.t.csplit;
   const bool cluster = (MODE & kModeShrink) && C > 1;
 
+  for (int i = 0; i < prm.t.n_proj; ++i) {
+    CCProj& q = prm.t.proj[i];
+    if (MODE & kModeShrink) {
+      const uint64_t dims[2] = {static_cast<uint64_t>(R), static_cast<uint64_t>(prm.t.n_adapters) * q.h_in};
+      const uint64_t strides[1] = {static_cast<uint64_t>(R) * 2};
+      const uint32_t box[2] = {static_cast<uint32_t>(R), static_cast<uint32_t>(Cfg::BA)};
+      const lora_status s = encode_tmap_bf16(&prm.tmA[i], q.A, 2, dims, strides, box, Cfg::SWA);
+      if (s != LORA_OK) return s;
+    }
+    if (MODE & kModeExpand) {
+      // stage = nb boxes of bw columns, nb*bw <= WS; bw <= 256 (the TMA box
+      // limit) and an odd multiple of 8 (16-byte chunks), which puts the 8 rows
+      // an ldmatrix reads into different banks.  Fewest boxes that cover a
+      // stage's share of the chunk.
+      const int nst = std::max(1, ceil_div(q.n_chunk, Cfg::WS));
+      const int pe = round_up(ceil_div(q.n_chunk, nst), 8);
+      q.nb = 0;
+      for (int nb = 1; nb <= 16 && q.nb == 0; ++nb) {
+        int bw = round_up(ceil_div(pe, nb), 8);
+        if ((bw / 8) % 2 == 0) bw += 8;
+        if (bw <= 256 && nb * bw <= Cfg::WS) {
+          q.nb = nb;
+          q.bw = bw;
+        }
+      }
+      if (q.nb == 0) {  // covering is impossible within WS: largest odd box that fits
+        q.nb = 1;
+        q.bw = std::min(256, Cfg::WS) / 8 * 8;
+        if ((q.bw / 8) % 2 == 0) q.bw -= 8;
+      }
+      const uint64_t dims[2] = {static_cast<uint64_t>(q.h_out), static_cast<uint64_t>(prm.t.n_adapters) * R};
+      const uint64_t strides[1] = {static_cast<uint64_t>(q.h_out) * 2};
+      const uint32_t box[2] = {static_cast<uint32_t>(q.bw), static_cast<uint32_t>(R)};
+      const lora_status s = encode_tmap_bf16(&prm.tmB[i], q.B, 2, dims, strides, box, 0);
+      if (s != LORA_OK) return s;
+    }
+  }
+
   static std::mutex mu;
-  static KernelInfo info[64][17];
+  static KernelInfo info[64][kMaxC + 1];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
   KernelInfo ki;
@@ -540,8 +836,6 @@ lora_status launch_rtm(const CCParams& prm, int items_bound, cudaStream_t stream
   if (ki.max_groups == 0) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess)
-      return LORA_ERR_CUDA;
-    if (C > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
       return LORA_ERR_CUDA;
     if (cluster) {
       cudaLaunchConfig_t cfg{};
@@ -593,7 +887,7 @@ lora_status launch_rtm(const CCParams& prm, int items_bound, cudaStream_t stream
 }
 
 template <int R, int T>
-lora_status dispatch_mode(Mode m, const CCParams& prm, int items_bound, cudaStream_t st) {
+lora_status dispatch_mode(Mode m, CCParams& prm, int items_bound, cudaStream_t st) {
   switch (m) {
     case kModeShrink: return launch_rtm<R, T, kModeShrink>(prm, items_bound, st);
     case kModeExpand: return launch_rtm<R, T, kModeExpand>(prm, items_bound, st);
@@ -602,7 +896,7 @@ lora_status dispatch_mode(Mode m, const CCParams& prm, int items_bound, cudaStre
 }
 
 template <int T>
-lora_status dispatch_r(int r, Mode m, const CCParams& prm, int items_bound, cudaStream_t st) {
+lora_status dispatch_r(int r, Mode m, CCParams& prm, int items_bound, cudaStream_t st) {
   switch (r) {
     case 8: return dispatch_mode<8, T>(m, prm, items_bound, st);
     case 16: return dispatch_mode<16, T>(m, prm, items_bound, st);
@@ -623,15 +917,15 @@ lora_status launch_sgmv_cc(const SgmvCall& call, cudaStream_t stream) {
     if (call.mode & kModeExpand) hmax = std::max(hmax, call.proj[i].h_out);
   }
   // ranks per item: about 512 rows/columns per CTA, at most 8 (portable cluster)
-  const int C = std::clamp(ceil_div(hmax, 512), 1, 8);
-  // tokens per tile: small tiles when segments are short on average
+  const int C = std::clamp(ceil_div(hmax, 512), 1, kMaxC);
+  // tokens per tile (MMA rows): small tiles when segments are short on average
   const double avg = static_cast<double>(n) / std::max(1, std::min(n, call.n_adapters));
-  const int T = avg <= 2.5 ? 2 : 8;
+  const int T = avg <= 3.0 ? 4 : 16;
 
   CCParams prm{};
   for (int i = 0; i < call.n_proj; ++i) {
     const ProjArgs& a = call.proj[i];
-    CCProj& q = prm.proj[i];
+    CCProj& q = prm.t.proj[i];
     q.x = a.x;
     q.A = a.A;
     q.B = a.B;
@@ -640,28 +934,30 @@ lora_status launch_sgmv_cc(const SgmvCall& call, cudaStream_t stream) {
     q.ldy = a.ldy;
     q.h_in = a.h_in;
     q.h_out = a.h_out;
-    q.k_chunk = round_up(ceil_div(a.h_in, C), 8);
+    q.k_chunk = round_up(ceil_div(a.h_in, C), 16);
     q.n_chunk = round_up(ceil_div(a.h_out, C), 8);
+    q.bw = 8;
+    q.nb = 1;
     q.scale = a.scale;
   }
-  prm.perm = call.seg.perm;
-  prm.seg_offsets = call.seg.seg_offsets;
-  prm.seg_adapter = call.seg.seg_adapter;
-  prm.num_segments = call.seg.num_segments;
-  prm.v_out = call.v_out;
-  prm.v_in = call.v_in;
-  prm.err_flag = call.err_flag;
-  prm.n_proj = call.n_proj;
-  prm.n_tokens = n;
-  prm.max_segments = S_max;
-  prm.n_adapters = call.n_adapters;
-  prm.csplit = C;
+  prm.t.perm = call.seg.perm;
+  prm.t.seg_offsets = call.seg.seg_offsets;
+  prm.t.seg_adapter = call.seg.seg_adapter;
+  prm.t.num_segments = call.seg.num_segments;
+  prm.t.v_out = call.v_out;
+  prm.t.v_in = call.v_in;
+  prm.t.err_flag = call.err_flag;
+  prm.t.n_proj = call.n_proj;
+  prm.t.n_tokens = n;
+  prm.t.max_segments = S_max;
+  prm.t.n_adapters = call.n_adapters;
+  prm.t.csplit = C;
 
   // upper bound of the number of tiles: sum over segments of ceil(len/T)
   const int64_t tiles = std::min<int64_t>(n, (static_cast<int64_t>(n) + static_cast<int64_t>(S_max) * (T - 1)) / T);
   const int items_bound = static_cast<int>(std::min<int64_t>(tiles * call.n_proj, 1 << 30));
-  if (T == 2) return dispatch_r<2>(call.r, call.mode, prm, items_bound, stream);
-  return dispatch_r<8>(call.r, call.mode, prm, items_bound, stream);
+  if (T == 4) return dispatch_r<4>(call.r, call.mode, prm, items_bound, stream);
+  return dispatch_r<16>(call.r, call.mode, prm, items_bound, stream);
 }
 
 }  // namespace lsg
