@@ -55,6 +55,14 @@ struct SgmvCall {
 
 lora_status launch_sgmv_cc(const SgmvCall& call, cudaStream_t stream);
 
+// ---- SGMV (tcgen05 tile path for long segments)
+// Segments of at least kLongSeg tokens whose rows are contiguous in x / y go
+// to the tensor-tile kernel when it applies (fused calls, r in {16, 32, 64});
+// the split-K kernel skips exactly those segments then.
+constexpr int kLongSeg = 64;
+bool sgmv_tc_applicable(const SgmvCall& call);
+lora_status launch_sgmv_tc(const SgmvCall& call, cudaStream_t stream);
+
 // TMA tensor map over bf16 data: `rank` dims (innermost first), byte strides
 // of dims 1.., box extents in elements, swizzle span in bytes (0 = none).
 lora_status encode_tmap_bf16(CUtensorMap* out, const void* base, int rank, const uint64_t* dims,

@@ -103,7 +103,8 @@ struct CCTail {
   int32_t n_tokens;
   int32_t max_segments;
   int32_t n_adapters;
-  int32_t csplit;  // C
+  int32_t csplit;     // C
+  int32_t skip_long;  // segments of >= kLongSeg contiguous tokens belong to the tensor-tile kernel
 };
 
 struct CCParams {
@@ -162,13 +163,6 @@ struct CCSmem {
 
 __device__ __forceinline__ void consumer_sync() { named_bar_sync(1, kCThreads); }
 
-// TMA swizzle (16-byte chunk index XOR address bits 7..) of a shared-memory
-// byte address; SWM = span/16 - 1 (0: no swizzle).
-template <uint32_t SWM>
-__device__ __forceinline__ uint32_t swz(uint32_t addr) {
-  return addr ^ (((addr >> 7) & SWM) << 4);
-}
-
 __device__ __forceinline__ uint32_t ld_shared_u32(const void* p) {
   return *reinterpret_cast<const uint32_t*>(p);
 }
@@ -199,6 +193,10 @@ struct SegCursor {
       ad = q.seg_adapter[s];
       off = o;
       len = (o >= 0 && e <= q.n_tokens && e >= o) ? e - o : 0;
+      if (q.skip_long && len >= kLongSeg) {
+        const int f = q.perm[o], b = q.perm[e - 1];
+        if (f >= 0 && b < q.n_tokens && b - f == len - 1) len = 0;  // taken by the tensor-tile kernel
+      }
     }
   }
 
@@ -762,7 +760,6 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
       phase ^= 1u;
     }
   }
-  if (ct < T) bulk_wait0();  // our y stores have landed
   if (xchg) {
     if (!start_waited) cluster_wait_acquire();
     cluster_arrive_relaxed();
@@ -952,6 +949,13 @@ lora_status launch_sgmv_cc(const SgmvCall& call, cudaStream_t stream) {
   prm.t.max_segments = S_max;
   prm.t.n_adapters = call.n_adapters;
   prm.t.csplit = C;
+  prm.t.skip_long = 0;
+  if (sgmv_tc_applicable(call)) {
+    // long contiguous segments on tcgen05 tiles, the rest of the batch here
+    const lora_status s = launch_sgmv_tc(call, stream);
+    if (s != LORA_OK) return s;
+    prm.t.skip_long = 1;
+  }
 
   // upper bound of the number of tiles: sum over segments of ceil(len/T)
   const int64_t tiles = std::min<int64_t>(n, (static_cast<int64_t>(n) + static_cast<int64_t>(S_max) * (T - 1)) / T);

@@ -1,0 +1,660 @@
+// SGMV for long segments (prefill) on the 5th-generation tensor cores.
+//
+// Punica: Multi-Tenant LoRA Serving (research.elamur.ai summary), "Key
+// points": the SGMV kernel batches the LoRA add-on computation across
+// adapters and uses the GPU's tensor cores; "Interesting ideas" I2: sorting
+// the batch by adapter turns scattered small products into dense segments.
+// For a prefill segment (hundreds of tokens of one adapter) both products
+// are real matrix products, tiled here as M = 128 tokens:
+//
+//   shrink  v[128][r]   = x[128][h_in] . A[h_in][r]            (K = h_in)
+//   expand  y[128][c]  += s * v[128][r] . B[r][c], c in chunk  (K = r)
+//
+// One CTA per SM, persistent, seven warps with fixed roles:
+//   warps 0-3  epilogue: TMEM lane quarter w; turn v (fp32, TMEM) into the
+//              expand's bf16 operand pair v = hi + lo in shared memory, then
+//              add s * acc to the y tile in shared memory and store it
+//   warp 4     shrink producer: TMA x tiles [128][64] (K-major, 128 B swizzle)
+//              and A tiles [64][r] (MN-major, 2r-byte swizzle), 3 stages
+//   warp 5     expand producer: TMA y tiles [128][128] (two 64-column 128 B
+//              swizzled halves) and B tiles [r][128] (MN-major), 2 stages
+//   warp 6     TMEM allocation and the single MMA-issuing thread:
+//              tcgen05.mma kind::f16, fp32 accumulators in TMEM (v: columns
+//              0..r-1; expand: two 128-column buffers, so the epilogue of one
+//              block overlaps the MMAs of the next)
+//
+// Work item = (128-token tile of a segment, projection, column chunk of
+// h_out).  Each item recomputes its tile's shrink (x is re-read from L2 by
+// the items of the same tile), which keeps items of similar size for load
+// balance.  Only segments of at least kLongSeg tokens whose rows are
+// contiguous in x / y (true for prefill requests) are taken here; the
+// decode kernel handles the rest of the batch (it skips these segments).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace lsg {
+
+constexpr int kTcThreads = 224;
+constexpr int kTcEpiThreads = 128;
+constexpr int kShStages = 3;
+constexpr int kExStages = 2;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemV = 0;      // v accumulator: columns [0, r)
+constexpr uint32_t kTmemAcc = 128;  // expand accumulators: [128, 256), [256, 384)
+constexpr int kChunkCols = 5120;    // expand columns per item, about
+constexpr int kMaxItemsPerTile = 64;
+constexpr uint64_t kTcWaitNs = 2000000000ull;
+
+struct TcProj {
+  uint16_t* y;  // for the direct stores of a tile's last rows
+  int64_t ldy;
+  int32_t h_in, h_out;
+  int32_t chunk;  // columns per chunk (multiple of 128)
+  float scale;
+};
+
+struct TcTail {
+  TcProj proj[kMaxProj];
+  int8_t item_proj[kMaxItemsPerTile];
+  int8_t item_chunk[kMaxItemsPerTile];
+  const int32_t* perm;
+  const int32_t* seg_offsets;
+  const int32_t* seg_adapter;
+  const int32_t* num_segments;
+  int32_t* err_flag;
+  int32_t n_proj;
+  int32_t ipt;  // items per tile
+  int32_t n_tokens;
+  int32_t max_segments;
+  int32_t n_adapters;
+};
+
+struct TcParams {
+  CUtensorMap tmX[kMaxProj];   // x [n][h_in], box {64, 128}, 128 B swizzle
+  CUtensorMap tmA[kMaxProj];   // A_pool [P][h_in][r], box {r, 64, 1}, 2r B swizzle
+  CUtensorMap tmB[kMaxProj];   // B_pool [P*r][h_out], box {64, r}, 128 B swizzle
+  CUtensorMap tmYl[kMaxProj];  // y [n][h_out], box {64, 128}, 128 B swizzle (load)
+  CUtensorMap tmYs[kMaxProj];  // y, box {64, 32}, 128 B swizzle (store)
+  TcTail t;
+};
+
+template <int R>
+struct TcCfg {
+  static constexpr int kShA = 64 * R * 2;                          // A tile bytes
+  static constexpr int kShBytes = ((16384 + kShA + 1023) / 1024) * 1024;
+  static constexpr int kExB = R * 256;                             // B tile bytes (two 64-column atoms)
+  static constexpr int kExBytes = ((32768 + kExB + 1023) / 1024) * 1024;
+  static constexpr int kVop = 128 * R * 2;                         // one bf16 operand [128][r]
+  static constexpr uint32_t kSwR = R * 2;                          // swizzle span of r-wide rows
+  static constexpr uint32_t kSwM = kSwR / 16 - 1;
+};
+
+template <int R>
+struct TcSmem {
+  alignas(1024) uint8_t sh[kShStages][TcCfg<R>::kShBytes];
+  alignas(1024) uint8_t ex[kExStages][TcCfg<R>::kExBytes];
+  alignas(1024) uint8_t vop[2][TcCfg<R>::kVop];  // hi, lo
+  alignas(16) TcTail t;
+  alignas(8) uint64_t sh_full[kShStages];
+  uint64_t sh_empty[kShStages];
+  uint64_t ex_full[kExStages];
+  uint64_t ex_empty[kExStages];
+  uint64_t v_full;
+  uint64_t vop_ready;
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint32_t tmem_base;
+  int32_t abort;
+};
+
+// Cursor over the segments taken by this kernel (at least kLongSeg tokens,
+// rows contiguous), 32 at a time, locating 128-token tiles.  Executed by a
+// full warp; tile indices asked for only grow.
+struct TcCursor {
+  int base = 0, tiles_before = 0, S = 0;
+  int off = 0, len = 0, ad = -1, row0 = 0;  // segment base + lane
+
+  __device__ void load(const TcTail& q, int lane) {
+    const int s = base + lane;
+    off = 0;
+    len = 0;
+    ad = -1;
+    row0 = 0;
+    if (s < S) {
+      const int o = q.seg_offsets[s];
+      const int e = q.seg_offsets[s + 1];
+      ad = q.seg_adapter[s];
+      const int l = (o >= 0 && e <= q.n_tokens && e >= o) ? e - o : 0;
+      if (l >= kLongSeg) {
+        const int f = q.perm[o], b = q.perm[e - 1];
+        if (f >= 0 && b < q.n_tokens && b - f == l - 1) {
+          off = o;
+          len = l;
+          row0 = f;
+        }
+      }
+    }
+  }
+
+  __device__ void init(const TcTail& q, int lane) {
+    S = min(max(*q.num_segments, 0), q.max_segments);
+    load(q, lane);
+  }
+
+  // tile -> first token position t0 in perm order, length, adapter, first x/y row
+  __device__ bool find(const TcTail& q, int lane, int tile, int& tlen, int& a, int& row) {
+    while (base < S) {
+      const int tl = (len + 127) >> 7;
+      int inc = tl;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, inc, d);
+        if (lane >= d) inc += o;
+      }
+      const int total = __shfl_sync(0xffffffffu, inc, 31);
+      if (tile < tiles_before + total) {
+        const unsigned m = __ballot_sync(0xffffffffu, tiles_before + inc > tile);
+        const int ls = __ffs(m) - 1;
+        const int excl = __shfl_sync(0xffffffffu, inc - tl, ls);
+        const int l = __shfl_sync(0xffffffffu, len, ls);
+        const int r0 = __shfl_sync(0xffffffffu, row0, ls);
+        a = __shfl_sync(0xffffffffu, ad, ls);
+        const int k = (tile - tiles_before - excl) * 128;
+        tlen = min(128, l - k);
+        row = r0 + k;
+        return true;
+      }
+      tiles_before += total;
+      base += 32;
+      load(q, lane);
+    }
+    return false;
+  }
+};
+
+// Bounded wait by lane 0, result broadcast to the warp; a time-out sets the
+// error flag and the CTA-wide abort flag.
+template <typename SM>
+__device__ __forceinline__ bool warp_wait(SM& sm, uint64_t* bar, uint32_t parity, int lane) {
+  bool ok = true;
+  if (lane == 0) {
+    ok = mbar_wait(bar, parity, kTcWaitNs);
+    if (!ok) {
+      set_err(sm.t.err_flag, LORA_ERR_TIMEOUT);
+      atomicExch(&sm.abort, 1);
+    }
+  }
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+template <int R>
+__global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_constant__ TcParams p) {
+  using Cfg = TcCfg<R>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  auto& sm = *reinterpret_cast<TcSmem<R>*>(smem_raw);
+  const TcTail& q = sm.t;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  {
+    static_assert(sizeof(TcTail) % 4 == 0, "tail size");
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(&p.t);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.t);
+    for (int i = tid; i < static_cast<int>(sizeof(TcTail) / 4); i += kTcThreads) dst[i] = src[i];
+  }
+  if (warp == 4 && lane < kMaxProj) {
+    prefetch_tmap(&p.tmX[lane]);
+    prefetch_tmap(&p.tmA[lane]);
+  }
+  if (warp == 5 && lane < kMaxProj) {
+    prefetch_tmap(&p.tmB[lane]);
+    prefetch_tmap(&p.tmYl[lane]);
+    prefetch_tmap(&p.tmYs[lane]);
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kShStages; ++s) {
+      mbar_init(&sm.sh_full[s], 1);
+      mbar_init(&sm.sh_empty[s], 1);
+    }
+    for (int s = 0; s < kExStages; ++s) {
+      mbar_init(&sm.ex_full[s], 1);
+      mbar_init(&sm.ex_empty[s], 1);
+    }
+    mbar_init(&sm.v_full, 1);
+    mbar_init(&sm.vop_ready, 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.acc_full[b], 1);
+      mbar_init(&sm.acc_empty[b], 4);
+    }
+    sm.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 6) tmem_alloc(&sm.tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  pdl_launch_dependents();
+  pdl_wait();
+  // the operand swizzle below is computed on absolute shared addresses
+  const bool aligned = (smem_u32(sm.sh) & 1023u) == 0;
+  if (!aligned && tid == 0) set_err(q.err_flag, LORA_ERR_UNSUPPORTED);
+
+  if (aligned && warp == 4) {
+    // ============================== shrink producer
+    int slot = 0;
+    uint32_t ph = 0;
+    TcCursor cur;
+    cur.init(q, lane);
+    for (int item = blockIdx.x;; item += gridDim.x) {
+      const int tile = item / q.ipt, is = item - tile * q.ipt;
+      int tlen, a, row;
+      if (!cur.find(q, lane, tile, tlen, a, row)) break;
+      if (a < 0 || a >= q.n_adapters) continue;
+      const int pj = q.item_proj[is];
+      const int nkb = (q.proj[pj].h_in + 63) >> 6;
+      bool ok = true;
+      for (int kb = 0; kb < nkb && ok; ++kb) {
+        ok = warp_wait(sm, &sm.sh_empty[slot], ph ^ 1u, lane);
+        if (!ok) break;
+        if (lane == 0) {
+          uint8_t* st = sm.sh[slot];
+          mbar_arrive_expect_tx(&sm.sh_full[slot], 16384u + Cfg::kShA);
+          tma_load_2d(st, &p.tmX[pj], kb * 64, row, &sm.sh_full[slot]);
+          tma_load_3d(st + 16384, &p.tmA[pj], 0, kb * 64, a, &sm.sh_full[slot]);
+        }
+        if (++slot == kShStages) {
+          slot = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!ok || sm.abort) break;
+    }
+  } else if (aligned && warp == 5) {
+    // ============================== expand producer
+    int slot = 0;
+    uint32_t ph = 0;
+    TcCursor cur;
+    cur.init(q, lane);
+    for (int item = blockIdx.x;; item += gridDim.x) {
+      const int tile = item / q.ipt, is = item - tile * q.ipt;
+      int tlen, a, row;
+      if (!cur.find(q, lane, tile, tlen, a, row)) break;
+      if (a < 0 || a >= q.n_adapters) continue;
+      const int pj = q.item_proj[is], ch = q.item_chunk[is];
+      const TcProj& pr = q.proj[pj];
+      const int c0 = ch * pr.chunk;
+      const int nblk = (min(pr.chunk, pr.h_out - c0) + 127) >> 7;
+      bool ok = true;
+      for (int b = 0; b < nblk && ok; ++b) {
+        ok = warp_wait(sm, &sm.ex_empty[slot], ph ^ 1u, lane);
+        if (!ok) break;
+        if (lane == 0) {
+          uint8_t* st = sm.ex[slot];
+          const int c = c0 + b * 128;
+          mbar_arrive_expect_tx(&sm.ex_full[slot], 32768u + Cfg::kExB);
+          tma_load_2d(st, &p.tmYl[pj], c, row, &sm.ex_full[slot]);
+          tma_load_2d(st + 16384, &p.tmYl[pj], c + 64, row, &sm.ex_full[slot]);
+          tma_load_2d(st + 32768, &p.tmB[pj], c, a * R, &sm.ex_full[slot]);
+          tma_load_2d(st + 32768 + R * 128, &p.tmB[pj], c + 64, a * R, &sm.ex_full[slot]);
+        }
+        if (++slot == kExStages) {
+          slot = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!ok || sm.abort) break;
+    }
+  } else if (aligned && warp == 6) {
+    // ============================== MMA issuer
+    constexpr uint32_t kIdSh = umma_idesc_bf16(128, R, 0, 1);
+    constexpr uint32_t kIdEx = umma_idesc_bf16(128, 128, 0, 1);
+    int sslot = 0, xslot = 0, ae = 0, it = 0;
+    uint32_t sph = 0, xph = 0;
+    TcCursor cur;
+    cur.init(q, lane);
+    for (int item = blockIdx.x;; item += gridDim.x) {
+      const int tile = item / q.ipt, is = item - tile * q.ipt;
+      int tlen, a, row;
+      if (!cur.find(q, lane, tile, tlen, a, row)) break;
+      if (a < 0 || a >= q.n_adapters) continue;
+      const int pj = q.item_proj[is], ch = q.item_chunk[is];
+      const TcProj& pr = q.proj[pj];
+      const int nkb = (pr.h_in + 63) >> 6;
+      bool ok = true;
+      // ---- shrink: v = x . A over all k-blocks
+      for (int kb = 0; kb < nkb && ok; ++kb) {
+        ok = warp_wait(sm, &sm.sh_full[sslot], sph, lane);
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t xs = smem_u32(sm.sh[sslot]), as = xs + 16384;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t ad = umma_desc(xs + k * 32, 16, 1024, 2);
+            const uint64_t bd = umma_desc(as + k * 16 * R * 2, Cfg::kShA, 8 * R * 2, umma_layout(R * 2));
+            umma_bf16(tmem + kTmemV, ad, bd, kIdSh, kb > 0 || k > 0);
+          }
+          umma_commit(&sm.sh_empty[sslot]);  // the stage is free once these MMAs have read it
+        }
+        __syncwarp();
+        if (++sslot == kShStages) {
+          sslot = 0;
+          sph ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) umma_commit(&sm.v_full);
+      __syncwarp();
+      // ---- expand: acc = v_hi . B + v_lo . B per 128-column block
+      ok = warp_wait(sm, &sm.vop_ready, it & 1, lane);
+      if (!ok) break;
+      tc_fence_after();
+      const int c0 = ch * pr.chunk;
+      const int nblk = (min(pr.chunk, pr.h_out - c0) + 127) >> 7;
+      for (int b = 0; b < nblk && ok; ++b) {
+        const int buf = ae & 1;
+        ok = warp_wait(sm, &sm.acc_empty[buf], ((ae >> 1) & 1) ^ 1u, lane) &&
+             warp_wait(sm, &sm.ex_full[xslot], xph, lane);
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t bs = smem_u32(sm.ex[xslot]) + 32768;
+#pragma unroll
+          for (int k = 0; k < R / 16; ++k) {
+            const uint64_t bd = umma_desc(bs + k * 16 * 128, R * 128, 1024, 2);
+#pragma unroll
+            for (int hl = 0; hl < 2; ++hl) {
+              const uint64_t ad = umma_desc(smem_u32(sm.vop[hl]) + k * 32, 16, 8 * R * 2, umma_layout(R * 2));
+              umma_bf16(tmem + kTmemAcc + buf * 128, ad, bd, kIdEx, k > 0 || hl > 0);
+            }
+          }
+          umma_commit(&sm.acc_full[buf]);
+        }
+        __syncwarp();
+        ++ae;
+        if (++xslot == kExStages) {
+          xslot = 0;
+          xph ^= 1u;
+        }
+      }
+      if (!ok || sm.abort) break;
+      ++it;
+    }
+  } else if (aligned && warp < 4) {
+    // ============================== epilogue (row m = TMEM lane m)
+    const int m = tid;
+    const uint32_t tq = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    int xslot = 0, ae = 0, it = 0;
+    uint32_t xph = 0;
+    TcCursor cur;
+    cur.init(q, lane);
+    for (int item = blockIdx.x;; item += gridDim.x) {
+      const int tile = item / q.ipt, is = item - tile * q.ipt;
+      int tlen, a, row;
+      if (!cur.find(q, lane, tile, tlen, a, row)) break;
+      if (a < 0 || a >= q.n_adapters) {
+        if (tid == 0) set_err(q.err_flag, LORA_ERR_BAD_ADAPTER_ID);
+        continue;
+      }
+      const int pj = q.item_proj[is], ch = q.item_chunk[is];
+      const TcProj& pr = q.proj[pj];
+      const float scale = pr.scale;
+      // ---- v (fp32, TMEM) -> bf16 operands hi, lo (K-major, 2r-byte swizzle)
+      bool ok = warp_wait(sm, &sm.v_full, it & 1, lane);
+      if (!ok) break;
+      tc_fence_after();
+      {
+        uint32_t v[R];
+        if constexpr (R == 16) {
+          uint32_t r16[16];
+          tmem_ld16(tq + kTmemV, r16);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = r16[i];
+        } else {
+#pragma unroll
+          for (int c = 0; c < R / 32; ++c) {
+            uint32_t r32[32];
+            tmem_ld32(tq + kTmemV + c * 32, r32);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[c * 32 + i] = r32[i];
+          }
+        }
+        const uint32_t hrow = smem_u32(sm.vop[0]) + static_cast<uint32_t>(m) * (R * 2);
+        const uint32_t lrow = smem_u32(sm.vop[1]) + static_cast<uint32_t>(m) * (R * 2);
+#pragma unroll
+        for (int j = 0; j < R / 8; ++j) {
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float f0 = __uint_as_float(v[j * 8 + 2 * e]), f1 = __uint_as_float(v[j * 8 + 2 * e + 1]);
+            const __nv_bfloat162 h = __floats2bfloat162_rn(f0, f1);
+            const float2 hf = __bfloat1622float2(h);
+            const __nv_bfloat162 l = __floats2bfloat162_rn(f0 - hf.x, f1 - hf.y);
+            hi[e] = *reinterpret_cast<const uint32_t*>(&h);
+            lo[e] = *reinterpret_cast<const uint32_t*>(&l);
+          }
+          const uint32_t ha = swz<Cfg::kSwM>(hrow + j * 16), la = swz<Cfg::kSwM>(lrow + j * 16);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(ha), "r"(hi[0]), "r"(hi[1]), "r"(hi[2]),
+                       "r"(hi[3])
+                       : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(la), "r"(lo[0]), "r"(lo[1]), "r"(lo[2]),
+                       "r"(lo[3])
+                       : "memory");
+        }
+      }
+      fence_proxy_async_smem();  // the tensor core reads the operands through the async proxy
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.vop_ready);
+      // ---- expand blocks: y = bf16(y + s * acc)
+      const int c0 = ch * pr.chunk;
+      const int nblk = (min(pr.chunk, pr.h_out - c0) + 127) >> 7;
+      const int full_rows = (tlen >> 5) << 5;
+      for (int b = 0; b < nblk && ok; ++b) {
+        const int buf = ae & 1;
+        ok = warp_wait(sm, &sm.acc_full[buf], (ae >> 1) & 1, lane);
+        if (!ok) break;
+        tc_fence_after();
+        uint8_t* st = sm.ex[xslot];
+        const int c = c0 + b * 128;
+#pragma unroll 1
+        for (int c32 = 0; c32 < 4; ++c32) {
+          uint32_t acc[32];
+          tmem_ld32(tq + kTmemAcc + buf * 128 + c32 * 32, acc);
+          tmem_ld_wait();
+          const uint32_t rbase = smem_u32(st + (c32 >> 1) * 16384) + static_cast<uint32_t>(m) * 128;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int j = (c32 & 1) * 4 + i;  // 16-byte chunk of the 64-column half
+            const uint32_t addr = rbase + ((static_cast<uint32_t>(j) ^ (m & 7u)) << 4);
+            uint32_t yw[4];
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(yw[0]), "=r"(yw[1]), "=r"(yw[2]), "=r"(yw[3])
+                         : "r"(addr));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 yf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&yw[e]));
+              const __nv_bfloat162 o = __floats2bfloat162_rn(yf.x + scale * __uint_as_float(acc[i * 8 + 2 * e]),
+                                                             yf.y + scale * __uint_as_float(acc[i * 8 + 2 * e + 1]));
+              yw[e] = *reinterpret_cast<const uint32_t*>(&o);
+            }
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(yw[0]), "r"(yw[1]), "r"(yw[2]),
+                         "r"(yw[3])
+                         : "memory");
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.acc_empty[buf]);  // TMEM buffer free for the next block
+        // rows past the last whole group of 32: written directly (16-byte stores)
+        if (m >= full_rows && m < tlen) {
+          uint16_t* yrow = pr.y + static_cast<int64_t>(row + m) * pr.ldy;
+#pragma unroll 1
+          for (int j = 0; j < 16; ++j) {
+            const int col = c + j * 8;
+            if (col < pr.h_out) {
+              const uint32_t addr = smem_u32(st + (j >> 3) * 16384) + static_cast<uint32_t>(m) * 128 +
+                                    ((static_cast<uint32_t>(j & 7) ^ (m & 7u)) << 4);
+              uint4 w;
+              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                           : "r"(addr));
+              *reinterpret_cast<uint4*>(yrow + col) = w;
+            }
+          }
+        }
+        fence_proxy_async_smem();  // our y updates, visible to the tensor stores
+        named_bar_sync(2, kTcEpiThreads);
+        if (tid == 0) {
+          for (int g = 0; g < full_rows; g += 32)
+            for (int h = 0; h < 2; ++h)
+              if (c + h * 64 < pr.h_out) tma_store_2d(&p.tmYs[pj], c + h * 64, row + g, st + h * 16384 + g * 128);
+          bulk_commit();
+          bulk_wait_read0();
+          mbar_arrive(&sm.ex_empty[xslot]);  // y tile read by the stores, B tile read by the MMAs
+        }
+        ++ae;
+        if (++xslot == kExStages) {
+          xslot = 0;
+          xph ^= 1u;
+        }
+      }
+      if (!ok || sm.abort) break;
+      ++it;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 6) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+namespace {
+
+template <int R>
+lora_status launch_tc_r(TcParams& prm, const SgmvCall& call, int tiles_bound, cudaStream_t stream) {
+  auto kern = sgmv_tc_kernel<R>;
+  const size_t smem = sizeof(TcSmem<R>);
+  for (int i = 0; i < call.n_proj; ++i) {
+    const ProjArgs& a = call.proj[i];
+    lora_status s;
+    {
+      const uint64_t dims[2] = {static_cast<uint64_t>(a.h_in), static_cast<uint64_t>(call.seg.n_tokens)};
+      const uint64_t str[1] = {static_cast<uint64_t>(a.ldx) * 2};
+      const uint32_t box[2] = {64, 128};
+      if ((s = encode_tmap_bf16(&prm.tmX[i], a.x, 2, dims, str, box, 128)) != LORA_OK) return s;
+    }
+    {
+      const uint64_t dims[3] = {static_cast<uint64_t>(R), static_cast<uint64_t>(a.h_in),
+                                static_cast<uint64_t>(call.n_adapters)};
+      const uint64_t str[2] = {static_cast<uint64_t>(R) * 2, static_cast<uint64_t>(a.h_in) * R * 2};
+      const uint32_t box[3] = {static_cast<uint32_t>(R), 64, 1};
+      if ((s = encode_tmap_bf16(&prm.tmA[i], a.A, 3, dims, str, box, R * 2)) != LORA_OK) return s;
+    }
+    {
+      const uint64_t dims[2] = {static_cast<uint64_t>(a.h_out), static_cast<uint64_t>(call.n_adapters) * R};
+      const uint64_t str[1] = {static_cast<uint64_t>(a.h_out) * 2};
+      const uint32_t box[2] = {64, static_cast<uint32_t>(R)};
+      if ((s = encode_tmap_bf16(&prm.tmB[i], a.B, 2, dims, str, box, 128)) != LORA_OK) return s;
+    }
+    {
+      const uint64_t dims[2] = {static_cast<uint64_t>(a.h_out), static_cast<uint64_t>(call.seg.n_tokens)};
+      const uint64_t str[1] = {static_cast<uint64_t>(a.ldy) * 2};
+      const uint32_t box_l[2] = {64, 128}, box_s[2] = {64, 32};
+      if ((s = encode_tmap_bf16(&prm.tmYl[i], a.y, 2, dims, str, box_l, 128)) != LORA_OK) return s;
+      if ((s = encode_tmap_bf16(&prm.tmYs[i], a.y, 2, dims, str, box_s, 128)) != LORA_OK) return s;
+    }
+  }
+
+  static std::once_flag once[64];
+  static int nsm_cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
+  cudaError_t aerr = cudaSuccess;
+  std::call_once(once[dev & 63], [&] {
+    aerr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (aerr == cudaSuccess) aerr = cudaDeviceGetAttribute(&nsm_cache[dev & 63], cudaDevAttrMultiProcessorCount, dev);
+  });
+  if (aerr != cudaSuccess) return LORA_ERR_CUDA;
+  const int64_t items = static_cast<int64_t>(tiles_bound) * prm.t.ipt;
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(nsm_cache[dev & 63], items)));
+
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute at[1];
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, prm));
+}
+
+}  // namespace
+
+// Launched when segments are long on average (tokens per possible segment,
+// known on the host without reading the segmentation); a long segment in a
+// batch of short ones is then left to the split-K kernel, which handles any
+// segment.
+bool sgmv_tc_applicable(const SgmvCall& call) {
+  const int n = call.seg.n_tokens;
+  const int max_seg = std::max(1, std::min(n, call.n_adapters));
+  return call.mode == kModeFused && (call.r == 16 || call.r == 32 || call.r == 64) && n >= kLongSeg &&
+         n / max_seg >= kLongSeg;
+}
+
+lora_status launch_sgmv_tc(const SgmvCall& call, cudaStream_t stream) {
+  TcParams prm{};
+  int ipt = 0;
+  for (int i = 0; i < call.n_proj; ++i) {
+    const ProjArgs& a = call.proj[i];
+    TcProj& t = prm.t.proj[i];
+    t.y = a.y;
+    t.ldy = a.ldy;
+    t.h_in = a.h_in;
+    t.h_out = a.h_out;
+    t.scale = a.scale;
+    const int nch = std::clamp(ceil_div(a.h_out, kChunkCols), 1, 8);
+    t.chunk = round_up(ceil_div(a.h_out, nch), 128);
+    const int nch_real = ceil_div(a.h_out, t.chunk);
+    for (int c = 0; c < nch_real; ++c) {
+      prm.t.item_proj[ipt] = static_cast<int8_t>(i);
+      prm.t.item_chunk[ipt] = static_cast<int8_t>(c);
+      ++ipt;
+    }
+  }
+  prm.t.perm = call.seg.perm;
+  prm.t.seg_offsets = call.seg.seg_offsets;
+  prm.t.seg_adapter = call.seg.seg_adapter;
+  prm.t.num_segments = call.seg.num_segments;
+  prm.t.err_flag = call.err_flag;
+  prm.t.n_proj = call.n_proj;
+  prm.t.ipt = ipt;
+  prm.t.n_tokens = call.seg.n_tokens;
+  prm.t.max_segments = call.seg.max_segments;
+  prm.t.n_adapters = call.n_adapters;
+  // upper bound of the tiles of segments of at least kLongSeg tokens
+  const int tiles_bound = ceil_div(call.seg.n_tokens, 128) + call.seg.n_tokens / kLongSeg;
+  switch (call.r) {
+    case 16: return launch_tc_r<16>(prm, call, tiles_bound, stream);
+    case 32: return launch_tc_r<32>(prm, call, tiles_bound, stream);
+    case 64: return launch_tc_r<64>(prm, call, tiles_bound, stream);
+    default: return LORA_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace lsg
