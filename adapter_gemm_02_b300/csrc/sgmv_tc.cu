@@ -15,16 +15,21 @@
 //              expand's bf16 operand pair v = hi + lo in shared memory, then
 //              add s * acc to the y tile in shared memory and store it
 //   warp 4     shrink producer: TMA x tiles [128][64] (K-major, 128 B swizzle)
-//              and A tiles [64][r] (MN-major, 2r-byte swizzle), 3 stages
+//              and A tiles [64][r] (MN-major, 2r-byte swizzle), 4 stages
 //   warp 5     expand producer: TMA y tiles [128][128] (two 64-column 128 B
 //              swizzled halves) and B tiles [r][128] (MN-major), 2 stages
-//   warp 6     TMEM allocation and the single MMA-issuing thread:
-//              tcgen05.mma kind::f16, fp32 accumulators in TMEM (v: columns
-//              0..r-1; expand: two 128-column buffers, so the epilogue of one
-//              block overlaps the MMAs of the next)
+//   warp 6     TMEM allocation; one thread issues the shrink MMAs
+//   warp 7     one thread issues the expand MMAs
+//              (tcgen05.mma kind::f16, fp32 accumulators in TMEM: v in columns
+//              0..r-1, two 128-column expand buffers, so the epilogue of one
+//              block overlaps the MMAs of the next).  With one issuer per
+//              stream the shrink of item i+1 streams x and A while item i is
+//              expanded; the epilogue orders the two: it reads v(i) before it
+//              releases the shrink of item i+1 (vop_ready), and it rewrites the
+//              v operand only after the last expand MMAs of item i completed.
 //
 // Work item = (128-token tile of a segment, projection, column chunk of
-// h_out).  Each item recomputes its tile's shrink (x is re-read from L2 by
+// h_out), round robin over the CTAs.  Each item recomputes its tile's shrink (x is re-read from L2 by
 // the items of the same tile), which keeps items of similar size for load
 // balance.  Only segments of at least kLongSeg tokens whose rows are
 // contiguous in x / y (true for prefill requests) are taken here; the
@@ -40,14 +45,20 @@
 
 namespace lsg {
 
-constexpr int kTcThreads = 224;
+constexpr int kTcThreads = 256;
 constexpr int kTcEpiThreads = 128;
-constexpr int kShStages = 3;
+#ifndef LSG_TC_SH_STAGES
+#define LSG_TC_SH_STAGES 4
+#endif
+#ifndef LSG_TC_CHUNK
+#define LSG_TC_CHUNK 5120
+#endif
+constexpr int kShStages = LSG_TC_SH_STAGES;
 constexpr int kExStages = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemV = 0;      // v accumulator: columns [0, r)
 constexpr uint32_t kTmemAcc = 128;  // expand accumulators: [128, 256), [256, 384)
-constexpr int kChunkCols = 5120;    // expand columns per item, about
+constexpr int kChunkCols = LSG_TC_CHUNK;  // expand columns per item, about
 constexpr int kMaxItemsPerTile = 64;
 constexpr uint64_t kTcWaitNs = 2000000000ull;
 
@@ -311,11 +322,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       if (!ok || sm.abort) break;
     }
   } else if (aligned && warp == 6) {
-    // ============================== MMA issuer
+    // ============================== shrink MMA issuer: v = x . A
     constexpr uint32_t kIdSh = umma_idesc_bf16(128, R, 0, 1);
-    constexpr uint32_t kIdEx = umma_idesc_bf16(128, 128, 0, 1);
-    int sslot = 0, xslot = 0, ae = 0, it = 0;
-    uint32_t sph = 0, xph = 0;
+    int sslot = 0, it = 0;
+    uint32_t sph = 0;
     TcCursor cur;
     cur.init(q, lane);
     for (int item = blockIdx.x;; item += gridDim.x) {
@@ -323,11 +333,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       int tlen, a, row;
       if (!cur.find(q, lane, tile, tlen, a, row)) break;
       if (a < 0 || a >= q.n_adapters) continue;
-      const int pj = q.item_proj[is], ch = q.item_chunk[is];
-      const TcProj& pr = q.proj[pj];
+      const TcProj& pr = q.proj[q.item_proj[is]];
       const int nkb = (pr.h_in + 63) >> 6;
-      bool ok = true;
-      // ---- shrink: v = x . A over all k-blocks
+      // the epilogue has read the previous item's v out of TMEM
+      bool ok = it == 0 || warp_wait(sm, &sm.vop_ready, (it - 1) & 1, lane);
+      if (!ok) break;
+      tc_fence_after();
       for (int kb = 0; kb < nkb && ok; ++kb) {
         ok = warp_wait(sm, &sm.sh_full[sslot], sph, lane);
         if (!ok) break;
@@ -351,11 +362,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       if (!ok) break;
       if (lane == 0) umma_commit(&sm.v_full);
       __syncwarp();
-      // ---- expand: acc = v_hi . B + v_lo . B per 128-column block
-      ok = warp_wait(sm, &sm.vop_ready, it & 1, lane);
+      if (sm.abort) break;
+      ++it;
+    }
+  } else if (aligned && warp == 7) {
+    // ============================== expand MMA issuer: acc = v_hi . B + v_lo . B
+    constexpr uint32_t kIdEx = umma_idesc_bf16(128, 128, 0, 1);
+    int xslot = 0, ae = 0, it = 0;
+    uint32_t xph = 0;
+    TcCursor cur;
+    cur.init(q, lane);
+    for (int item = blockIdx.x;; item += gridDim.x) {
+      const int tile = item / q.ipt, is = item - tile * q.ipt;
+      int tlen, a, row;
+      if (!cur.find(q, lane, tile, tlen, a, row)) break;
+      if (a < 0 || a >= q.n_adapters) continue;
+      const TcProj& pr = q.proj[q.item_proj[is]];
+      bool ok = warp_wait(sm, &sm.vop_ready, it & 1, lane);
       if (!ok) break;
       tc_fence_after();
-      const int c0 = ch * pr.chunk;
+      const int c0 = q.item_chunk[is] * pr.chunk;
       const int nblk = (min(pr.chunk, pr.h_out - c0) + 127) >> 7;
       for (int b = 0; b < nblk && ok; ++b) {
         const int buf = ae & 1;

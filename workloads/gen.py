@@ -136,6 +136,11 @@ def _build_workloads() -> Dict[str, Workload]:
                            prefill_ids,
                            "Llama2-13B prefill, 7 projections, r=64, 8 requests of U[128,2048] tokens, "
                            "8 adapters of pool 32, sorted by adapter")
+    ids13s = prefill_ids(n_requests=2)
+    w["13b_prefill_small"] = _mk("13b_prefill_small", llama_projs("13b"), 64, 32, int(ids13s.size),
+                                 1.0, lambda: prefill_ids(n_requests=2),
+                                 "Llama2-13B prefill, 7 projections, r=64, 2 requests of U[128,2048] tokens, "
+                                 "2 adapters of pool 32, sorted by adapter (a smaller case of the 8-request batch)")
     for r in (8, 16, 32, 64):
         nm = f"70b_decode_r{r}"
         w[nm] = _mk(nm, llama_projs("70b"), r, 1000, 256, 1.0, lambda: zipf_ids(256, 1000, 0.8),
