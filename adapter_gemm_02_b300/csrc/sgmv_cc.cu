@@ -66,7 +66,13 @@ namespace lsg {
 #ifndef LSG_CC_KB_BIG
 #define LSG_CC_KB_BIG 28
 #endif
-constexpr int kCW = 4;                 // consumer warps
+#ifndef LSG_CC_WARPS
+#define LSG_CC_WARPS 4
+#endif
+#ifndef LSG_CC_ROWS_PER_CTA
+#define LSG_CC_ROWS_PER_CTA 512
+#endif
+constexpr int kCW = LSG_CC_WARPS;      // consumer warps
 constexpr int kCThreads = kCW * 32;    // consumer threads
 constexpr int kThreads = kCThreads + 32;
 constexpr int kMaxC = 8;               // CTAs per cluster (portable limit)
@@ -913,8 +919,8 @@ lora_status launch_sgmv_cc(const SgmvCall& call, cudaStream_t stream) {
     if (call.mode & kModeShrink) hmax = std::max(hmax, call.proj[i].h_in);
     if (call.mode & kModeExpand) hmax = std::max(hmax, call.proj[i].h_out);
   }
-  // ranks per item: about 512 rows/columns per CTA, at most 8 (portable cluster)
-  const int C = std::clamp(ceil_div(hmax, 512), 1, kMaxC);
+  // ranks per item: about LSG_CC_ROWS_PER_CTA rows/columns per CTA, at most 8 (portable cluster)
+  const int C = std::clamp(ceil_div(hmax, LSG_CC_ROWS_PER_CTA), 1, kMaxC);
   // tokens per tile (MMA rows): small tiles when segments are short on average
   const double avg = static_cast<double>(n) / std::max(1, std::min(n, call.n_adapters));
   const int T = avg <= 3.0 ? 4 : 16;
