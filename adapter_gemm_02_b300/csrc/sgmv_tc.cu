@@ -53,8 +53,14 @@ constexpr int kTcEpiThreads = 128;
 #ifndef LSG_TC_CHUNK
 #define LSG_TC_CHUNK 5120
 #endif
+#ifndef LSG_TC_BN
+#define LSG_TC_BN 64
+#endif
 constexpr int kShStages = LSG_TC_SH_STAGES;
-constexpr int kExStages = 2;
+constexpr int kBN = LSG_TC_BN;       // expand block columns (MMA N): 64 or 128
+constexpr int kBH = kBN / 64;        // 64-column halves per block
+static_assert(kBN == 64 || kBN == 128, "expand block");
+constexpr int kExStages = kBN == 64 ? 4 : 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemV = 0;      // v accumulator: columns [0, r)
 constexpr uint32_t kTmemAcc = 128;  // expand accumulators: [128, 256), [256, 384)
@@ -99,8 +105,9 @@ template <int R>
 struct TcCfg {
   static constexpr int kShA = 64 * R * 2;                          // A tile bytes
   static constexpr int kShBytes = ((16384 + kShA + 1023) / 1024) * 1024;
-  static constexpr int kExB = R * 256;                             // B tile bytes (two 64-column atoms)
-  static constexpr int kExBytes = ((32768 + kExB + 1023) / 1024) * 1024;
+  static constexpr int kExY = 16384 * kBH;                         // y tile bytes [128][kBN]
+  static constexpr int kExB = R * 128 * kBH;                       // B tile bytes (64-column atoms)
+  static constexpr int kExBytes = ((kExY + kExB + 1023) / 1024) * 1024;
   static constexpr int kVop = 128 * R * 2;                         // one bf16 operand [128][r]
   static constexpr uint32_t kSwR = R * 2;                          // swizzle span of r-wide rows
   static constexpr uint32_t kSwM = kSwR / 16 - 1;
@@ -300,19 +307,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       const int pj = q.item_proj[is], ch = q.item_chunk[is];
       const TcProj& pr = q.proj[pj];
       const int c0 = ch * pr.chunk;
-      const int nblk = (min(pr.chunk, pr.h_out - c0) + 127) >> 7;
+      const int nblk = (min(pr.chunk, pr.h_out - c0) + kBN - 1) / kBN;
       bool ok = true;
       for (int b = 0; b < nblk && ok; ++b) {
         ok = warp_wait(sm, &sm.ex_empty[slot], ph ^ 1u, lane);
         if (!ok) break;
         if (lane == 0) {
           uint8_t* st = sm.ex[slot];
-          const int c = c0 + b * 128;
-          mbar_arrive_expect_tx(&sm.ex_full[slot], 32768u + Cfg::kExB);
-          tma_load_2d(st, &p.tmYl[pj], c, row, &sm.ex_full[slot]);
-          tma_load_2d(st + 16384, &p.tmYl[pj], c + 64, row, &sm.ex_full[slot]);
-          tma_load_2d(st + 32768, &p.tmB[pj], c, a * R, &sm.ex_full[slot]);
-          tma_load_2d(st + 32768 + R * 128, &p.tmB[pj], c + 64, a * R, &sm.ex_full[slot]);
+          const int c = c0 + b * kBN;
+          mbar_arrive_expect_tx(&sm.ex_full[slot], static_cast<uint32_t>(Cfg::kExY + Cfg::kExB));
+#pragma unroll
+          for (int h = 0; h < kBH; ++h) {
+            tma_load_2d(st + h * 16384, &p.tmYl[pj], c + h * 64, row, &sm.ex_full[slot]);
+            tma_load_2d(st + Cfg::kExY + h * R * 128, &p.tmB[pj], c + h * 64, a * R, &sm.ex_full[slot]);
+          }
         }
         if (++slot == kExStages) {
           slot = 0;
@@ -367,7 +375,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
     }
   } else if (aligned && warp == 7) {
     // ============================== expand MMA issuer: acc = v_hi . B + v_lo . B
-    constexpr uint32_t kIdEx = umma_idesc_bf16(128, 128, 0, 1);
+    constexpr uint32_t kIdEx = umma_idesc_bf16(128, kBN, 0, 1);
     int xslot = 0, ae = 0, it = 0;
     uint32_t xph = 0;
     TcCursor cur;
@@ -382,7 +390,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       if (!ok) break;
       tc_fence_after();
       const int c0 = q.item_chunk[is] * pr.chunk;
-      const int nblk = (min(pr.chunk, pr.h_out - c0) + 127) >> 7;
+      const int nblk = (min(pr.chunk, pr.h_out - c0) + kBN - 1) / kBN;
       for (int b = 0; b < nblk && ok; ++b) {
         const int buf = ae & 1;
         ok = warp_wait(sm, &sm.acc_empty[buf], ((ae >> 1) & 1) ^ 1u, lane) &&
@@ -390,14 +398,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t bs = smem_u32(sm.ex[xslot]) + 32768;
+          const uint32_t bs = smem_u32(sm.ex[xslot]) + Cfg::kExY;
 #pragma unroll
           for (int k = 0; k < R / 16; ++k) {
             const uint64_t bd = umma_desc(bs + k * 16 * 128, R * 128, 1024, 2);
 #pragma unroll
             for (int hl = 0; hl < 2; ++hl) {
               const uint64_t ad = umma_desc(smem_u32(sm.vop[hl]) + k * 32, 16, 8 * R * 2, umma_layout(R * 2));
-              umma_bf16(tmem + kTmemAcc + buf * 128, ad, bd, kIdEx, k > 0 || hl > 0);
+              umma_bf16(tmem + kTmemAcc + buf * kBN, ad, bd, kIdEx, k > 0 || hl > 0);
             }
           }
           umma_commit(&sm.acc_full[buf]);
@@ -482,7 +490,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       if (lane == 0) mbar_arrive(&sm.vop_ready);
       // ---- expand blocks: y = bf16(y + s * acc)
       const int c0 = ch * pr.chunk;
-      const int nblk = (min(pr.chunk, pr.h_out - c0) + 127) >> 7;
+      const int nblk = (min(pr.chunk, pr.h_out - c0) + kBN - 1) / kBN;
       const int full_rows = (tlen >> 5) << 5;
       for (int b = 0; b < nblk && ok; ++b) {
         const int buf = ae & 1;
@@ -490,11 +498,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
         if (!ok) break;
         tc_fence_after();
         uint8_t* st = sm.ex[xslot];
-        const int c = c0 + b * 128;
+        const int c = c0 + b * kBN;
 #pragma unroll 1
-        for (int c32 = 0; c32 < 4; ++c32) {
+        for (int c32 = 0; c32 < kBN / 32; ++c32) {
           uint32_t acc[32];
-          tmem_ld32(tq + kTmemAcc + buf * 128 + c32 * 32, acc);
+          tmem_ld32(tq + kTmemAcc + buf * kBN + c32 * 32, acc);
           tmem_ld_wait();
           const uint32_t rbase = smem_u32(st + (c32 >> 1) * 16384) + static_cast<uint32_t>(m) * 128;
 #pragma unroll
@@ -524,7 +532,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
         if (m >= full_rows && m < tlen) {
           uint16_t* yrow = pr.y + static_cast<int64_t>(row + m) * pr.ldy;
 #pragma unroll 1
-          for (int j = 0; j < 16; ++j) {
+          for (int j = 0; j < kBN / 8; ++j) {
             const int col = c + j * 8;
             if (col < pr.h_out) {
               const uint32_t addr = smem_u32(st + (j >> 3) * 16384) + static_cast<uint32_t>(m) * 128 +
@@ -541,7 +549,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
         named_bar_sync(2, kTcEpiThreads);
         if (tid == 0) {
           for (int g = 0; g < full_rows; g += 32)
-            for (int h = 0; h < 2; ++h)
+            for (int h = 0; h < kBH; ++h)
               if (c + h * 64 < pr.h_out) tma_store_2d(&p.tmYs[pj], c + h * 64, row + g, st + h * 16384 + g * 128);
           bulk_commit();
           bulk_wait_read0();

@@ -428,6 +428,8 @@ def run_ours(args) -> None:
     }
     if mixed is not None:
         out["mixed_vs_single_us"] = mixed
+    if args.batch_curve:
+        out["batch_curve_us"] = batch_curve(K, Wm, dev, lsg, args.max_copies)
     if rank == 0 and world == 1 and not args.no_cpu:
         threads = os.cpu_count() or 1
         inp_cpu = make_inputs(wl, "cpu")
@@ -496,6 +498,73 @@ def _time_variant(name, K, Wm, dev, lsg, max_copies):
     return e0.elapsed_time(e1) / K * 1e3
 
 
+def _time_ids(wl, ids, K, Wm, dev, lsg, max_copies):
+    """Microseconds per step (segment + fused) of projection 0 of `wl` on the
+    given adapter ids (inputs rotated over copies that exceed twice the L2)."""
+    import torch
+
+    ids = np.asarray(ids, np.int32)
+    NB = max(2, min(max_copies, int(np.ceil(2.2 * L2_BYTES / algorithmic_bytes(wl, ids)))))
+    copies = []
+    for c in range(NB):
+        inp = make_inputs(wl, dev, copy=c, ids=ids)
+        copies.append((inp, lsg.Segments.empty(ids.size, wl.P, dev)))
+    p0 = wl.projs[0]
+    side = torch.cuda.Stream(dev)
+
+    def step(k):
+        inp, seg = copies[k % NB]
+        lsg.lora_segment(inp.ids, wl.P, out=seg)
+        lsg.sgmv_fused(inp.x[p0.x_key], inp.A[0], inp.B[0], seg, inp.y0[0], wl.scale)
+
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for k in range(max(Wm, NB)):
+            step(k)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for k in range(K):
+            step(k)
+    t = _time_graph(g, side) / K * 1e3
+    del g, copies
+    torch.cuda.empty_cache()
+    return round(t, 3)
+
+
+def batch_curve(K, Wm, dev, lsg, max_copies):
+    """Step latency against batch size, identical vs mixed adapters, for a
+    decode projection (Llama2-7B 4096->4096, r=16) and a prefill projection
+    (Llama2-13B 5120->5120, r=64): the kernel-level analogue of measuring
+    latency against batch size per stage (Punica: Multi-Tenant LoRA Serving,
+    "Interesting ideas" I5; "Key points": identical vs mixed adapters)."""
+    from workloads import Proj, Workload
+
+    out = {}
+    dec_n = [1, 4, 16, 32, 64, 128, 256]
+    rows = {"n": dec_n, "identical_us": [], "mixed_us": []}
+    for n in dec_n:
+        P = max(64, n)
+        wl = Workload("curve_dec", (Proj("proj", 4096, 4096, "x"),), 16, P, n, 1.0, lambda: None, "", "curve_dec")
+        rng = np.random.default_rng(n)
+        rows["identical_us"].append(_time_ids(wl, np.full(n, 3, np.int32), K, Wm, dev, lsg, max_copies))
+        rows["mixed_us"].append(_time_ids(wl, rng.choice(P, n, replace=False), K, Wm, dev, lsg, max_copies))
+    out["decode_llama2_7b_proj_r16"] = rows
+    pre_n = [128, 512, 1024, 2048, 4096]
+    rows = {"n": pre_n, "identical_us": [], "mixed_us": [], "mixed_requests": []}
+    for n in pre_n:
+        P = 32
+        wl = Workload("curve_pre", (Proj("proj", 5120, 5120, "x"),), 64, P, n, 1.0, lambda: None, "", "curve_pre")
+        nreq = max(1, n // 256)
+        mixed = np.repeat(np.arange(nreq, dtype=np.int32), n // nreq)
+        mixed = np.concatenate([mixed, np.full(n - mixed.size, nreq - 1, np.int32)])
+        rows["identical_us"].append(_time_ids(wl, np.zeros(n, np.int32), max(3, K // 4), Wm, dev, lsg, max_copies))
+        rows["mixed_us"].append(_time_ids(wl, mixed, max(3, K // 4), Wm, dev, lsg, max_copies))
+        rows["mixed_requests"].append(nreq)
+    out["prefill_llama2_13b_proj_r64"] = rows
+    return out
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -509,6 +578,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-mixed", action="store_true")
+    ap.add_argument("--batch-curve", action="store_true",
+                    help="add step latency against batch size (decode and prefill, identical vs mixed adapters)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
