@@ -11,18 +11,24 @@ from .lora_sgmv import (  # noqa: F401
     STATUS,
     SYMBOLS,
     Segments,
+    SlotTable,
     load_library,
     lora_segment,
     lora_segment_noalloc,
     lora_segment_workspace_bytes,
     make_projs,
+    make_slot_projs,
+    rank_mask,
     sgmv_expand,
     sgmv_fused,
+    sgmv_fused_slots,
     sgmv_multi,
+    sgmv_multi_slots,
     sgmv_shrink,
 )
 
 __all__ = [
     "Segments", "load_library", "lora_segment", "lora_segment_noalloc", "lora_segment_workspace_bytes", "sgmv_shrink", "sgmv_expand",
-    "sgmv_fused", "sgmv_multi", "make_projs",
+    "sgmv_fused", "sgmv_multi", "make_projs", "SlotTable", "rank_mask", "make_slot_projs", "sgmv_multi_slots",
+    "sgmv_fused_slots",
 ]

@@ -51,6 +51,14 @@ struct SgmvCall {
   float* v_out;       // shrink output [n][r]
   const float* v_in;  // expand input [n][r]
   int32_t* err_flag;
+  // Slot arenas (null slot_of: each pool is contiguous, [n_adapters] slabs of
+  // rank r).  Adapter a lives in slot slot_of[a] with rank rank_of[a], a bit
+  // of rank_mask (bit c: rank 8 << c); a slot holds rank <= r_max.
+  const int32_t* slot_of;
+  const int32_t* rank_of;
+  int n_slots;
+  int r_max;
+  unsigned rank_mask;
 };
 
 lora_status launch_sgmv_cc(const SgmvCall& call, cudaStream_t stream);

@@ -157,6 +157,44 @@ lora_status sgmv_multi(const lora_proj* projs, int32_t n_proj, int32_t n_adapter
   return launch_sgmv_cc(c, reinterpret_cast<cudaStream_t>(stream));
 }
 
+lora_status sgmv_multi_slots(const lora_proj* projs, int32_t n_proj, const lora_slot_table* table,
+                             const lora_segments* seg, int32_t* err_flag, lora_stream_t stream) {
+  if (!projs || n_proj < 1 || !table) return LORA_ERR_INVALID_ARG;
+  if (n_proj > LORA_MAX_PROJ) return LORA_ERR_UNSUPPORTED;
+  const lora_slot_table& t = *table;
+  lora_status s = check_seg(seg, t.n_adapters);
+  if (s != LORA_OK) return s;
+  if (!t.slot_of || !t.rank_of || t.n_slots < 1) return LORA_ERR_INVALID_ARG;
+  if (!al4(t.slot_of) || !al4(t.rank_of)) return LORA_ERR_MISALIGNED;
+  if (!rank_ok(t.r_max)) return LORA_ERR_UNSUPPORTED;
+  if (t.rank_mask == 0 || (t.rank_mask >> 4) != 0) return LORA_ERR_UNSUPPORTED;
+  for (int c = 0; c < 4; ++c)
+    if ((t.rank_mask & (1u << c)) && (8 << c) > t.r_max) return LORA_ERR_UNSUPPORTED;
+  if (seg->n_tokens == 0) return LORA_OK;
+  SgmvCall c{};
+  c.mode = kModeFused;
+  for (int i = 0; i < n_proj; ++i) {
+    const lora_proj& q = projs[i];
+    s = check_proj(q.x, q.ldx, q.A_pool, q.B_pool, q.y, q.ldy, q.h_in, q.h_out, true, true);
+    if (s != LORA_OK) return s;
+    // tensor-map rows: n_slots * h_in * r_max / 8 (A as rank-8 rows) and n_slots * r_max (B)
+    const int64_t cells = static_cast<int64_t>(t.n_slots) * t.r_max * std::max(q.h_in, q.h_out);
+    if (cells >= (int64_t{1} << 31)) return LORA_ERR_UNSUPPORTED;
+    c.proj[i] = ProjArgs{q.x, q.A_pool, q.B_pool, q.y, q.ldx, q.ldy, q.h_in, q.h_out, q.scale};
+  }
+  c.n_proj = n_proj;
+  c.r = t.r_max;
+  c.n_adapters = t.n_adapters;
+  c.seg = *seg;
+  c.err_flag = err_flag;
+  c.slot_of = t.slot_of;
+  c.rank_of = t.rank_of;
+  c.n_slots = t.n_slots;
+  c.r_max = t.r_max;
+  c.rank_mask = t.rank_mask;
+  return launch_sgmv_cc(c, reinterpret_cast<cudaStream_t>(stream));
+}
+
 lora_status sgmv_fused(const lora_bf16* x, int64_t ldx, const lora_bf16* A_pool, const lora_bf16* B_pool,
                        int32_t n_adapters, int32_t h_in, int32_t h_out, int32_t r, float scale,
                        const lora_segments* seg, lora_bf16* y, int64_t ldy, int32_t* err_flag,

@@ -38,11 +38,21 @@
 //
 // Modes: shrink (v -> device memory), expand (v from device memory, no
 // cluster), fused (v on chip).
+//
+// Adapter pools: a contiguous pool ([n_adapters][h_in][r], one rank) or slot
+// arenas (fixed-size slots of capacity r_max, adapter a in slot slot_of[a]
+// with rank rank_of[a], its A packed as [h_in][rank] and its B as
+// [rank][h_out] at the slot start).  A kernel compiled for a set of ranks
+// takes each item's rank from the table and runs the rank's code (fragment
+// counts, swizzle, stage shape) for that item; the ring is shaped for the
+// largest rank of the set.  Ranks stay far below the hidden size and
+// adapters of different ranks share a batch ([Punica-el] "Key points").
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -81,6 +91,31 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
 enum : int { kStShrink = 1, kStExpand = 2, kStFirst = 4, kStLast = 8, kStEnd = 16 };
 
+// A set of ranks as bits: 8 -> 1, 16 -> 2, 32 -> 4, 64 -> 8.
+constexpr int kAllRanks = 15;
+__host__ __device__ constexpr int rank_bit(int r) { return r == 8 ? 1 : r == 16 ? 2 : r == 32 ? 4 : r == 64 ? 8 : 0; }
+__host__ __device__ constexpr int rank_class(int r) { return r == 8 ? 0 : r == 16 ? 1 : r == 32 ? 2 : 3; }
+__host__ __device__ constexpr int set_max_rank(int set) { return (set & 8) ? 64 : (set & 4) ? 32 : (set & 2) ? 16 : 8; }
+__host__ __device__ constexpr bool single_rank(int set) { return set == 1 || set == 2 || set == 4 || set == 8; }
+
+// Runs f(integral_constant<int, r>) for the rank r of the set (a single-rank
+// set needs no test).
+template <int RSET, class F>
+__device__ __forceinline__ void with_rank(int r, F&& f) {
+  if constexpr (single_rank(RSET)) {
+    f(std::integral_constant<int, set_max_rank(RSET)>{});
+  } else {
+    if constexpr ((RSET & 1) != 0)
+      if (r == 8) return f(std::integral_constant<int, 8>{});
+    if constexpr ((RSET & 2) != 0)
+      if (r == 16) return f(std::integral_constant<int, 16>{});
+    if constexpr ((RSET & 4) != 0)
+      if (r == 32) return f(std::integral_constant<int, 32>{});
+    if constexpr ((RSET & 8) != 0)
+      if (r == 64) return f(std::integral_constant<int, 64>{});
+  }
+}
+
 struct CCProj {
   const uint16_t* x;
   const uint16_t* A;
@@ -89,8 +124,6 @@ struct CCProj {
   int64_t ldx, ldy;
   int32_t h_in, h_out;
   int32_t k_chunk, n_chunk;  // rows of A / columns of B per rank (k_chunk: multiple of 16)
-  int32_t bw;                // TMA box width of B (columns, an odd multiple of 8)
-  int32_t nb;                // B boxes per expand stage
   float scale;
 };
 
@@ -111,18 +144,31 @@ struct CCTail {
   int32_t n_adapters;
   int32_t csplit;     // C
   int32_t skip_long;  // segments of >= kLongSeg contiguous tokens belong to the tensor-tile kernel
+  const int32_t* slot_of;  // slot of each adapter (null: adapter a lives in slot a)
+  const int32_t* rank_of;  // rank of each adapter (null: every adapter has the kernel's rank)
+  int32_t n_slots;
+  int32_t rmax;                    // slot capacity in ranks (the contiguous pool: its rank)
+  int32_t rank_mask;               // ranks that have tensor maps in this launch (rank_bit)
+  int32_t map_of[kMaxProj][4];     // tensor-map pair of (projection, rank class), -1: none
+  int32_t map_bw[kMaxProj];        // B box width of a map pair (columns, an odd multiple of 8)
+  int32_t map_nb[kMaxProj];        // B boxes per expand stage of a map pair
 };
 
+// Map pair m serves one (projection, rank r): tmA views the projection's A
+// storage as 2-D rows of r elements ([n_slots*h_in*rmax/r][r], box {r, BA}:
+// slot s starts at row s*h_in*rmax/r), tmB views its B storage as
+// [n_slots*rmax][h_out] (box {bw, r}: slot s starts at row s*rmax).
 struct CCParams {
-  CUtensorMap tmA[kMaxProj];  // A_pool of projection p as 2-D [n_adapters*h_in][r], box {r, BA}
-  CUtensorMap tmB[kMaxProj];  // B_pool of projection p as 2-D [n_adapters*r][h_out], box {bw, r}
+  CUtensorMap tmA[kMaxProj];
+  CUtensorMap tmB[kMaxProj];
   CCTail t;
 };
 
-template <int R, int T>
+// Rank R's stage contents in a ring shaped for rank RM >= R.
+template <int R, int T, int RM = R>
 struct CCCfg {
-  static constexpr int kStages = R >= 64 ? LSG_CC_STAGES_BIG : LSG_CC_STAGES_SMALL;
-  static constexpr int kStageBytes = (R >= 64 ? LSG_CC_KB_BIG : LSG_CC_KB_SMALL) * 1024;
+  static constexpr int kStages = RM >= 64 ? LSG_CC_STAGES_BIG : LSG_CC_STAGES_SMALL;
+  static constexpr int kStageBytes = (RM >= 64 ? LSG_CC_KB_BIG : LSG_CC_KB_SMALL) * 1024;
   // shrink: A rows per stage (A part + x part fit a stage), whole k-steps of
   // 16, made of NBA TMA boxes of BA rows (a box extent is at most 256)
   static constexpr int WS0 = (((kStageBytes - T * 16) / ((R + T) * 2)) / 16) * 16;
@@ -149,9 +195,12 @@ struct StageHdr {
   int32_t len;    // rows (shrink) or columns (expand) in this stage
   int32_t off;    // first row / column
   int32_t pitch;  // expand: box width (columns) of the B part
+  int32_t rk;     // the item's rank
   int32_t tok[T];
 };
 
+// Shared memory of a kernel whose largest rank is R (smaller ranks use the
+// leading part of red / xbuf / vfull, as [.][T][r] arrays).
 template <int R, int T>
 struct CCSmem {
   static constexpr int kStages = CCCfg<R, T>::kStages;
@@ -187,12 +236,15 @@ template <int T>
 struct SegCursor {
   int base = 0, tiles_before = 0, S = 0;
   int off = 0, len = 0, ad = -1;  // segment base + lane
+  int sl = -1, rk = 0;            // its adapter's slot and rank (0: the kernel's rank)
 
   __device__ void load(const CCTail& q, int lane, int bound) {
     const int s = base + lane;
     off = 0;
     len = 0;
     ad = -1;
+    sl = -1;
+    rk = 0;
     if (s < bound) {
       const int o = q.seg_offsets[s];
       const int e = q.seg_offsets[s + 1];
@@ -202,6 +254,11 @@ struct SegCursor {
       if (q.skip_long && len >= kLongSeg) {
         const int f = q.perm[o], b = q.perm[e - 1];
         if (f >= 0 && b < q.n_tokens && b - f == len - 1) len = 0;  // taken by the tensor-tile kernel
+      }
+      sl = ad;
+      if (q.slot_of != nullptr && ad >= 0 && ad < q.n_adapters) {
+        sl = q.slot_of[ad];
+        rk = q.rank_of[ad];
       }
     }
   }
@@ -213,7 +270,7 @@ struct SegCursor {
     if (lane >= S) len = 0;
   }
 
-  __device__ bool find(const CCTail& q, int lane, int tile, int& t0, int& tlen, int& a) {
+  __device__ bool find(const CCTail& q, int lane, int tile, int& t0, int& tlen, int& a, int& slot, int& r) {
     while (base < S) {
       const int tl = (len + T - 1) / T;
       int inc = tl;
@@ -230,6 +287,8 @@ struct SegCursor {
         const int o = __shfl_sync(0xffffffffu, off, ls);
         const int l = __shfl_sync(0xffffffffu, len, ls);
         a = __shfl_sync(0xffffffffu, ad, ls);
+        slot = __shfl_sync(0xffffffffu, sl, ls);
+        r = __shfl_sync(0xffffffffu, rk, ls);
         t0 = o + (tile - tiles_before - excl) * T;
         tlen = min(T, o + l - t0);
         return true;
@@ -242,16 +301,17 @@ struct SegCursor {
   }
 };
 
-template <int R, int T, int MODE>
+// RSET: the ranks this kernel runs (a single rank for a contiguous pool or a
+// one-rank slot table; several for a slot table of mixed ranks).
+template <int RSET, int T, int MODE>
 __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant__ CCParams p) {
-  using Cfg = CCCfg<R, T>;
-  constexpr int kStages = Cfg::kStages;
-  constexpr int WS = Cfg::WS;
-  constexpr int NT = Cfg::NT;
+  constexpr int RM = set_max_rank(RSET);
+  using CfgM = CCCfg<RM, T>;
+  constexpr int kStages = CfgM::kStages;
   constexpr bool kHasShrink = (MODE & kModeShrink) != 0;
   constexpr bool kHasExpand = (MODE & kModeExpand) != 0;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  auto& sm = *reinterpret_cast<CCSmem<R, T>*>(smem_raw);
+  auto& sm = *reinterpret_cast<CCSmem<RM, T>*>(smem_raw);
   const CCTail& q = sm.t;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -302,7 +362,7 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
     if (!ring_ok && lane == 0) set_err(q.err_flag, LORA_ERR_UNSUPPORTED);
     SegCursor<T> cur;
     cur.init(q, lane);
-    int last_tile = -1, a = -1, t0 = 0, tlen = 0, tok = -1, ntok = 0, tk = -1;
+    int last_tile = -1, a = -1, sl = -1, rk = 0, t0 = 0, tlen = 0, tok = -1, ntok = 0, tk = -1;
     bool tile_ok = false, tok_ready = false;
 
     auto acquire = [&]() -> bool {
@@ -338,6 +398,7 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
         h.len = len;
         h.off = off;
         h.pitch = pitch;
+        h.rk = rk;
       }
       __syncwarp();
     };
@@ -346,72 +407,81 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
       const int tile = item / q.n_proj;
       const int pj = item - tile * q.n_proj;
       if (tile != last_tile) {
-        if (!cur.find(q, lane, tile, t0, tlen, a)) break;
+        if (!cur.find(q, lane, tile, t0, tlen, a, sl, rk)) break;
         last_tile = tile;
         tk = -1;
         if (lane < tlen) tk = q.perm[t0 + lane];  // consumed after the first A copy is issued
         tok_ready = false;
-        tile_ok = (a >= 0 && a < q.n_adapters);
+        if (rk == 0) rk = RM;
+        // a rank outside the launch's mask has no tensor map: the item is skipped
+        tile_ok = a >= 0 && a < q.n_adapters && sl >= 0 && sl < q.n_slots &&
+                  (rank_bit(rk) & RSET & q.rank_mask) != 0 && rk <= q.rmax;
         if (!tile_ok && lane == 0) set_err(q.err_flag, LORA_ERR_BAD_ADAPTER_ID);
       }
       if (!tile_ok) continue;  // every CTA of the cluster skips it alike
       const CCProj& pr = q.proj[pj];
 
-      if (kHasShrink) {
-        const int k0 = rank * pr.k_chunk;
-        const int klen = max(0, min(pr.h_in, k0 + pr.k_chunk) - k0);
-        const int nst = max(1, (klen + WS - 1) / WS);
-        const int per = ((klen + nst - 1) / nst + 15) & ~15;
-        const int arow = a * pr.h_in;  // first pool row of the adapter
-        for (int st = 0; st < nst; ++st) {
-          const int r0 = k0 + st * per;
-          const int rl = max(0, min(per, k0 + klen - r0));
-          const int nbx = (rl + Cfg::BA - 1) / Cfg::BA;  // A boxes in this stage
-          if (!acquire()) {
-            failed = true;
-            break;
+      with_rank<RSET>(rk, [&](auto rc) {
+        constexpr int R = decltype(rc)::value;
+        using Cfg = CCCfg<R, T, RM>;
+        const int mi = q.map_of[pj][rank_class(R)];
+        if (kHasShrink) {
+          const int k0 = rank * pr.k_chunk;
+          const int klen = max(0, min(pr.h_in, k0 + pr.k_chunk) - k0);
+          const int nst = max(1, (klen + Cfg::WS - 1) / Cfg::WS);
+          const int per = ((klen + nst - 1) / nst + 15) & ~15;
+          const int arow = sl * pr.h_in * (q.rmax / R);  // first row of the adapter's A in the map
+          for (int st = 0; st < nst; ++st) {
+            const int r0 = k0 + st * per;
+            const int rl = max(0, min(per, k0 + klen - r0));
+            const int nbx = (rl + Cfg::BA - 1) / Cfg::BA;  // A boxes in this stage
+            if (!acquire()) {
+              failed = true;
+              break;
+            }
+            uint8_t* st_base = sm.ring[slot];
+            if (lane == 0 && nbx) mbar_expect_tx(&sm.full[slot], static_cast<uint32_t>(nbx) * Cfg::BA * R * 2u);
+            if (lane < nbx)
+              tma_load_2d(st_base + lane * Cfg::BA * R * 2, &p.tmA[mi], 0, arow + r0 + lane * Cfg::BA,
+                          &sm.full[slot]);
+            if (!tok_ready) resolve_tok();
+            header(kStShrink | (st == 0 ? kStFirst : 0) | (st == nst - 1 ? kStLast : 0), pj, rl, r0, 0);
+            if (lane == 0) mbar_arrive_expect_tx(&sm.full[slot], static_cast<uint32_t>(rl) * 2u * ntok);
+            if (rl > 0 && tok >= 0)
+              bulk_g2s(st_base + Cfg::kPartBytes + lane * Cfg::XP * 2,
+                       pr.x + static_cast<int64_t>(tok) * pr.ldx + r0, rl * 2, &sm.full[slot]);
+            advance();
           }
-          uint8_t* st_base = sm.ring[slot];
-          if (lane == 0 && nbx) mbar_expect_tx(&sm.full[slot], static_cast<uint32_t>(nbx) * Cfg::BA * R * 2u);
-          if (lane < nbx)
-            tma_load_2d(st_base + lane * Cfg::BA * R * 2, &p.tmA[pj], 0, arow + r0 + lane * Cfg::BA,
-                        &sm.full[slot]);
+        }
+        if (kHasExpand && !failed) {
+          const int c0 = rank * pr.n_chunk;
+          const int clen = max(0, min(pr.h_out, c0 + pr.n_chunk) - c0);
+          const int bw = q.map_bw[mi];
+          const int sc = bw * q.map_nb[mi];  // columns per stage
+          const int nst = (clen + sc - 1) / sc;
+          const int brow = sl * q.rmax;  // first row of the adapter's B in the map
           if (!tok_ready) resolve_tok();
-          header(kStShrink | (st == 0 ? kStFirst : 0) | (st == nst - 1 ? kStLast : 0), pj, rl, r0, 0);
-          if (lane == 0) mbar_arrive_expect_tx(&sm.full[slot], static_cast<uint32_t>(rl) * 2u * ntok);
-          if (rl > 0 && tok >= 0)
-            bulk_g2s(st_base + Cfg::kPartBytes + lane * Cfg::XP * 2, pr.x + static_cast<int64_t>(tok) * pr.ldx + r0,
-                     rl * 2, &sm.full[slot]);
-          advance();
-        }
-      }
-      if (kHasExpand && !failed) {
-        const int c0 = rank * pr.n_chunk;
-        const int clen = max(0, min(pr.h_out, c0 + pr.n_chunk) - c0);
-        const int bw = pr.bw;
-        const int sc = bw * pr.nb;  // columns per stage
-        const int nst = (clen + sc - 1) / sc;
-        if (!tok_ready) resolve_tok();
-        for (int st = 0; st < nst; ++st) {
-          const int cc = c0 + st * sc;
-          const int cl = min(sc, c0 + clen - cc);
-          const int nbs = (cl + bw - 1) / bw;  // boxes in this stage
-          if (!acquire()) {
-            failed = true;
-            break;
+          for (int st = 0; st < nst; ++st) {
+            const int cc = c0 + st * sc;
+            const int cl = min(sc, c0 + clen - cc);
+            const int nbs = (cl + bw - 1) / bw;  // boxes in this stage
+            if (!acquire()) {
+              failed = true;
+              break;
+            }
+            uint8_t* st_base = sm.ring[slot];
+            if (lane == 0) mbar_expect_tx(&sm.full[slot], static_cast<uint32_t>(nbs) * bw * R * 2u);
+            if (lane < nbs)
+              tma_load_2d(st_base + lane * bw * R * 2, &p.tmB[mi], cc + lane * bw, brow, &sm.full[slot]);
+            header(kStExpand | (st == 0 ? kStFirst : 0) | (st == nst - 1 ? kStLast : 0), pj, cl, cc, bw);
+            if (lane == 0) mbar_arrive_expect_tx(&sm.full[slot], static_cast<uint32_t>(cl) * 2u * ntok);
+            if (tok >= 0)
+              bulk_g2s(st_base + Cfg::kPartBytes + lane * Cfg::XP * 2,
+                       pr.y + static_cast<int64_t>(tok) * pr.ldy + cc, cl * 2, &sm.full[slot]);
+            advance();
           }
-          uint8_t* st_base = sm.ring[slot];
-          if (lane == 0) mbar_expect_tx(&sm.full[slot], static_cast<uint32_t>(nbs) * bw * R * 2u);
-          if (lane < nbs)
-            tma_load_2d(st_base + lane * bw * R * 2, &p.tmB[pj], cc + lane * bw, a * R, &sm.full[slot]);
-          header(kStExpand | (st == 0 ? kStFirst : 0) | (st == nst - 1 ? kStLast : 0), pj, cl, cc, bw);
-          if (lane == 0) mbar_arrive_expect_tx(&sm.full[slot], static_cast<uint32_t>(cl) * 2u * ntok);
-          if (tok >= 0)
-            bulk_g2s(st_base + Cfg::kPartBytes + lane * Cfg::XP * 2, pr.y + static_cast<int64_t>(tok) * pr.ldy + cc,
-                     cl * 2, &sm.full[slot]);
-          advance();
         }
-      }
+      });
     }
     if (!failed && acquire()) {
       if (lane == 0) {
@@ -441,9 +511,10 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
   uint32_t phase = 0;
   int nx = 0;  // partial-v exchanges done
   bool start_waited = false;
-  float acc[NT][4];  // this warp's partial v: rows g, g+8 of every 8-rank n-tile
+  // (sized for the largest rank; a smaller rank uses the leading entries)
+  float acc[CfgM::NT][4];  // this warp's partial v: rows g, g+8 of every 8-rank n-tile
   // expand operands: v as bf16 hi/lo MMA A fragments (per 16-rank k-step)
-  constexpr int KSA = Cfg::KS > 0 ? Cfg::KS : 1;
+  constexpr int KSA = CfgM::KS > 0 ? CfgM::KS : 1;
   uint32_t vah[KSA][4], val[KSA][4];
   uint32_t v8h[2] = {0u, 0u}, v8l[2] = {0u, 0u};  // r = 8: one m16n8k8 A fragment
 #pragma unroll
@@ -451,9 +522,10 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
 #pragma unroll
     for (int e = 0; e < 4; ++e) vah[ks][e] = val[ks][e] = 0u;
 #pragma unroll
-  for (int n = 0; n < NT; ++n)
+  for (int n = 0; n < CfgM::NT; ++n)
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
+  bool quit = false;
 
   for (;;) {
     bool ok = true;
@@ -469,298 +541,309 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
     const int tlen = h.tlen, len = h.len, off = h.off, pj = h.proj;
     const uint8_t* st_base = sm.ring[slot];
 
-    if (kind & kStShrink) {
-      const int b = nx & 1;
-      if (kind & kStFirst) {
-#pragma unroll
-        for (int n = 0; n < NT; ++n)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
-        if (xchg && ct == 0)
-          mbar_arrive_expect_tx(&sm.xbar[b], static_cast<uint32_t>(C - 1) * T * R * 4u);
-      }
-      // ---- v[t, :] += x[t, k-range] . A[k-range, :]  (tokens = MMA rows)
-      const uint32_t a_base = smem_u32(st_base);
-      const uint32_t x_base = a_base + Cfg::kPartBytes;
-      const int nk16 = len >> 4;
-      // x fragment (A operand): lane L gives row (L/8 & 1)*8 + L%8, k offset (L/16)*8 of the
-      // 16x16 block; rows past the tile read the zero row
-      const int xrow = (lm & 1) * 8 + lr;
-      const uint32_t xaddr0 = xrow < tlen ? x_base + static_cast<uint32_t>(xrow * Cfg::XP + (lm >> 1) * 8) * 2
-                                          : smem_u32(sm.zero_row);
-      const uint32_t xstep = xrow < tlen ? 32u : 0u;  // bytes per k-step of 16
-      // A fragment (B operand, swizzled rows of R ranks): per-lane offset, independent of the k-step
-      const int krow = (lm & 1) * 8 + lr;
-      auto step = [&](int ks, float (&ac)[NT][4]) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(xaddr0 + static_cast<uint32_t>(ks) * xstep, a0, a1, a2, a3);
-        const uint32_t kbase = a_base + static_cast<uint32_t>(ks) * (16 * R * 2);
-        if constexpr (NT == 1) {
-          // r = 8: matrices (k 0-7), (k 8-15) of the single n-tile; lanes 16+ repeat 0-15
-          uint32_t b0, b1;
-          ldsm_x2_trans(kbase + static_cast<uint32_t>(krow) * (R * 2), b0, b1);
-          mma_bf16_16816(ac[0], a0, a1, a2, a3, b0, b1);
-        } else {
-#pragma unroll
-          for (int np = 0; np < NT / 2; ++np) {
-            // matrices: (k 0-7, n 0-7), (k 8-15, n 0-7), (k 0-7, n 8-15), (k 8-15, n 8-15) of the pair
-            const uint32_t off = swz<Cfg::SWM>(static_cast<uint32_t>(krow) * (R * 2) +
-                                               static_cast<uint32_t>(np * 16 + (lm >> 1) * 8) * 2);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_trans(kbase + off, b0, b1, b2, b3);
-            mma_bf16_16816(ac[2 * np], a0, a1, a2, a3, b0, b1);
-            mma_bf16_16816(ac[2 * np + 1], a0, a1, a2, a3, b2, b3);
-          }
+    with_rank<RSET>(h.rk, [&](auto rc) {
+      constexpr int R = decltype(rc)::value;
+      using Cfg = CCCfg<R, T, RM>;
+      constexpr int NT = Cfg::NT;
+      // this rank's views of the exchange buffers
+      auto& red = *reinterpret_cast<float(*)[kCW][T][R]>(&sm.red[0][0][0]);
+      auto& xbuf = *reinterpret_cast<float(*)[kXB][kMaxC][T][R]>(&sm.xbuf[0][0][0][0]);
+      auto& vfull = *reinterpret_cast<float(*)[T][R]>(&sm.vfull[0][0]);
+      if (kind & kStShrink) {
+        const int b = nx & 1;
+        if (kind & kStFirst) {
+  #pragma unroll
+          for (int n = 0; n < NT; ++n)
+  #pragma unroll
+            for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
+          if (xchg && ct == 0)
+            mbar_arrive_expect_tx(&sm.xbar[b], static_cast<uint32_t>(C - 1) * T * R * 4u);
         }
-      };
-      {
-        // two k-steps per iteration into independent accumulators (overlaps the MMA latency)
-        float ac2[NT][4];
-#pragma unroll
-        for (int n = 0; n < NT; ++n)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) ac2[n][e] = 0.f;
-        int ks = warp;
-        for (; ks + kCW < nk16; ks += 2 * kCW) {
-          step(ks, acc);
-          step(ks + kCW, ac2);
-        }
-        if (ks < nk16) step(ks, acc);
-#pragma unroll
-        for (int n = 0; n < NT; ++n)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[n][e] += ac2[n][e];
-      }
-      if ((len & 8) && warp == (nk16 % kCW)) {
-        // tail of 8 rows (h_in is a multiple of 8): m16n8k8
-        const int kb = nk16 * 16;
-        const uint16_t* Xs = reinterpret_cast<const uint16_t*>(st_base + Cfg::kPartBytes);
-        const uint32_t a0 = g < tlen ? ld_shared_u32(Xs + g * Cfg::XP + kb + 2 * tig) : 0u;
-        const uint32_t a1 = g + 8 < tlen ? ld_shared_u32(Xs + (g + 8) * Cfg::XP + kb + 2 * tig) : 0u;
-        if constexpr (NT == 1) {
-          uint32_t b0, b1;  // b1 (lanes 8-15's rows) is not used
-          ldsm_x2_trans(a_base + static_cast<uint32_t>(kb + lr) * (R * 2), b0, b1);
-          mma_bf16_1688(acc[0], a0, a1, b0);
-        } else {
-#pragma unroll
-          for (int np = 0; np < NT / 2; ++np) {
-            // matrices: (k 0-7, n 0-7), (k 0-7, n 8-15) of the pair
-            const uint32_t addr = swz<Cfg::SWM>(a_base + static_cast<uint32_t>(kb + lr) * (R * 2) +
-                                                static_cast<uint32_t>(np * 16 + (lm & 1) * 8) * 2);
+        // ---- v[t, :] += x[t, k-range] . A[k-range, :]  (tokens = MMA rows)
+        const uint32_t a_base = smem_u32(st_base);
+        const uint32_t x_base = a_base + Cfg::kPartBytes;
+        const int nk16 = len >> 4;
+        // x fragment (A operand): lane L gives row (L/8 & 1)*8 + L%8, k offset (L/16)*8 of the
+        // 16x16 block; rows past the tile read the zero row
+        const int xrow = (lm & 1) * 8 + lr;
+        const uint32_t xaddr0 = xrow < tlen ? x_base + static_cast<uint32_t>(xrow * Cfg::XP + (lm >> 1) * 8) * 2
+                                            : smem_u32(sm.zero_row);
+        const uint32_t xstep = xrow < tlen ? 32u : 0u;  // bytes per k-step of 16
+        // A fragment (B operand, swizzled rows of R ranks): per-lane offset, independent of the k-step
+        const int krow = (lm & 1) * 8 + lr;
+        auto step = [&](int ks, auto& ac) {  // ac: float[>= NT][4]
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(xaddr0 + static_cast<uint32_t>(ks) * xstep, a0, a1, a2, a3);
+          const uint32_t kbase = a_base + static_cast<uint32_t>(ks) * (16 * R * 2);
+          if constexpr (NT == 1) {
+            // r = 8: matrices (k 0-7), (k 8-15) of the single n-tile; lanes 16+ repeat 0-15
             uint32_t b0, b1;
-            ldsm_x2_trans(addr, b0, b1);
-            mma_bf16_1688(acc[2 * np], a0, a1, b0);
-            mma_bf16_1688(acc[2 * np + 1], a0, a1, b1);
-          }
-        }
-      }
-      if (!(kind & kStLast)) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[slot]);  // header and data of this slot no longer read
-      } else {
-        // the slot is released before the exchange, so the producer keeps streaming
-        int tokr[T];
-#pragma unroll
-        for (int t = 0; t < T; ++t) tokr[t] = h.tok[t];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[slot]);
-        // ---- this warp's partial v to shared memory, then the sum over warps
-#pragma unroll
-        for (int n = 0; n < NT; ++n) {
-          if (g < T) {
-            sm.red[warp][g][n * 8 + 2 * tig] = acc[n][0];
-            sm.red[warp][g][n * 8 + 2 * tig + 1] = acc[n][1];
-          }
-          if (g + 8 < T) {
-            sm.red[warp][g + 8][n * 8 + 2 * tig] = acc[n][2];
-            sm.red[warp][g + 8][n * 8 + 2 * tig + 1] = acc[n][3];
-          }
-        }
-        consumer_sync();
-        constexpr int kV4 = T * R / 4;  // float4 elements of one partial v
-        auto red_sum = [&](int i) {
-          float4 vp = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int w = 0; w < kCW; ++w) {
-            const float4 u = reinterpret_cast<const float4*>(&sm.red[w][0][0])[i];
-            vp.x += u.x;
-            vp.y += u.y;
-            vp.z += u.z;
-            vp.w += u.w;
-          }
-          return vp;
-        };
-        if (xchg) {
-          if (!start_waited) {
-            cluster_wait_acquire();  // every peer's mbarriers are initialised
-            start_waited = true;
-          }
-          const uint32_t bar = smem_u32(&sm.xbar[b]);
-          for (int i = ct; i < kV4; i += kCThreads) {
-            const float4 vp = red_sum(i);
-            reinterpret_cast<float4*>(&sm.xbuf[b][rank][0][0])[i] = vp;
-            const uint32_t src = smem_u32(&sm.xbuf[b][rank][0][0]) + i * 16;
-            for (int qq = 0; qq < C; ++qq)
-              if (qq != rank) st_async_v4(mapa_shared(src, qq), vp, mapa_shared(bar, qq));
-          }
-          bool got = true;
-          if (lane == 0) got = mbar_wait(&sm.xbar[b], (nx >> 1) & 1, kWaitLimitNs);
-          got = __shfl_sync(0xffffffffu, got, 0);
-          if (!got) {
-            if (lane == 0) set_err(q.err_flag, LORA_ERR_TIMEOUT);
-            return;
-          }
-          consumer_sync();  // our own partial (plain stores) is visible to every consumer
-          for (int i = ct; i < kV4; i += kCThreads) {
-            float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int qq = 0; qq < C; ++qq) {  // fixed order: identical v in every CTA
-              const float4 u = reinterpret_cast<const float4*>(&sm.xbuf[b][qq][0][0])[i];
-              sum.x += u.x;
-              sum.y += u.y;
-              sum.z += u.z;
-              sum.w += u.w;
+            ldsm_x2_trans(kbase + static_cast<uint32_t>(krow) * (R * 2), b0, b1);
+            mma_bf16_16816(ac[0], a0, a1, a2, a3, b0, b1);
+          } else {
+  #pragma unroll
+            for (int np = 0; np < NT / 2; ++np) {
+              // matrices: (k 0-7, n 0-7), (k 8-15, n 0-7), (k 0-7, n 8-15), (k 8-15, n 8-15) of the pair
+              const uint32_t off = swz<Cfg::SWM>(static_cast<uint32_t>(krow) * (R * 2) +
+                                                 static_cast<uint32_t>(np * 16 + (lm >> 1) * 8) * 2);
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4_trans(kbase + off, b0, b1, b2, b3);
+              mma_bf16_16816(ac[2 * np], a0, a1, a2, a3, b0, b1);
+              mma_bf16_16816(ac[2 * np + 1], a0, a1, a2, a3, b2, b3);
             }
-            reinterpret_cast<float4*>(&sm.vfull[0][0])[i] = sum;
           }
+        };
+        {
+          // two k-steps per iteration into independent accumulators (overlaps the MMA latency)
+          float ac2[NT][4];
+  #pragma unroll
+          for (int n = 0; n < NT; ++n)
+  #pragma unroll
+            for (int e = 0; e < 4; ++e) ac2[n][e] = 0.f;
+          int ks = warp;
+          for (; ks + kCW < nk16; ks += 2 * kCW) {
+            step(ks, acc);
+            step(ks + kCW, ac2);
+          }
+          if (ks < nk16) step(ks, acc);
+  #pragma unroll
+          for (int n = 0; n < NT; ++n)
+  #pragma unroll
+            for (int e = 0; e < 4; ++e) acc[n][e] += ac2[n][e];
+        }
+        if ((len & 8) && warp == (nk16 % kCW)) {
+          // tail of 8 rows (h_in is a multiple of 8): m16n8k8
+          const int kb = nk16 * 16;
+          const uint16_t* Xs = reinterpret_cast<const uint16_t*>(st_base + Cfg::kPartBytes);
+          const uint32_t a0 = g < tlen ? ld_shared_u32(Xs + g * Cfg::XP + kb + 2 * tig) : 0u;
+          const uint32_t a1 = g + 8 < tlen ? ld_shared_u32(Xs + (g + 8) * Cfg::XP + kb + 2 * tig) : 0u;
+          if constexpr (NT == 1) {
+            uint32_t b0, b1;  // b1 (lanes 8-15's rows) is not used
+            ldsm_x2_trans(a_base + static_cast<uint32_t>(kb + lr) * (R * 2), b0, b1);
+            mma_bf16_1688(acc[0], a0, a1, b0);
+          } else {
+  #pragma unroll
+            for (int np = 0; np < NT / 2; ++np) {
+              // matrices: (k 0-7, n 0-7), (k 0-7, n 8-15) of the pair
+              const uint32_t addr = swz<Cfg::SWM>(a_base + static_cast<uint32_t>(kb + lr) * (R * 2) +
+                                                  static_cast<uint32_t>(np * 16 + (lm & 1) * 8) * 2);
+              uint32_t b0, b1;
+              ldsm_x2_trans(addr, b0, b1);
+              mma_bf16_1688(acc[2 * np], a0, a1, b0);
+              mma_bf16_1688(acc[2 * np + 1], a0, a1, b1);
+            }
+          }
+        }
+        if (!(kind & kStLast)) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.empty[slot]);  // header and data of this slot no longer read
         } else {
-          for (int i = ct; i < kV4; i += kCThreads) reinterpret_cast<float4*>(&sm.vfull[0][0])[i] = red_sum(i);
-        }
-        consumer_sync();
-        ++nx;
-        if (MODE == kModeShrink && rank == 0) {
-          for (int idx = ct; idx < tlen * R; idx += kCThreads) {
-            const int t = idx / R, k = idx % R;
-            int tkv = -1;
-#pragma unroll
-            for (int u = 0; u < T; ++u)
-              if (u == t) tkv = tokr[u];
-            if (tkv >= 0) q.v_out[static_cast<int64_t>(tkv) * R + k] = sm.vfull[t][k];
-          }
-        }
-      }
-    } else {
-      // ---- expand stage: y[tok, off .. off+len) += s * vfull[t] . B[:, off .. off+len)
-      if (kind & kStFirst) {
-        if (MODE == kModeExpand) {
-          consumer_sync();  // every warp is done with the previous item's v
-          for (int idx = ct; idx < T * R; idx += kCThreads) {
-            const int t = idx / R, k = idx % R;
-            const int tk = t < tlen ? h.tok[t] : -1;
-            sm.vfull[t][k] = tk >= 0 ? q.v_in[static_cast<int64_t>(tk) * R + k] : 0.f;
+          // the slot is released before the exchange, so the producer keeps streaming
+          int tokr[T];
+  #pragma unroll
+          for (int t = 0; t < T; ++t) tokr[t] = h.tok[t];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.empty[slot]);
+          // ---- this warp's partial v to shared memory, then the sum over warps
+  #pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            if (g < T) {
+              red[warp][g][n * 8 + 2 * tig] = acc[n][0];
+              red[warp][g][n * 8 + 2 * tig + 1] = acc[n][1];
+            }
+            if (g + 8 < T) {
+              red[warp][g + 8][n * 8 + 2 * tig] = acc[n][2];
+              red[warp][g + 8][n * 8 + 2 * tig + 1] = acc[n][3];
+            }
           }
           consumer_sync();
+          constexpr int kV4 = T * R / 4;  // float4 elements of one partial v
+          auto red_sum = [&](int i) {
+            float4 vp = make_float4(0.f, 0.f, 0.f, 0.f);
+  #pragma unroll
+            for (int w = 0; w < kCW; ++w) {
+              const float4 u = reinterpret_cast<const float4*>(&red[w][0][0])[i];
+              vp.x += u.x;
+              vp.y += u.y;
+              vp.z += u.z;
+              vp.w += u.w;
+            }
+            return vp;
+          };
+          if (xchg) {
+            if (!start_waited) {
+              cluster_wait_acquire();  // every peer's mbarriers are initialised
+              start_waited = true;
+            }
+            const uint32_t bar = smem_u32(&sm.xbar[b]);
+            for (int i = ct; i < kV4; i += kCThreads) {
+              const float4 vp = red_sum(i);
+              reinterpret_cast<float4*>(&xbuf[b][rank][0][0])[i] = vp;
+              const uint32_t src = smem_u32(&xbuf[b][rank][0][0]) + i * 16;
+              for (int qq = 0; qq < C; ++qq)
+                if (qq != rank) st_async_v4(mapa_shared(src, qq), vp, mapa_shared(bar, qq));
+            }
+            bool got = true;
+            if (lane == 0) got = mbar_wait(&sm.xbar[b], (nx >> 1) & 1, kWaitLimitNs);
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got) {
+              if (lane == 0) set_err(q.err_flag, LORA_ERR_TIMEOUT);
+              quit = true;
+              return;
+            }
+            consumer_sync();  // our own partial (plain stores) is visible to every consumer
+            for (int i = ct; i < kV4; i += kCThreads) {
+              float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+              for (int qq = 0; qq < C; ++qq) {  // fixed order: identical v in every CTA
+                const float4 u = reinterpret_cast<const float4*>(&xbuf[b][qq][0][0])[i];
+                sum.x += u.x;
+                sum.y += u.y;
+                sum.z += u.z;
+                sum.w += u.w;
+              }
+              reinterpret_cast<float4*>(&vfull[0][0])[i] = sum;
+            }
+          } else {
+            for (int i = ct; i < kV4; i += kCThreads) reinterpret_cast<float4*>(&vfull[0][0])[i] = red_sum(i);
+          }
+          consumer_sync();
+          ++nx;
+          if (MODE == kModeShrink && rank == 0) {
+            for (int idx = ct; idx < tlen * R; idx += kCThreads) {
+              const int t = idx / R, k = idx % R;
+              int tkv = -1;
+  #pragma unroll
+              for (int u = 0; u < T; ++u)
+                if (u == t) tkv = tokr[u];
+              if (tkv >= 0) q.v_out[static_cast<int64_t>(tkv) * R + k] = vfull[t][k];
+            }
+          }
         }
-        // v as bf16 hi/lo MMA A fragments (rows >= tlen are zero)
-        auto split = [&](int row, int col, uint32_t& hi, uint32_t& lo) {
-          const bool ok = row < tlen;
-          const float x0 = ok ? sm.vfull[row][col] : 0.f, x1 = ok ? sm.vfull[row][col + 1] : 0.f;
-          hi = pack_bf16(x0, x1);
-          const float2 hf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi));
-          lo = pack_bf16(x0 - hf.x, x1 - hf.y);
+      } else {
+        // ---- expand stage: y[tok, off .. off+len) += s * vfull[t] . B[:, off .. off+len)
+        if (kind & kStFirst) {
+          if (MODE == kModeExpand) {
+            consumer_sync();  // every warp is done with the previous item's v
+            for (int idx = ct; idx < T * R; idx += kCThreads) {
+              const int t = idx / R, k = idx % R;
+              const int tk = t < tlen ? h.tok[t] : -1;
+              vfull[t][k] = tk >= 0 ? q.v_in[static_cast<int64_t>(tk) * R + k] : 0.f;
+            }
+            consumer_sync();
+          }
+          // v as bf16 hi/lo MMA A fragments (rows >= tlen are zero)
+          auto split = [&](int row, int col, uint32_t& hi, uint32_t& lo) {
+            const bool ok = row < tlen;
+            const float x0 = ok ? vfull[row][col] : 0.f, x1 = ok ? vfull[row][col + 1] : 0.f;
+            hi = pack_bf16(x0, x1);
+            const float2 hf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi));
+            lo = pack_bf16(x0 - hf.x, x1 - hf.y);
+          };
+          if constexpr (Cfg::KS == 0) {
+            split(g, 2 * tig, v8h[0], v8l[0]);
+            split(g + 8, 2 * tig, v8h[1], v8l[1]);
+          } else {
+  #pragma unroll
+            for (int ks = 0; ks < Cfg::KS; ++ks) {
+              split(g, ks * 16 + 2 * tig, vah[ks][0], val[ks][0]);
+              split(g + 8, ks * 16 + 2 * tig, vah[ks][1], val[ks][1]);
+              split(g, ks * 16 + 8 + 2 * tig, vah[ks][2], val[ks][2]);
+              split(g + 8, ks * 16 + 8 + 2 * tig, vah[ks][3], val[ks][3]);
+            }
+          }
+        }
+        const CCProj& pr = q.proj[pj];
+        const float scale = pr.scale;
+        uint16_t* const yg = pr.y;
+        const int64_t ldy = pr.ldy;
+        const int bw = h.pitch;  // box width (columns) of the B part; box = [R][bw]
+        const uint32_t b_base = smem_u32(st_base);
+        uint16_t* const Ys = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(st_base) + Cfg::kPartBytes);
+        const int ntl = len >> 3;  // 8-column n-tiles in the stage
+        const int tpb = bw >> 3;   // n-tiles per box (odd)
+        const uint32_t mtpb = 65536u / static_cast<uint32_t>(tpb) + 1u;  // i / tpb == (i * mtpb) >> 16 here
+        // element offset in the B part of column 0 of n-tile i (box-major layout [box][R][bw])
+        auto tile_off = [&](int i) -> int {
+          const int bx = static_cast<int>((static_cast<uint32_t>(i) * mtpb) >> 16);
+          return bx * (R * bw) + (i - bx * tpb) * 8;
         };
-        if constexpr (Cfg::KS == 0) {
-          split(g, 2 * tig, v8h[0], v8l[0]);
-          split(g + 8, 2 * tig, v8h[1], v8l[1]);
-        } else {
-#pragma unroll
-          for (int ks = 0; ks < Cfg::KS; ++ks) {
-            split(g, ks * 16 + 2 * tig, vah[ks][0], val[ks][0]);
-            split(g + 8, ks * 16 + 2 * tig, vah[ks][1], val[ks][1]);
-            split(g, ks * 16 + 8 + 2 * tig, vah[ks][2], val[ks][2]);
-            split(g + 8, ks * 16 + 8 + 2 * tig, vah[ks][3], val[ks][3]);
+        // y += s * products, in place in the stage's y rows (rows g, g+8 of a tile pair)
+        auto upd = [&](int row, int col, float e0, float e1) {
+          uint32_t* yp = reinterpret_cast<uint32_t*>(Ys + row * Cfg::XP + col);
+          const float2 yf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(yp));
+          *yp = pack_bf16(yf.x + scale * e0, yf.y + scale * e1);
+        };
+        auto pair = [&](int j, float (&d0)[4], float (&d1)[4]) {
+          // n-tiles j and j+1 (a missing second tile repeats the first)
+          const int oa = tile_off(j), ob = j + 1 < ntl ? tile_off(j + 1) : oa;
+  #pragma unroll
+          for (int e = 0; e < 4; ++e) d0[e] = d1[e] = 0.f;
+          if constexpr (Cfg::KS == 0) {
+            // r = 8: matrices (k 0-7, tile a), (k 0-7, tile b); lanes 16+ repeat 0-15
+            const int o = (lm & 1) ? ob : oa;
+            uint32_t b0, b1;
+            ldsm_x2_trans(b_base + static_cast<uint32_t>(o + lr * bw) * 2, b0, b1);
+            mma_bf16_1688(d0, v8h[0], v8h[1], b0);
+            mma_bf16_1688(d0, v8l[0], v8l[1], b0);
+            mma_bf16_1688(d1, v8h[0], v8h[1], b1);
+            mma_bf16_1688(d1, v8l[0], v8l[1], b1);
+          } else {
+            const int o = (lm >> 1) ? ob : oa;
+  #pragma unroll
+            for (int ks = 0; ks < Cfg::KS; ++ks) {
+              // matrices: (k 0-7, a), (k 8-15, a), (k 0-7, b), (k 8-15, b)
+              const int krow = ks * 16 + (lm & 1) * 8 + lr;
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4_trans(b_base + static_cast<uint32_t>(o + krow * bw) * 2, b0, b1, b2, b3);
+              mma_bf16_16816(d0, vah[ks][0], vah[ks][1], vah[ks][2], vah[ks][3], b0, b1);
+              mma_bf16_16816(d0, val[ks][0], val[ks][1], val[ks][2], val[ks][3], b0, b1);
+              mma_bf16_16816(d1, vah[ks][0], vah[ks][1], vah[ks][2], vah[ks][3], b2, b3);
+              mma_bf16_16816(d1, val[ks][0], val[ks][1], val[ks][2], val[ks][3], b2, b3);
+            }
+          }
+        };
+        auto store = [&](int j, const float (&d0)[4], const float (&d1)[4]) {
+          const bool has_b = j + 1 < ntl;
+          const int col_a = 8 * j + 2 * tig, col_b = col_a + 8;
+          if (g < tlen) {
+            upd(g, col_a, d0[0], d0[1]);
+            if (has_b) upd(g, col_b, d1[0], d1[1]);
+          }
+          if (g + 8 < tlen) {
+            upd(g + 8, col_a, d0[2], d0[3]);
+            if (has_b) upd(g + 8, col_b, d1[2], d1[3]);
+          }
+        };
+        // this warp's tile pairs: j = 2*warp + 2*kCW*i, two pairs per iteration
+        int j = 2 * warp;
+        for (; j + 2 * kCW < ntl; j += 4 * kCW) {
+          float d0[4], d1[4], d2[4], d3[4];
+          pair(j, d0, d1);
+          pair(j + 2 * kCW, d2, d3);
+          store(j, d0, d1);
+          store(j + 2 * kCW, d2, d3);
+        }
+        if (j < ntl) {
+          float d0[4], d1[4];
+          pair(j, d0, d1);
+          store(j, d0, d1);
+        }
+        fence_proxy_async_smem();  // our y updates, visible to the bulk stores below
+        consumer_sync();
+        // ---- the tile's updated y rows back to global memory, one bulk copy per token
+        if (ct < tlen) {
+          const int tkv = h.tok[ct];
+          if (tkv >= 0) {
+            bulk_s2g(yg + static_cast<int64_t>(tkv) * ldy + off, Ys + ct * Cfg::XP, static_cast<uint32_t>(len) * 2u);
+            bulk_commit();
+            bulk_wait_read0();  // the slot may be refilled once the copy has read it
           }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[slot]);
       }
-      const CCProj& pr = q.proj[pj];
-      const float scale = pr.scale;
-      uint16_t* const yg = pr.y;
-      const int64_t ldy = pr.ldy;
-      const int bw = h.pitch;  // box width (columns) of the B part; box = [R][bw]
-      const uint32_t b_base = smem_u32(st_base);
-      uint16_t* const Ys = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(st_base) + Cfg::kPartBytes);
-      const int ntl = len >> 3;  // 8-column n-tiles in the stage
-      const int tpb = bw >> 3;   // n-tiles per box (odd)
-      const uint32_t mtpb = 65536u / static_cast<uint32_t>(tpb) + 1u;  // i / tpb == (i * mtpb) >> 16 here
-      // element offset in the B part of column 0 of n-tile i (box-major layout [box][R][bw])
-      auto tile_off = [&](int i) -> int {
-        const int bx = static_cast<int>((static_cast<uint32_t>(i) * mtpb) >> 16);
-        return bx * (R * bw) + (i - bx * tpb) * 8;
-      };
-      // y += s * products, in place in the stage's y rows (rows g, g+8 of a tile pair)
-      auto upd = [&](int row, int col, float e0, float e1) {
-        uint32_t* yp = reinterpret_cast<uint32_t*>(Ys + row * Cfg::XP + col);
-        const float2 yf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(yp));
-        *yp = pack_bf16(yf.x + scale * e0, yf.y + scale * e1);
-      };
-      auto pair = [&](int j, float (&d0)[4], float (&d1)[4]) {
-        // n-tiles j and j+1 (a missing second tile repeats the first)
-        const int oa = tile_off(j), ob = j + 1 < ntl ? tile_off(j + 1) : oa;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) d0[e] = d1[e] = 0.f;
-        if constexpr (Cfg::KS == 0) {
-          // r = 8: matrices (k 0-7, tile a), (k 0-7, tile b); lanes 16+ repeat 0-15
-          const int o = (lm & 1) ? ob : oa;
-          uint32_t b0, b1;
-          ldsm_x2_trans(b_base + static_cast<uint32_t>(o + lr * bw) * 2, b0, b1);
-          mma_bf16_1688(d0, v8h[0], v8h[1], b0);
-          mma_bf16_1688(d0, v8l[0], v8l[1], b0);
-          mma_bf16_1688(d1, v8h[0], v8h[1], b1);
-          mma_bf16_1688(d1, v8l[0], v8l[1], b1);
-        } else {
-          const int o = (lm >> 1) ? ob : oa;
-#pragma unroll
-          for (int ks = 0; ks < Cfg::KS; ++ks) {
-            // matrices: (k 0-7, a), (k 8-15, a), (k 0-7, b), (k 8-15, b)
-            const int krow = ks * 16 + (lm & 1) * 8 + lr;
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_trans(b_base + static_cast<uint32_t>(o + krow * bw) * 2, b0, b1, b2, b3);
-            mma_bf16_16816(d0, vah[ks][0], vah[ks][1], vah[ks][2], vah[ks][3], b0, b1);
-            mma_bf16_16816(d0, val[ks][0], val[ks][1], val[ks][2], val[ks][3], b0, b1);
-            mma_bf16_16816(d1, vah[ks][0], vah[ks][1], vah[ks][2], vah[ks][3], b2, b3);
-            mma_bf16_16816(d1, val[ks][0], val[ks][1], val[ks][2], val[ks][3], b2, b3);
-          }
-        }
-      };
-      auto store = [&](int j, const float (&d0)[4], const float (&d1)[4]) {
-        const bool has_b = j + 1 < ntl;
-        const int col_a = 8 * j + 2 * tig, col_b = col_a + 8;
-        if (g < tlen) {
-          upd(g, col_a, d0[0], d0[1]);
-          if (has_b) upd(g, col_b, d1[0], d1[1]);
-        }
-        if (g + 8 < tlen) {
-          upd(g + 8, col_a, d0[2], d0[3]);
-          if (has_b) upd(g + 8, col_b, d1[2], d1[3]);
-        }
-      };
-      // this warp's tile pairs: j = 2*warp + 2*kCW*i, two pairs per iteration
-      int j = 2 * warp;
-      for (; j + 2 * kCW < ntl; j += 4 * kCW) {
-        float d0[4], d1[4], d2[4], d3[4];
-        pair(j, d0, d1);
-        pair(j + 2 * kCW, d2, d3);
-        store(j, d0, d1);
-        store(j + 2 * kCW, d2, d3);
-      }
-      if (j < ntl) {
-        float d0[4], d1[4];
-        pair(j, d0, d1);
-        store(j, d0, d1);
-      }
-      fence_proxy_async_smem();  // our y updates, visible to the bulk stores below
-      consumer_sync();
-      // ---- the tile's updated y rows back to global memory, one bulk copy per token
-      if (ct < tlen) {
-        const int tkv = h.tok[ct];
-        if (tkv >= 0) {
-          bulk_s2g(yg + static_cast<int64_t>(tkv) * ldy + off, Ys + ct * Cfg::XP, static_cast<uint32_t>(len) * 2u);
-          bulk_commit();
-          bulk_wait_read0();  // the slot may be refilled once the copy has read it
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.empty[slot]);
-    }
+    });
+    if (quit) return;
     if (++slot == kStages) {
       slot = 0;
       phase ^= 1u;
@@ -781,49 +864,83 @@ struct KernelInfo {
   int max_groups = 0;  // co-resident clusters (or CTA groups) on the device
 };
 
-template <int R, int T, int MODE>
-lora_status launch_rtm(CCParams& prm, int items_bound, cudaStream_t stream) {
-  using Cfg = CCCfg<R, T>;
-  auto kern = sgmv_cc_kernel<R, T, MODE>;
-  const size_t smem = sizeof(CCSmem<R, T>);
+// Stage shape of rank r in the ring of a kernel whose largest rank is RM.
+struct RankShape {
+  int BA, WS, SWA;
+};
+template <int T, int RM>
+RankShape rank_shape(int r) {
+  switch (r) {
+    case 8: return {CCCfg<8, T, RM>::BA, CCCfg<8, T, RM>::WS, CCCfg<8, T, RM>::SWA};
+    case 16: return {CCCfg<16, T, RM>::BA, CCCfg<16, T, RM>::WS, CCCfg<16, T, RM>::SWA};
+    case 32: return {CCCfg<32, T, RM>::BA, CCCfg<32, T, RM>::WS, CCCfg<32, T, RM>::SWA};
+    default: return {CCCfg<64, T, RM>::BA, CCCfg<64, T, RM>::WS, CCCfg<64, T, RM>::SWA};
+  }
+}
+
+// Encodes the tensor-map pairs of every (projection, rank of `ranks`) and
+// launches.  prm.t holds the projections, the tables and rmax / n_slots.
+template <int RSET, int T, int MODE>
+lora_status launch_rtm(CCParams& prm, const int* ranks, int n_ranks, int items_bound, cudaStream_t stream) {
+  constexpr int RM = set_max_rank(RSET);
+  auto kern = sgmv_cc_kernel<RSET, T, MODE>;
+  const size_t smem = sizeof(CCSmem<RM, T>);
   const int C = prm.t.csplit;
   const bool cluster = (MODE & kModeShrink) && C > 1;
+  if (prm.t.n_proj * n_ranks > kMaxProj) return LORA_ERR_UNSUPPORTED;
 
+  prm.t.rank_mask = 0;
+  for (int j = 0; j < n_ranks; ++j) {
+    if ((rank_bit(ranks[j]) & RSET) == 0) return LORA_ERR_UNSUPPORTED;
+    prm.t.rank_mask |= rank_bit(ranks[j]);
+  }
+  int m = 0;
   for (int i = 0; i < prm.t.n_proj; ++i) {
     CCProj& q = prm.t.proj[i];
-    if (MODE & kModeShrink) {
-      const uint64_t dims[2] = {static_cast<uint64_t>(R), static_cast<uint64_t>(prm.t.n_adapters) * q.h_in};
-      const uint64_t strides[1] = {static_cast<uint64_t>(R) * 2};
-      const uint32_t box[2] = {static_cast<uint32_t>(R), static_cast<uint32_t>(Cfg::BA)};
-      const lora_status s = encode_tmap_bf16(&prm.tmA[i], q.A, 2, dims, strides, box, Cfg::SWA);
-      if (s != LORA_OK) return s;
-    }
-    if (MODE & kModeExpand) {
-      // stage = nb boxes of bw columns, nb*bw <= WS; bw <= 256 (the TMA box
-      // limit) and an odd multiple of 8 (16-byte chunks), which puts the 8 rows
-      // an ldmatrix reads into different banks.  Fewest boxes that cover a
-      // stage's share of the chunk.
-      const int nst = std::max(1, ceil_div(q.n_chunk, Cfg::WS));
-      const int pe = round_up(ceil_div(q.n_chunk, nst), 8);
-      q.nb = 0;
-      for (int nb = 1; nb <= 16 && q.nb == 0; ++nb) {
-        int bw = round_up(ceil_div(pe, nb), 8);
-        if ((bw / 8) % 2 == 0) bw += 8;
-        if (bw <= 256 && nb * bw <= Cfg::WS) {
-          q.nb = nb;
-          q.bw = bw;
+    for (int c = 0; c < 4; ++c) prm.t.map_of[i][c] = -1;
+    for (int j = 0; j < n_ranks; ++j, ++m) {
+      const int r = ranks[j];
+      const RankShape sh = rank_shape<T, RM>(r);
+      prm.t.map_of[i][rank_class(r)] = m;
+      prm.t.map_bw[m] = 8;
+      prm.t.map_nb[m] = 1;
+      if (MODE & kModeShrink) {
+        const uint64_t rows = static_cast<uint64_t>(prm.t.n_slots) * q.h_in * (prm.t.rmax / r);
+        const uint64_t dims[2] = {static_cast<uint64_t>(r), rows};
+        const uint64_t strides[1] = {static_cast<uint64_t>(r) * 2};
+        const uint32_t box[2] = {static_cast<uint32_t>(r), static_cast<uint32_t>(sh.BA)};
+        const lora_status s = encode_tmap_bf16(&prm.tmA[m], q.A, 2, dims, strides, box, sh.SWA);
+        if (s != LORA_OK) return s;
+      }
+      if (MODE & kModeExpand) {
+        // stage = nb boxes of bw columns, nb*bw <= WS; bw <= 256 (the TMA box
+        // limit) and an odd multiple of 8 (16-byte chunks), which puts the 8 rows
+        // an ldmatrix reads into different banks.  Fewest boxes that cover a
+        // stage's share of the chunk.
+        const int nst = std::max(1, ceil_div(q.n_chunk, sh.WS));
+        const int pe = round_up(ceil_div(q.n_chunk, nst), 8);
+        int bw = 8, nb = 0;
+        for (int k = 1; k <= 16 && nb == 0; ++k) {
+          int w = round_up(ceil_div(pe, k), 8);
+          if ((w / 8) % 2 == 0) w += 8;
+          if (w <= 256 && k * w <= sh.WS) {
+            nb = k;
+            bw = w;
+          }
         }
+        if (nb == 0) {  // covering is impossible within WS: largest odd box that fits
+          nb = 1;
+          bw = std::min(256, sh.WS) / 8 * 8;
+          if ((bw / 8) % 2 == 0) bw -= 8;
+        }
+        prm.t.map_bw[m] = bw;
+        prm.t.map_nb[m] = nb;
+        const uint64_t dims[2] = {static_cast<uint64_t>(q.h_out), static_cast<uint64_t>(prm.t.n_slots) * prm.t.rmax};
+        const uint64_t strides[1] = {static_cast<uint64_t>(q.h_out) * 2};
+        const uint32_t box[2] = {static_cast<uint32_t>(bw), static_cast<uint32_t>(r)};
+        const lora_status s = encode_tmap_bf16(&prm.tmB[m], q.B, 2, dims, strides, box, 0);
+        if (s != LORA_OK) return s;
       }
-      if (q.nb == 0) {  // covering is impossible within WS: largest odd box that fits
-        q.nb = 1;
-        q.bw = std::min(256, Cfg::WS) / 8 * 8;
-        if ((q.bw / 8) % 2 == 0) q.bw -= 8;
-      }
-      const uint64_t dims[2] = {static_cast<uint64_t>(q.h_out), static_cast<uint64_t>(prm.t.n_adapters) * R};
-      const uint64_t strides[1] = {static_cast<uint64_t>(q.h_out) * 2};
-      const uint32_t box[2] = {static_cast<uint32_t>(q.bw), static_cast<uint32_t>(R)};
-      const lora_status s = encode_tmap_bf16(&prm.tmB[i], q.B, 2, dims, strides, box, 0);
-      if (s != LORA_OK) return s;
     }
   }
 
@@ -891,10 +1008,11 @@ lora_status launch_rtm(CCParams& prm, int items_bound, cudaStream_t stream) {
 
 template <int R, int T>
 lora_status dispatch_mode(Mode m, CCParams& prm, int items_bound, cudaStream_t st) {
+  const int ranks[1] = {R};
   switch (m) {
-    case kModeShrink: return launch_rtm<R, T, kModeShrink>(prm, items_bound, st);
-    case kModeExpand: return launch_rtm<R, T, kModeExpand>(prm, items_bound, st);
-    default: return launch_rtm<R, T, kModeFused>(prm, items_bound, st);
+    case kModeShrink: return launch_rtm<rank_bit(R), T, kModeShrink>(prm, ranks, 1, items_bound, st);
+    case kModeExpand: return launch_rtm<rank_bit(R), T, kModeExpand>(prm, ranks, 1, items_bound, st);
+    default: return launch_rtm<rank_bit(R), T, kModeFused>(prm, ranks, 1, items_bound, st);
   }
 }
 
@@ -907,6 +1025,24 @@ lora_status dispatch_r(int r, Mode m, CCParams& prm, int items_bound, cudaStream
     case 64: return dispatch_mode<64, T>(m, prm, items_bound, st);
     default: return LORA_ERR_UNSUPPORTED;
   }
+}
+
+// Mixed ranks (fused only): one launch per group of projections whose
+// (projection, rank) map pairs fit the parameter block.
+template <int T>
+lora_status dispatch_mixed(CCParams& base, const int* ranks, int n_ranks, int items_per_proj, cudaStream_t st) {
+  const int per = std::max(1, kMaxProj / n_ranks);
+  const int n_proj = base.t.n_proj;
+  for (int p0 = 0; p0 < n_proj; p0 += per) {
+    CCParams prm = base;
+    const int np = std::min(per, n_proj - p0);
+    for (int i = 0; i < np; ++i) prm.t.proj[i] = base.t.proj[p0 + i];
+    prm.t.n_proj = np;
+    const int items = static_cast<int>(std::min<int64_t>(static_cast<int64_t>(items_per_proj) * np, 1 << 30));
+    const lora_status s = launch_rtm<kAllRanks, T, kModeFused>(prm, ranks, n_ranks, items, st);
+    if (s != LORA_OK) return s;
+  }
+  return LORA_OK;
 }
 
 }  // namespace
@@ -939,8 +1075,6 @@ lora_status launch_sgmv_cc(const SgmvCall& call, cudaStream_t stream) {
     q.h_out = a.h_out;
     q.k_chunk = round_up(ceil_div(a.h_in, C), 16);
     q.n_chunk = round_up(ceil_div(a.h_out, C), 8);
-    q.bw = 8;
-    q.nb = 1;
     q.scale = a.scale;
   }
   prm.t.perm = call.seg.perm;
@@ -956,7 +1090,12 @@ lora_status launch_sgmv_cc(const SgmvCall& call, cudaStream_t stream) {
   prm.t.n_adapters = call.n_adapters;
   prm.t.csplit = C;
   prm.t.skip_long = 0;
-  if (sgmv_tc_applicable(call)) {
+  const bool slots = call.slot_of != nullptr;
+  prm.t.slot_of = call.slot_of;
+  prm.t.rank_of = call.rank_of;
+  prm.t.n_slots = slots ? call.n_slots : call.n_adapters;
+  prm.t.rmax = slots ? call.r_max : call.r;
+  if (!slots && sgmv_tc_applicable(call)) {
     // long contiguous segments on tcgen05 tiles, the rest of the batch here
     const lora_status s = launch_sgmv_tc(call, stream);
     if (s != LORA_OK) return s;
@@ -965,9 +1104,21 @@ lora_status launch_sgmv_cc(const SgmvCall& call, cudaStream_t stream) {
 
   // upper bound of the number of tiles: sum over segments of ceil(len/T)
   const int64_t tiles = std::min<int64_t>(n, (static_cast<int64_t>(n) + static_cast<int64_t>(S_max) * (T - 1)) / T);
+  int ranks[4], n_ranks = 0;
+  if (slots) {
+    for (int c = 0; c < 4; ++c)
+      if (call.rank_mask & (1u << c)) ranks[n_ranks++] = 8 << c;
+  }
+  if (slots && n_ranks > 1) {
+    if (call.mode != kModeFused) return LORA_ERR_UNSUPPORTED;
+    const int items_per_proj = static_cast<int>(std::min<int64_t>(tiles, 1 << 30));
+    if (T == 4) return dispatch_mixed<4>(prm, ranks, n_ranks, items_per_proj, stream);
+    return dispatch_mixed<16>(prm, ranks, n_ranks, items_per_proj, stream);
+  }
+  const int r = slots ? ranks[0] : call.r;
   const int items_bound = static_cast<int>(std::min<int64_t>(tiles * call.n_proj, 1 << 30));
-  if (T == 4) return dispatch_r<4>(call.r, call.mode, prm, items_bound, stream);
-  return dispatch_r<16>(call.r, call.mode, prm, items_bound, stream);
+  if (T == 4) return dispatch_r<4>(r, call.mode, prm, items_bound, stream);
+  return dispatch_r<16>(r, call.mode, prm, items_bound, stream);
 }
 
 }  // namespace lsg

@@ -26,7 +26,7 @@ STATUS = {
 }
 # exported symbols declared in include/lora_sgmv.h
 SYMBOLS = ("lora_status_str", "lora_abi_version", "lora_segment_workspace_bytes", "lora_segment",
-           "lora_segment_noalloc", "sgmv_shrink", "sgmv_expand", "sgmv_fused", "sgmv_multi")
+           "lora_segment_noalloc", "sgmv_shrink", "sgmv_expand", "sgmv_fused", "sgmv_multi", "sgmv_multi_slots")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -39,6 +39,11 @@ class LoraProj(ctypes.Structure):
     _fields_ = [("x", ctypes.c_void_p), ("A_pool", ctypes.c_void_p), ("B_pool", ctypes.c_void_p),
                 ("y", ctypes.c_void_p), ("ldx", ctypes.c_int64), ("ldy", ctypes.c_int64),
                 ("h_in", ctypes.c_int32), ("h_out", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+
+class LoraSlotTable(ctypes.Structure):
+    _fields_ = [("slot_of", ctypes.c_void_p), ("rank_of", ctypes.c_void_p), ("n_adapters", ctypes.c_int32),
+                ("n_slots", ctypes.c_int32), ("r_max", ctypes.c_int32), ("rank_mask", ctypes.c_uint32)]
 
 
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
@@ -69,6 +74,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                p, i64, p, p]
     lib.sgmv_multi.restype = ctypes.c_int
     lib.sgmv_multi.argtypes = [ctypes.POINTER(LoraProj), i32, i32, i32, ctypes.POINTER(LoraSegments), p, p]
+    lib.sgmv_multi_slots.restype = ctypes.c_int
+    lib.sgmv_multi_slots.argtypes = [ctypes.POINTER(LoraProj), i32, ctypes.POINTER(LoraSlotTable),
+                                     ctypes.POINTER(LoraSegments), p, p]
     _lib = lib
     return lib
 
@@ -257,3 +265,82 @@ def sgmv_multi(projs: Sequence, seg: Segments, *, err_flag: Optional[torch.Tenso
     P, _, r = projs[0][1].shape
     _check(lib.sgmv_multi(arr, len(projs), P, r, ctypes.byref(seg.c_struct), _ptr(err_flag), _stream(stream)),
            "sgmv_multi")
+
+
+def rank_mask(ranks) -> int:
+    """Bit c set for each rank 8 << c in `ranks`."""
+    m = 0
+    for r in ranks:
+        if r not in (8, 16, 32, 64):
+            raise ValueError(f"rank {r} not in (8, 16, 32, 64)")
+        m |= 1 << (int(r).bit_length() - 4)
+    return m
+
+
+@dataclass
+class SlotTable:
+    """Where each adapter of the batch lives in slot arenas, and its rank
+    (device int32 tables of n_adapters entries)."""
+    slot_of: torch.Tensor  # int32 [n_adapters]
+    rank_of: torch.Tensor  # int32 [n_adapters]
+    n_slots: int
+    r_max: int
+    rank_mask: int
+
+    def __post_init__(self):
+        _req(self.slot_of, "slot_of", torch.int32, 1)
+        _req(self.rank_of, "rank_of", torch.int32, 1)
+        if self.slot_of.shape != self.rank_of.shape:
+            raise ValueError("slot_of and rank_of differ in length")
+        self._c = LoraSlotTable(self.slot_of.data_ptr(), self.rank_of.data_ptr(), self.slot_of.shape[0],
+                                int(self.n_slots), int(self.r_max), int(self.rank_mask))
+
+    @property
+    def n_adapters(self) -> int:
+        return self.slot_of.shape[0]
+
+    @property
+    def c_struct(self) -> LoraSlotTable:
+        return self._c
+
+
+def make_slot_projs(projs: Sequence, table: SlotTable) -> "ctypes.Array":
+    """Host array of lora_proj from (x, A_arena, B_arena, y, scale) tuples;
+    A_arena is [n_slots, h_in * r_max], B_arena [n_slots, r_max * h_out]."""
+    arr = (LoraProj * len(projs))()
+    for i, (x, A, B, y, s) in enumerate(projs):
+        _req(x, "x", torch.bfloat16, 2)
+        _req(y, "y", torch.bfloat16, 2)
+        _req(A, "A_arena", torch.bfloat16, 2)
+        _req(B, "B_arena", torch.bfloat16, 2)
+        h_in, h_out = x.shape[1], y.shape[1]
+        if not (A.is_contiguous() and B.is_contiguous()):
+            raise ValueError(f"projection {i}: arenas must be contiguous")
+        if tuple(A.shape) != (table.n_slots, h_in * table.r_max) or \
+                tuple(B.shape) != (table.n_slots, table.r_max * h_out):
+            raise ValueError(f"projection {i}: arena shapes do not match n_slots / r_max / widths")
+        arr[i] = LoraProj(x.data_ptr(), A.data_ptr(), B.data_ptr(), y.data_ptr(), _rows(x, "x"), _rows(y, "y"),
+                          h_in, h_out, float(s))
+    return arr
+
+
+def sgmv_multi_slots(projs: Sequence, table: SlotTable, seg: Segments, *, err_flag: Optional[torch.Tensor] = None,
+                     stream=None, c_projs=None) -> None:
+    """sgmv_multi over slot arenas, adapters of mixed ranks (include/lora_sgmv.h).
+    projs: sequence of (x, A_arena, B_arena, y, scale)."""
+    lib = load_library()
+    if not 1 <= len(projs) <= LORA_MAX_PROJ:
+        raise ValueError("1..8 projections")
+    if seg.n_adapters != table.n_adapters:
+        raise ValueError("segmentation and slot table disagree on n_adapters")
+    arr = c_projs if c_projs is not None else make_slot_projs(projs, table)
+    _check(lib.sgmv_multi_slots(arr, len(projs), ctypes.byref(table.c_struct), ctypes.byref(seg.c_struct),
+                                _ptr(err_flag), _stream(stream)), "sgmv_multi_slots")
+
+
+def sgmv_fused_slots(x: torch.Tensor, A_arena: torch.Tensor, B_arena: torch.Tensor, table: SlotTable,
+                     seg: Segments, y: torch.Tensor, scale: float, *, err_flag: Optional[torch.Tensor] = None,
+                     stream=None) -> torch.Tensor:
+    """One projection of sgmv_multi_slots (in place on y)."""
+    sgmv_multi_slots([(x, A_arena, B_arena, y, scale)], table, seg, err_flag=err_flag, stream=stream)
+    return y

@@ -53,7 +53,7 @@
 extern "C" {
 #endif
 
-#define LORA_SGMV_ABI_VERSION 1
+#define LORA_SGMV_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define LORA_API __attribute__((visibility("default")))
@@ -180,9 +180,10 @@ LORA_API lora_status sgmv_expand(const float* v, const lora_bf16* B_pool, int32_
 /*
  * Shrink and expand in one launch, v kept on chip (never written to device
  * memory): y[i,:] += s * ((x[i,:] . A[a_i]) . B[a_i]).  Arguments as for
- * sgmv_shrink / sgmv_expand.  The tensor-core path for long segments rounds v
- * to bf16 before the expand product (its error, about 2^-9 relative to |v|,
- * is far inside the parity tolerance); the CUDA-core path keeps v in fp32.
+ * sgmv_shrink / sgmv_expand.  v is accumulated in fp32; the expand product
+ * takes it as two bf16 operands, v = hi + lo with hi = bf16(v) and
+ * lo = bf16(v - hi), which keep 16 bits of its mantissa (relative error about
+ * 2^-17, far inside the parity tolerance).
  */
 LORA_API lora_status sgmv_fused(const lora_bf16* x, int64_t ldx, const lora_bf16* A_pool,
                        const lora_bf16* B_pool, int32_t n_adapters, int32_t h_in, int32_t h_out,
@@ -210,6 +211,50 @@ typedef struct {
  */
 LORA_API lora_status sgmv_multi(const lora_proj* projs, int32_t n_proj, int32_t n_adapters, int32_t r,
                        const lora_segments* seg, int32_t* err_flag, lora_stream_t stream);
+
+/*
+ * Slot tables: adapter pools stored as arenas of fixed-size slots, so that
+ * adapters are loaded into free slots and evicted while the pool is in use,
+ * and adapters of different ranks share one launch.  Punica: Multi-Tenant
+ * LoRA Serving (research.elamur.ai summary), "Summary": adapters are loaded
+ * on demand, in milliseconds; "Key points": rank is far below the hidden
+ * size (16 vs 4096).
+ *
+ * Per projection, the arenas are (lora_proj.A_pool / B_pool point to them):
+ *   A arena [n_slots][h_in * r_max]: slot s holds its adapter's A, rank r,
+ *           as [h_in][r] row-major at the slot start (the rest unused);
+ *   B arena [n_slots][r_max * h_out]: B as [r][h_out] row-major at the start.
+ * Adapter id a of the batch (0 <= a < n_adapters) lives in slot slot_of[a]
+ * with rank rank_of[a]; one id names the same slot in every projection's
+ * arenas.  Both tables are device int32 arrays of n_adapters entries, read
+ * by the kernel after the segmentation it waits for.
+ */
+typedef struct {
+  const int32_t* slot_of; /* device [n_adapters]: slot of adapter a */
+  const int32_t* rank_of; /* device [n_adapters]: rank of adapter a, in {8,16,32,64}, <= r_max */
+  int32_t n_adapters;     /* ids of the batch and of the segmentation index these tables */
+  int32_t n_slots;        /* slots in every arena */
+  int32_t r_max;          /* slot capacity in ranks: 8, 16, 32 or 64 */
+  uint32_t rank_mask;     /* ranks that may occur: bit c for rank 8 << c; no bit above r_max */
+} lora_slot_table;
+
+/*
+ * sgmv_multi over slot arenas: y_p[i,:] += s_p * ((x_p[i,:] . A_p[a_i]) .
+ * B_p[a_i]) with A_p[a], B_p[a] the rank-rank_of[a] matrices in slot
+ * slot_of[a] of projection p's arenas.  One rank in rank_mask: one launch
+ * for all projections; several ranks: each launch takes the projections
+ * whose (projection, rank) pairs fit 8, i.e. 8 / popcount(rank_mask)
+ * projections.  Long segments go through the split-K kernel here (the
+ * tensor-tile kernel serves contiguous pools only).
+ * Host errors as sgmv_multi, plus: table NULL, a table pointer NULL or not
+ * 4-byte aligned, n_slots < 1, r_max or rank_mask invalid
+ * (LORA_ERR_INVALID_ARG / LORA_ERR_UNSUPPORTED), n_slots*r_max*max(h_in,
+ * h_out) >= 2^31 (LORA_ERR_UNSUPPORTED).  Device errors: an adapter id
+ * outside [0, n_adapters), a slot outside [0, n_slots) or a rank not in
+ * rank_mask: LORA_ERR_BAD_ADAPTER_ID in *err_flag, the segment skipped.
+ */
+LORA_API lora_status sgmv_multi_slots(const lora_proj* projs, int32_t n_proj, const lora_slot_table* table,
+                                      const lora_segments* seg, int32_t* err_flag, lora_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -61,6 +61,9 @@ def load(mutant: int = 0) -> ctypes.CDLL:
     lib.oracle_sgmv_f32.argtypes = [p, i64, p, p, p, i32, i32, i32, i32, i32, ctypes.c_float, p, i64, p, p, i32]
     lib.oracle_sgmv_f64.restype = i32
     lib.oracle_sgmv_f64.argtypes = [p, i64, p, p, p, i32, i32, i32, i32, i32, ctypes.c_double, p, i64, p, p, i32]
+    lib.oracle_sgmv_slots_f32.restype = i32
+    lib.oracle_sgmv_slots_f32.argtypes = [p, i64, p, p, p, p, i32, i32, ctypes.c_uint32, p, i32, i32, i32, i32,
+                                          ctypes.c_float, p, i64, p, i32]
     lib.oracle_mutant.restype = i32
     assert lib.oracle_mutant() == mutant
     _loaded[mutant] = lib
@@ -119,3 +122,29 @@ def sgmv_ref(x, A_pool, B_pool, ids, s: float, y0, *, threads: int = 1, f64: boo
     fn(_ptr(xb), xb.shape[1], _ptr(Ab), _ptr(Bb), _ptr(ids), n, P, h_in, h_out, r, float(s),
        _ptr(yb), yb.shape[1], _ptr(y), _ptr(v) if want_v else None, int(threads))
     return (y, v) if want_v else y
+
+
+def sgmv_slots_ref(x, A_arena, B_arena, slot_of, rank_of, r_max: int, rank_mask: int, ids, s: float, y0, *,
+                   threads: int = 1, mutant: int = 0, return_invalid: bool = False):
+    """The delta over slot arenas with adapters of mixed ranks (see the C file).
+
+    x: [n, >=h_in] bf16; A_arena: [n_slots, h_in*r_max]; B_arena:
+    [n_slots, r_max*h_out]; slot_of, rank_of: int32 [P]; ids: int32 [n];
+    y0: [n, >=h_out].  Returns y ([n, h_out] fp32, unrounded)."""
+    xb, Ab, Bb, yb = bits(x), bits(A_arena), bits(B_arena), bits(y0)
+    ids = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    slot_of = np.ascontiguousarray(np.asarray(slot_of, dtype=np.int32))
+    rank_of = np.ascontiguousarray(np.asarray(rank_of, dtype=np.int32))
+    assert slot_of.shape == rank_of.shape and slot_of.ndim == 1
+    P = int(slot_of.size)
+    n = int(ids.size)
+    n_slots = Ab.shape[0]
+    assert Ab.ndim == 2 and Bb.ndim == 2 and Bb.shape[0] == n_slots
+    assert Ab.shape[1] % r_max == 0 and Bb.shape[1] % r_max == 0
+    h_in, h_out = Ab.shape[1] // r_max, Bb.shape[1] // r_max
+    assert xb.shape[0] == n and xb.shape[1] >= h_in and yb.shape[0] == n and yb.shape[1] >= h_out
+    y = np.empty((n, h_out), np.float32)
+    bad = load(mutant).oracle_sgmv_slots_f32(_ptr(xb), xb.shape[1], _ptr(Ab), _ptr(Bb), _ptr(slot_of),
+                                             _ptr(rank_of), n_slots, int(r_max), int(rank_mask), _ptr(ids), n, P,
+                                             h_in, h_out, float(s), _ptr(yb), yb.shape[1], _ptr(y), int(threads))
+    return (y, int(bad)) if return_invalid else y

@@ -236,3 +236,58 @@ int oracle_sgmv_f64(const uint16_t* x, int64_t ldx, const uint16_t* A_pool, cons
   }
   return n_invalid;
 }
+
+/*
+ * Slot arenas with adapters of mixed ranks (the pool layout of the slot-table
+ * entry point).  Adapter a lives in slot slot_of[a] with rank rank_of[a]; its
+ * A is [h_in][rank] row-major at A_arena + slot*h_in*r_max and its B is
+ * [rank][h_out] row-major at B_arena + slot*r_max*h_out.  An entry is valid
+ * when 0 <= a < P, 0 <= slot < n_slots, the rank is 8, 16, 32 or 64, is at
+ * most r_max and has its bit (rank 8 << c: bit c) in rank_mask.  Each valid
+ * token takes the same steps as oracle_sgmv_f32 with its adapter's rank;
+ * any other token gets y = y0.  Returns the number of tokens that are not
+ * valid.
+ */
+static int slot_rank_valid(int32_t rk, int32_t r_max, uint32_t rank_mask) {
+  int32_t c = rk == 8 ? 0 : rk == 16 ? 1 : rk == 32 ? 2 : rk == 64 ? 3 : -1;
+  return c >= 0 && rk <= r_max && ((rank_mask >> c) & 1u);
+}
+
+int oracle_sgmv_slots_f32(const uint16_t* x, int64_t ldx, const uint16_t* A_arena, const uint16_t* B_arena,
+                          const int32_t* slot_of, const int32_t* rank_of, int32_t n_slots, int32_t r_max,
+                          uint32_t rank_mask, const int32_t* ids, int32_t n, int32_t P, int32_t h_in,
+                          int32_t h_out, float s, const uint16_t* y0, int64_t ldy0, float* y, int32_t n_threads) {
+  int32_t n_invalid = 0;
+  if (n_threads < 1) n_threads = 1;
+#pragma omp parallel num_threads(n_threads) reduction(+ : n_invalid)
+  {
+    float* vtmp = (float*)malloc(sizeof(float) * (size_t)(r_max > 0 ? r_max : 1));
+#pragma omp for schedule(static)
+    for (int32_t i = 0; i < n; ++i) {
+      int32_t a = ids[i];
+      float* yi = y + (int64_t)i * h_out;
+      const uint16_t* y0i = y0 + (int64_t)i * ldy0;
+      int ok = a >= 0 && a < P;
+      int32_t sl = ok ? slot_of[a] : -1, rk = ok ? rank_of[a] : 0;
+      ok = ok && sl >= 0 && sl < n_slots && slot_rank_valid(rk, r_max, rank_mask);
+      if (!ok) {
+        n_invalid += 1;
+        for (int32_t c = 0; c < h_out; ++c) yi[c] = bf16_to_f32(y0i[c]);
+        continue;
+      }
+#if ORACLE_MUTANT == 8 /* slot stride taken from the adapter's rank instead of the slot capacity */
+      const uint16_t* A = A_arena + (int64_t)sl * h_in * rk;
+      const uint16_t* B = B_arena + (int64_t)sl * rk * h_out;
+#else
+      const uint16_t* A = A_arena + (int64_t)sl * h_in * r_max;
+      const uint16_t* B = B_arena + (int64_t)sl * r_max * h_out;
+#endif
+#if ORACLE_MUTANT == 9 /* every adapter read at the slot capacity's rank */
+      rk = r_max;
+#endif
+      token_f32(x + (int64_t)i * ldx, A, B, y0i, h_in, h_out, rk, s, yi, NULL, vtmp);
+    }
+    free(vtmp);
+  }
+  return n_invalid;
+}

@@ -6,7 +6,9 @@ planted mistake, selected by `mutant`) disagrees with:
   - brute force (dense W = A.B in fp64; Python's stable sort),
   - a library routine in the special case of one adapter (torch.matmul),
   - invariants: B = 0 leaves y unchanged, permuting tokens permutes outputs,
-    linearity in s, and the rank-1 closed form y = y0 + s*h_in*c*d.
+    linearity in s, and the rank-1 closed form y = y0 + s*h_in*c*d;
+  - for slot arenas of mixed ranks: the dense fp64 product per adapter, the
+    contiguous-pool oracle on zero-padded adapters, and relocation of slots.
 """
 
 from __future__ import annotations
@@ -197,6 +199,123 @@ def pin_rank1_closed_form(mutant=0):
     assert np.array_equal(y, f32_from_bf16_bits(y0) + np.float32(s * h_in * c * d))
 
 
+# ------------------------------------------------------------------ slot arenas, mixed ranks
+
+def slot_problem(rng, n, P, n_slots, h_in, h_out, r_max, ranks, p_invalid=0.0):
+    """Adapters of the given ranks placed in shuffled slots of r_max capacity;
+    the unused part of every slot holds random junk, so that reading past an
+    adapter's rank or at the wrong slot stride changes the result."""
+    slots = rng.permutation(n_slots)[:P].astype(np.int32)
+    rank_of = rng.choice(ranks, P).astype(np.int32)
+    A_ar, B_ar, As, Bs = place_adapters(rng, slots, rank_of, n_slots, h_in, h_out, r_max)
+    x = _b(rng.standard_normal((n, h_in)))
+    y0 = _b(rng.standard_normal((n, h_out)))
+    ids = rng.integers(0, P, n).astype(np.int32)
+    if p_invalid > 0:
+        bad = rng.random(n) < p_invalid
+        ids[bad] = rng.choice([-1, P], bad.sum())
+    return x, A_ar, B_ar, slots, rank_of, As, Bs, y0, ids
+
+
+def place_adapters(rng, slots, rank_of, n_slots, h_in, h_out, r_max):
+    """Arenas of n_slots slots (random junk) with adapter a, rank rank_of[a],
+    written at the start of slot slots[a]; returns the arenas and the
+    adapters' A [h_in][r] and B [r][h_out]."""
+    A_ar = _b(rng.standard_normal((n_slots, h_in * r_max)))
+    B_ar = _b(rng.standard_normal((n_slots, r_max * h_out)))
+    As, Bs = [], []
+    for a in range(len(slots)):
+        r = int(rank_of[a])
+        A = _b(rng.standard_normal((h_in, r)) / np.sqrt(h_in))
+        B = _b(rng.standard_normal((r, h_out)) / np.sqrt(r))
+        A_ar[slots[a], : h_in * r] = A.reshape(-1)
+        B_ar[slots[a], : r * h_out] = B.reshape(-1)
+        As.append(A)
+        Bs.append(B)
+    return A_ar, B_ar, As, Bs
+
+
+def _mask(ranks):
+    m = 0
+    for r in ranks:
+        m |= 1 << (int(r).bit_length() - 4)
+    return m
+
+
+def pin_slots_dense_bruteforce(mutant=0):
+    """Mixed ranks in shuffled slots against y0 + s * x . (A_a . B_a) in fp64
+    (the other association), within the fp32 forward error bound."""
+    rng = np.random.default_rng(21)
+    for n, P, n_slots, h_in, h_out, r_max, ranks in [(24, 5, 9, 64, 40, 64, [8, 16, 32, 64]),
+                                                       (10, 3, 3, 32, 48, 32, [8, 32]),
+                                                       (7, 4, 6, 16, 24, 16, [8, 16])]:
+        x, A_ar, B_ar, slots, rank_of, As, Bs, y0, ids = slot_problem(rng, n, P, n_slots, h_in, h_out, r_max,
+                                                                      ranks, p_invalid=0.1)
+        s = float(rng.choice([0.5, -1.5, 2.0]))
+        xf, yf = (f32_from_bf16_bits(t).astype(np.float64) for t in (x, y0))
+        ref, bound = yf.copy(), np.zeros_like(yf)
+        for i, a in enumerate(ids):
+            if 0 <= a < P:
+                Af, Bf = (f32_from_bf16_bits(t).astype(np.float64) for t in (As[a], Bs[a]))
+                ref[i] = yf[i] + s * (xf[i] @ (Af @ Bf))
+                mag = np.abs(yf[i]) + abs(s) * ((np.abs(xf[i]) @ np.abs(Af)) @ np.abs(Bf))
+                bound[i] = (h_in + Af.shape[1] + 3) * U32 * mag * 1.01
+        y = oracle.sgmv_slots_ref(x, A_ar, B_ar, slots, rank_of, r_max, _mask(ranks), ids, s, y0, mutant=mutant)
+        assert np.all(np.abs(y - ref) <= bound), np.max(np.abs(y - ref) - bound)
+
+
+def pin_slots_zero_padding(mutant=0):
+    """Each adapter zero-padded to rank r_max in a contiguous pool gives the
+    same values through the (separately pinned) contiguous-pool oracle: the
+    extra ranks add exact zeros after the real terms."""
+    rng = np.random.default_rng(22)
+    n, P, n_slots, h_in, h_out, r_max = 30, 6, 8, 48, 56, 64
+    ranks = [8, 16, 32, 64]
+    x, A_ar, B_ar, slots, rank_of, As, Bs, y0, ids = slot_problem(rng, n, P, n_slots, h_in, h_out, r_max, ranks)
+    A_pad = np.zeros((P, h_in, r_max), np.uint16)
+    B_pad = np.zeros((P, r_max, h_out), np.uint16)
+    for a in range(P):
+        r = int(rank_of[a])
+        A_pad[a, :, :r] = As[a]
+        B_pad[a, :r, :] = Bs[a]
+    y = oracle.sgmv_slots_ref(x, A_ar, B_ar, slots, rank_of, r_max, _mask(ranks), ids, 1.25, y0, mutant=mutant)
+    ref = oracle.sgmv_ref(x, A_pad, B_pad, ids, 1.25, y0)
+    assert np.array_equal(y, ref)
+
+
+def pin_slots_invalid_entries(mutant=0):
+    """A slot outside the arena, a rank that is not allowed, above the slot
+    capacity or not a LoRA rank, and an id outside the table: y = y0."""
+    rng = np.random.default_rng(23)
+    n, P, n_slots, h_in, h_out, r_max = 16, 7, 8, 32, 24, 32
+    x, A_ar, B_ar, slots, rank_of, As, Bs, y0, ids = slot_problem(rng, n, P, n_slots, h_in, h_out, r_max, [8, 16])
+    slots[1], slots[2] = n_slots, -1
+    rank_of[3], rank_of[4], rank_of[5] = 32, 64, 12  # 32 not in the mask; 64 > r_max; 12 no rank
+    ids[:8] = [0, 1, 2, 3, 4, 5, 6, P]
+    y, bad = oracle.sgmv_slots_ref(x, A_ar, B_ar, slots, rank_of, r_max, _mask([8, 16]), ids, 1.0, y0,
+                                   mutant=mutant, return_invalid=True)
+    y0f = f32_from_bf16_bits(y0)
+    rows_bad = np.isin(ids, [1, 2, 3, 4, 5, P])
+    assert bad == int(rows_bad.sum())
+    assert np.array_equal(y[rows_bad], y0f[rows_bad])
+    assert not np.array_equal(y[~rows_bad], y0f[~rows_bad])
+
+
+def pin_slots_relocation(mutant=0):
+    """Moving adapters to other slots (and the table with them) changes nothing."""
+    rng = np.random.default_rng(24)
+    n, P, n_slots, h_in, h_out, r_max = 20, 5, 9, 40, 32, 32
+    x, A_ar, B_ar, slots, rank_of, As, Bs, y0, ids = slot_problem(rng, n, P, n_slots, h_in, h_out, r_max,
+                                                                  [8, 16, 32])
+    y = oracle.sgmv_slots_ref(x, A_ar, B_ar, slots, rank_of, r_max, 7, ids, 0.5, y0, mutant=mutant)
+    new = rng.permutation(n_slots)[:P].astype(np.int32)
+    A2 = _b(rng.standard_normal(A_ar.shape))
+    B2 = _b(rng.standard_normal(B_ar.shape))
+    A2[new], B2[new] = A_ar[slots], B_ar[slots]
+    y2 = oracle.sgmv_slots_ref(x, A2, B2, new, rank_of, r_max, 7, ids, 0.5, y0, mutant=mutant)
+    assert np.array_equal(y, y2)
+
+
 ALL_PINS = [
     pin_golden_segment,
     pin_golden_sgmv,
@@ -207,4 +326,8 @@ ALL_PINS = [
     pin_permutation,
     pin_linear_in_s,
     pin_rank1_closed_form,
+    pin_slots_dense_bruteforce,
+    pin_slots_zero_padding,
+    pin_slots_invalid_entries,
+    pin_slots_relocation,
 ]

@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.lora_abi_version() == 1
+    assert lib.lora_abi_version() == 2
     for code, name in lsg.STATUS.items():
         assert lib.lora_status_str(code).decode().startswith(name)
     assert lib.lora_status_str(12345) == b"unknown status"
@@ -98,6 +98,34 @@ def test_host_validation_without_gpu(lib):
     arr = (lsg.lora_sgmv.LoraProj * 9)()
     assert lib.sgmv_multi(arr, 9, 4, 16, ctypes.byref(s), None, None) == -3
     assert lib.sgmv_multi(arr, 0, 4, 16, ctypes.byref(s), None, None) == -1
+
+
+def test_slot_table_validation_without_gpu(lib):
+    """sgmv_multi_slots rejects bad tables before any CUDA call."""
+    P = ctypes.c_void_p
+    s = _seg_struct()
+    arr = (lsg.lora_sgmv.LoraProj * 1)()
+    arr[0] = lsg.lora_sgmv.LoraProj(256, 256, 256, 256, 64, 64, 64, 64, 1.0)
+    T = lsg.lora_sgmv.LoraSlotTable
+
+    def call(tab, n_proj=1, seg=s):
+        return lib.sgmv_multi_slots(arr, n_proj, None if tab is None else ctypes.byref(tab), ctypes.byref(seg),
+                                    None, None)
+
+    assert call(None) == -1
+    assert call(T(256, 256, 4, 8, 64, 0b1111), n_proj=0) == -1
+    assert call(T(256, 256, 4, 8, 64, 0b1111), n_proj=9) == -3
+    assert call(T(0, 256, 4, 8, 64, 0b0010)) == -1          # slot_of missing
+    assert call(T(256, 258, 4, 8, 64, 0b0010)) == -2        # rank_of misaligned
+    assert call(T(256, 256, 4, 0, 64, 0b0010)) == -1        # no slots
+    assert call(T(256, 256, 4, 8, 48, 0b0010)) == -3        # r_max not a rank
+    assert call(T(256, 256, 4, 8, 16, 0b0100)) == -3        # rank 32 above r_max 16
+    assert call(T(256, 256, 4, 8, 64, 0)) == -3             # empty mask
+    assert call(T(256, 256, 4, 8, 64, 0b10000)) == -3       # unknown rank bit
+    assert call(T(256, 256, 0, 8, 64, 0b0010)) == -1        # no adapters
+    assert call(T(256, 256, 4, 1 << 20, 64, 0b0010)) == -3  # arena rows beyond the tensor-map range
+    zero = _seg_struct(n=0, ms=0, ptrs=False)
+    assert call(T(256, 256, 4, 8, 64, 0b1010), seg=zero) == 0
 
 
 def test_product_path_fails_loudly_without_library(tmp_path):

@@ -23,6 +23,8 @@ MUTANTS = {
     5: "sign of the delta flipped",
     6: "unstable segmentation",
     7: "empty adapters kept as segments",
+    8: "slot stride from the adapter's rank",
+    9: "slot adapters read at the slot capacity's rank",
 }
 
 
