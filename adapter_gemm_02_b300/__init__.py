@@ -16,13 +16,19 @@ from .lora_sgmv import (  # noqa: F401
     lora_segment,
     lora_segment_noalloc,
     lora_segment_workspace_bytes,
+    lora_slot_assign,
+    lora_slot_copy,
+    make_host_projs,
     make_projs,
     make_slot_projs,
+    make_slot_srcs,
     rank_mask,
     sgmv_expand,
     sgmv_fused,
     sgmv_fused_slots,
     sgmv_multi,
+    sgmv_multi_host,
+    sgmv_multi_host_workspace_bytes,
     sgmv_multi_slots,
     sgmv_shrink,
 )
@@ -30,5 +36,6 @@ from .lora_sgmv import (  # noqa: F401
 __all__ = [
     "Segments", "load_library", "lora_segment", "lora_segment_noalloc", "lora_segment_workspace_bytes", "sgmv_shrink", "sgmv_expand",
     "sgmv_fused", "sgmv_multi", "make_projs", "SlotTable", "rank_mask", "make_slot_projs", "sgmv_multi_slots",
-    "sgmv_fused_slots",
+    "sgmv_fused_slots", "lora_slot_copy", "lora_slot_assign", "make_slot_srcs",
+    "sgmv_multi_host", "sgmv_multi_host_workspace_bytes", "make_host_projs",
 ]

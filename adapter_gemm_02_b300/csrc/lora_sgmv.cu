@@ -195,6 +195,134 @@ lora_status sgmv_multi_slots(const lora_proj* projs, int32_t n_proj, const lora_
   return launch_sgmv_cc(c, reinterpret_cast<cudaStream_t>(stream));
 }
 
+}  // extern "C"
+
+namespace lsg {
+namespace {
+
+// Device workspace of a host-memory step: ids, segmentation, histogram
+// workspace, one x per distinct host x, one y per projection (each 256-byte
+// aligned, rows packed at ld = width).
+struct HostPlan {
+  size_t ids, perm, offs, adap, nseg, hist, total;
+  size_t x[kMaxProj], y[kMaxProj];
+  int x_of[kMaxProj];  // projection -> index of its distinct x
+};
+
+size_t al256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+HostPlan host_plan(const lora_proj* projs, int n_proj, int n, int P) {
+  HostPlan h{};
+  const int ms = std::min(n, P);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = al256(o + bytes);
+    return at;
+  };
+  h.ids = take(static_cast<size_t>(n) * 4);
+  h.perm = take(static_cast<size_t>(n) * 4);
+  h.offs = take(static_cast<size_t>(ms + 1) * 4);
+  h.adap = take(static_cast<size_t>(std::max(ms, 1)) * 4);
+  h.nseg = take(4);
+  h.hist = take(seg_plan(n, P).ws_bytes);
+  for (int i = 0; i < n_proj; ++i) {
+    h.x_of[i] = i;
+    for (int j = 0; j < i; ++j)
+      if (projs[j].x == projs[i].x && projs[j].h_in == projs[i].h_in) {
+        h.x_of[i] = h.x_of[j];
+        break;
+      }
+    if (h.x_of[i] == i) h.x[i] = take(static_cast<size_t>(n) * projs[i].h_in * 2);
+  }
+  for (int i = 0; i < n_proj; ++i) h.y[i] = take(static_cast<size_t>(n) * projs[i].h_out * 2);
+  h.total = o;
+  return h;
+}
+
+}  // namespace
+}  // namespace lsg
+
+extern "C" {
+
+size_t sgmv_multi_host_workspace_bytes(const lora_proj* projs, int32_t n_proj, int32_t n_tokens,
+                                       int32_t n_adapters) {
+  if (!projs || n_proj < 1 || n_proj > LORA_MAX_PROJ || n_tokens < 0 || n_adapters < 1) return 0;
+  return host_plan(projs, n_proj, n_tokens, n_adapters).total;
+}
+
+lora_status sgmv_multi_host(const lora_proj* projs, int32_t n_proj, int32_t n_adapters, int32_t r,
+                            const int32_t* ids_host, int32_t n_tokens, void* workspace, size_t workspace_bytes,
+                            int32_t* err_flag, lora_stream_t stream) {
+  if (!projs || n_proj < 1 || n_adapters < 1 || n_tokens < 0) return LORA_ERR_INVALID_ARG;
+  if (n_proj > LORA_MAX_PROJ) return LORA_ERR_UNSUPPORTED;
+  if (!rank_ok(r)) return LORA_ERR_UNSUPPORTED;
+  if (n_tokens == 0) return LORA_OK;
+  if (!ids_host) return LORA_ERR_INVALID_ARG;
+  for (int i = 0; i < n_proj; ++i) {
+    const lora_proj& q = projs[i];
+    // host x / y: widths and leading dimensions only (no device alignment rule)
+    if (!q.x || !q.y || !q.A_pool || !q.B_pool) return LORA_ERR_INVALID_ARG;
+    if (!width_ok(q.h_in) || !width_ok(q.h_out)) return LORA_ERR_UNSUPPORTED;
+    if (q.ldx < q.h_in || q.ldy < q.h_out) return LORA_ERR_INVALID_ARG;
+    if (!al16(q.A_pool) || !al16(q.B_pool)) return LORA_ERR_MISALIGNED;
+  }
+  const HostPlan h = host_plan(projs, n_proj, n_tokens, n_adapters);
+  if (!workspace || workspace_bytes < h.total) return LORA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LORA_ERR_MISALIGNED;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto at = [&](size_t off) { return ws + off; };
+  int32_t* ids = reinterpret_cast<int32_t*>(at(h.ids));
+  const size_t n = static_cast<size_t>(n_tokens);
+  if (cudaMemcpyAsync(ids, ids_host, n * 4, cudaMemcpyDefault, st) != cudaSuccess) return LORA_ERR_CUDA;
+  for (int i = 0; i < n_proj; ++i) {
+    const lora_proj& q = projs[i];
+    if (h.x_of[i] == i &&
+        cudaMemcpy2DAsync(at(h.x[i]), q.h_in * 2, q.x, q.ldx * 2, q.h_in * 2, n, cudaMemcpyDefault, st) !=
+            cudaSuccess)
+      return LORA_ERR_CUDA;
+    if (cudaMemcpy2DAsync(at(h.y[i]), q.h_out * 2, q.y, q.ldy * 2, q.h_out * 2, n, cudaMemcpyDefault, st) !=
+        cudaSuccess)
+      return LORA_ERR_CUDA;
+  }
+  lora_segments seg{};
+  seg.perm = reinterpret_cast<int32_t*>(at(h.perm));
+  seg.seg_offsets = reinterpret_cast<int32_t*>(at(h.offs));
+  seg.seg_adapter = reinterpret_cast<int32_t*>(at(h.adap));
+  seg.num_segments = reinterpret_cast<int32_t*>(at(h.nseg));
+  seg.n_tokens = n_tokens;
+  seg.max_segments = std::min(n_tokens, n_adapters);
+  lora_status s = launch_segment(ids, n_tokens, n_adapters, const_cast<int32_t*>(seg.perm),
+                                 const_cast<int32_t*>(seg.seg_offsets), const_cast<int32_t*>(seg.seg_adapter),
+                                 const_cast<int32_t*>(seg.num_segments),
+                                 seg_plan(n_tokens, n_adapters).gmem ? reinterpret_cast<int32_t*>(at(h.hist))
+                                                                     : nullptr,
+                                 err_flag, st);
+  if (s != LORA_OK) return s;
+  SgmvCall c{};
+  c.mode = kModeFused;
+  for (int i = 0; i < n_proj; ++i) {
+    const lora_proj& q = projs[i];
+    c.proj[i] = ProjArgs{reinterpret_cast<const uint16_t*>(at(h.x[h.x_of[i]])), q.A_pool, q.B_pool,
+                         reinterpret_cast<uint16_t*>(at(h.y[i])), q.h_in, q.h_out, q.h_in, q.h_out, q.scale};
+  }
+  c.n_proj = n_proj;
+  c.r = r;
+  c.n_adapters = n_adapters;
+  c.seg = seg;
+  c.err_flag = err_flag;
+  s = launch_sgmv_cc(c, st);
+  if (s != LORA_OK) return s;
+  for (int i = 0; i < n_proj; ++i) {
+    const lora_proj& q = projs[i];
+    if (cudaMemcpy2DAsync(q.y, q.ldy * 2, at(h.y[i]), q.h_out * 2, q.h_out * 2, n, cudaMemcpyDefault, st) !=
+        cudaSuccess)
+      return LORA_ERR_CUDA;
+  }
+  return LORA_OK;
+}
+
 lora_status sgmv_fused(const lora_bf16* x, int64_t ldx, const lora_bf16* A_pool, const lora_bf16* B_pool,
                        int32_t n_adapters, int32_t h_in, int32_t h_out, int32_t r, float scale,
                        const lora_segments* seg, lora_bf16* y, int64_t ldy, int32_t* err_flag,

@@ -26,7 +26,8 @@ STATUS = {
 }
 # exported symbols declared in include/lora_sgmv.h
 SYMBOLS = ("lora_status_str", "lora_abi_version", "lora_segment_workspace_bytes", "lora_segment",
-           "lora_segment_noalloc", "sgmv_shrink", "sgmv_expand", "sgmv_fused", "sgmv_multi", "sgmv_multi_slots")
+           "lora_segment_noalloc", "sgmv_shrink", "sgmv_expand", "sgmv_fused", "sgmv_multi", "sgmv_multi_slots",
+           "lora_slot_copy", "lora_slot_assign", "sgmv_multi_host_workspace_bytes", "sgmv_multi_host")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -44,6 +45,11 @@ class LoraProj(ctypes.Structure):
 class LoraSlotTable(ctypes.Structure):
     _fields_ = [("slot_of", ctypes.c_void_p), ("rank_of", ctypes.c_void_p), ("n_adapters", ctypes.c_int32),
                 ("n_slots", ctypes.c_int32), ("r_max", ctypes.c_int32), ("rank_mask", ctypes.c_uint32)]
+
+
+class LoraSlotSrc(ctypes.Structure):
+    _fields_ = [("A_arena", ctypes.c_void_p), ("B_arena", ctypes.c_void_p), ("A_src", ctypes.c_void_p),
+                ("B_src", ctypes.c_void_p), ("h_in", ctypes.c_int32), ("h_out", ctypes.c_int32)]
 
 
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
@@ -77,6 +83,14 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sgmv_multi_slots.restype = ctypes.c_int
     lib.sgmv_multi_slots.argtypes = [ctypes.POINTER(LoraProj), i32, ctypes.POINTER(LoraSlotTable),
                                      ctypes.POINTER(LoraSegments), p, p]
+    lib.sgmv_multi_host_workspace_bytes.restype = sz
+    lib.sgmv_multi_host_workspace_bytes.argtypes = [ctypes.POINTER(LoraProj), i32, i32, i32]
+    lib.sgmv_multi_host.restype = ctypes.c_int
+    lib.sgmv_multi_host.argtypes = [ctypes.POINTER(LoraProj), i32, i32, i32, p, i32, p, sz, p, p]
+    lib.lora_slot_copy.restype = ctypes.c_int
+    lib.lora_slot_copy.argtypes = [ctypes.POINTER(LoraSlotSrc), i32, i32, i32, i32, i32, p]
+    lib.lora_slot_assign.restype = ctypes.c_int
+    lib.lora_slot_assign.argtypes = [p, p, i32, i32, i32, i32, p]
     _lib = lib
     return lib
 
@@ -344,3 +358,88 @@ def sgmv_fused_slots(x: torch.Tensor, A_arena: torch.Tensor, B_arena: torch.Tens
     """One projection of sgmv_multi_slots (in place on y)."""
     sgmv_multi_slots([(x, A_arena, B_arena, y, scale)], table, seg, err_flag=err_flag, stream=stream)
     return y
+
+
+def make_slot_srcs(srcs: Sequence, r_max: int) -> "ctypes.Array":
+    """Host array of lora_slot_src from (A_arena, B_arena, A_src, B_src)
+    tuples: arenas [n_slots, h_in*r_max] / [n_slots, r_max*h_out] on the GPU,
+    sources A [h_in, rank] / B [rank, h_out], contiguous, in pinned host or
+    device memory."""
+    arr = (LoraSlotSrc * len(srcs))()
+    for i, (Aa, Ba, As, Bs) in enumerate(srcs):
+        _req(Aa, "A_arena", torch.bfloat16, 2)
+        _req(Ba, "B_arena", torch.bfloat16, 2)
+        for t, nm in ((As, "A_src"), (Bs, "B_src")):
+            if t.dtype != torch.bfloat16 or t.dim() != 2 or not t.is_contiguous():
+                raise ValueError(f"{nm} must be a contiguous 2-D bf16 tensor")
+            if not t.is_cuda and not t.is_pinned():
+                raise ValueError(f"{nm} in host memory must be pinned (asynchronous copy)")
+        h_in, rank = As.shape
+        rank2, h_out = Bs.shape
+        if rank2 != rank or Aa.shape[1] != h_in * r_max or Ba.shape[1] != r_max * h_out:
+            raise ValueError(f"source {i}: shapes do not match the arenas")
+        arr[i] = LoraSlotSrc(Aa.data_ptr(), Ba.data_ptr(), As.data_ptr(), Bs.data_ptr(), h_in, h_out)
+    return arr
+
+
+def lora_slot_copy(srcs: Sequence, n_slots: int, r_max: int, slot: int, rank: int, *, stream=None,
+                   c_srcs=None) -> None:
+    """Copy one adapter's matrices into `slot` of each arena pair (stream-ordered)."""
+    lib = load_library()
+    arr = c_srcs if c_srcs is not None else make_slot_srcs(srcs, r_max)
+    _check(lib.lora_slot_copy(arr, len(arr), int(n_slots), int(r_max), int(slot), int(rank), _stream(stream)),
+           "lora_slot_copy")
+
+
+def lora_slot_assign(table: SlotTable, adapter: int, slot: int, rank: int = 0, *, stream=None) -> None:
+    """slot_of[adapter] = slot, rank_of[adapter] = rank on the GPU (slot -1 evicts)."""
+    lib = load_library()
+    _check(lib.lora_slot_assign(_ptr(table.slot_of), _ptr(table.rank_of), table.n_adapters, int(adapter), int(slot),
+                                int(rank), _stream(stream)), "lora_slot_assign")
+
+
+def make_host_projs(projs: Sequence) -> "ctypes.Array":
+    """Host array of lora_proj for sgmv_multi_host from (x_host, A_pool,
+    B_pool, y_host, scale) tuples: x_host [n, >=h_in] and y_host [n, >=h_out]
+    bf16 CPU tensors (pinned, for an asynchronous call), pools on the GPU."""
+    arr = (LoraProj * len(projs))()
+    for i, (x, A, B, y, s) in enumerate(projs):
+        for t, nm in ((x, "x_host"), (y, "y_host")):
+            if t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 2:
+                raise ValueError(f"{nm} must be a 2-D bf16 CPU tensor")
+            if not t.is_pinned():
+                raise ValueError(f"{nm} must be pinned (asynchronous copies)")
+        _pool(A, "A_pool")
+        _pool(B, "B_pool")
+        if A.shape[2] != B.shape[1] or x.shape[1] < A.shape[1] or y.shape[1] < B.shape[2]:
+            raise ValueError(f"projection {i}: shape mismatch")
+        arr[i] = LoraProj(x.data_ptr(), A.data_ptr(), B.data_ptr(), y.data_ptr(), _rows(x, "x"), _rows(y, "y"),
+                          A.shape[1], B.shape[2], float(s))
+    return arr
+
+
+def sgmv_multi_host_workspace_bytes(c_projs, n_tokens: int, n_adapters: int) -> int:
+    return int(load_library().sgmv_multi_host_workspace_bytes(c_projs, len(c_projs), int(n_tokens),
+                                                              int(n_adapters)))
+
+
+def sgmv_multi_host(projs: Sequence, ids_host: torch.Tensor, *, workspace: Optional[torch.Tensor] = None,
+                    err_flag: Optional[torch.Tensor] = None, stream=None, c_projs=None) -> torch.Tensor:
+    """The whole step from host memory (include/lora_sgmv.h): ids_host int32
+    [n] and the projections' x / y pinned CPU tensors, pools on the GPU; y is
+    updated in place in host memory once the stream reaches the end of the
+    call.  Returns the device workspace (reuse it for the next call)."""
+    lib = load_library()
+    if not 1 <= len(projs) <= LORA_MAX_PROJ:
+        raise ValueError("1..8 projections")
+    if ids_host.is_cuda or ids_host.dtype != torch.int32 or ids_host.dim() != 1 or not ids_host.is_pinned():
+        raise ValueError("ids_host must be a pinned 1-D int32 CPU tensor")
+    arr = c_projs if c_projs is not None else make_host_projs(projs)
+    P, _, r = projs[0][1].shape
+    n = ids_host.shape[0]
+    need = sgmv_multi_host_workspace_bytes(arr, n, P)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=projs[0][1].device)
+    _check(lib.sgmv_multi_host(arr, len(arr), P, r, _ptr(ids_host), n, _ptr(workspace), workspace.numel(),
+                               _ptr(err_flag), _stream(stream)), "sgmv_multi_host")
+    return workspace

@@ -37,7 +37,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from workloads import WORKLOADS, make_inputs  # noqa: E402
+from workloads import WORKLOADS, distinct_ids, make_inputs  # noqa: E402
 
 DEFAULT_WORKLOAD = "7b_proj_distinct"
 METRIC = "fused SGMV µs & % HBM roofline, Llama2-7B dims r=16 bs32 mixed adapters"
@@ -346,52 +346,60 @@ def run_ours(args) -> None:
     clocks = sampler.stop()
     assert int(err.item()) == 0, f"device error flag {int(err.item())}"
 
-    # end to end through the Python API from pinned host memory
+    # end to end from pinned host memory through the C-ABI host-step call.
+    # Two pipelines (stream, pinned host buffers, device workspace) take the
+    # steps in turn, so one step's uploads overlap the previous step's kernels
+    # and download; every step still copies its own inputs in and its y out.
     e2e = None
     if not args.no_e2e:
-        inp0, seg0, projs0, cproj0 = copies[0]
-        h_ids = inp0.ids.cpu().pin_memory()
-        h_x = {k: v.cpu().pin_memory() for k, v in inp0.x.items()}
-        h_y = [y.cpu().pin_memory() for y in inp0.y0]
-        h_out = [torch.empty_like(y).pin_memory() for y in h_y]
-        d_ids = torch.empty_like(inp0.ids)
-        d_x = {k: torch.empty_like(v) for k, v in inp0.x.items()}
-        d_y = [torch.empty_like(y) for y in inp0.y0]
-        seg_e = lsg.Segments.empty(wl.n, wl.P, dev)
-        dprojs = [(d_x[p.x_key], inp0.A[i], inp0.B[i], d_y[i], wl.scale) for i, p in enumerate(wl.projs)]
-        cdp = lsg.make_projs(dprojs)
+        inp0 = copies[0][0]
+        pipes = []
+        for _ in range(2):
+            h_ids = inp0.ids.cpu().pin_memory()
+            h_x = {k: v.cpu().pin_memory() for k, v in inp0.x.items()}
+            h_y = [y.cpu().pin_memory() for y in inp0.y0]
+            hprojs = [(h_x[p.x_key], inp0.A[i], inp0.B[i], h_y[i], wl.scale) for i, p in enumerate(wl.projs)]
+            chp = lsg.make_host_projs(hprojs)
+            ws = torch.empty(lsg.sgmv_multi_host_workspace_bytes(chp, wl.n, wl.P), dtype=torch.uint8, device=dev)
+            pipes.append((torch.cuda.Stream(dev), h_ids, hprojs, chp, ws))
         bi = h_ids.numel() * 4 + sum(v.numel() * 2 for v in h_x.values()) + sum(y.numel() * 2 for y in h_y)
-        bo = sum(y.numel() * 2 for y in h_out)
+        bo = sum(y.numel() * 2 for y in h_y)
 
-        def e2e_step():
-            d_ids.copy_(h_ids, non_blocking=True)
-            for k in d_x:
-                d_x[k].copy_(h_x[k], non_blocking=True)
-            for d, h in zip(d_y, h_y):
-                d.copy_(h, non_blocking=True)
-            lsg.lora_segment(d_ids, wl.P, out=seg_e, err_flag=err)
-            if len(dprojs) == 1:
-                x, A, B, y, s = dprojs[0]
-                lsg.sgmv_fused(x, A, B, seg_e, y, s, err_flag=err)
-            else:
-                lsg.sgmv_multi(dprojs, seg_e, err_flag=err, c_projs=cdp)
-            for h, d in zip(h_out, d_y):
-                h.copy_(d, non_blocking=True)
+        def e2e_step(k, n_pipes):
+            st, h_ids, hprojs, chp, ws = pipes[k % n_pipes]
+            lsg.sgmv_multi_host(hprojs, h_ids, workspace=ws, err_flag=err, stream=st, c_projs=chp)
 
-        for _ in range(Wm):
-            e2e_step()
-        torch.cuda.synchronize()
-        barrier(world)
-        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        f0.record()
-        for _ in range(K):
-            e2e_step()
-        f1.record()
-        torch.cuda.synchronize()
-        barrier(world)
-        e2e_us = reduce_max(f0.elapsed_time(f1) / K * 1e3, world)
+        def e2e_time(n_pipes):
+            main = torch.cuda.current_stream()
+            for k in range(Wm):
+                e2e_step(k, n_pipes)
+            torch.cuda.synchronize()
+            barrier(world)
+            f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            f0.record(main)
+            for st, *_ in pipes[:n_pipes]:
+                st.wait_event(f0)
+            h0 = time.perf_counter()
+            for k in range(K):
+                e2e_step(k, n_pipes)
+            host = (time.perf_counter() - h0) / K * 1e6
+            for st, *_ in pipes[:n_pipes]:
+                ev = torch.cuda.Event()
+                ev.record(st)
+                main.wait_event(ev)
+            f1.record(main)
+            torch.cuda.synchronize()
+            barrier(world)
+            return reduce_max(f0.elapsed_time(f1) / K * 1e3, world), host
+
+        e2e_us, host_us = e2e_time(2)
+        serial_us, _ = e2e_time(1)
         e2e = {"value": round(e2e_us, 3), "unit": "us", "h2d_bytes_per_step": int(bi),
-               "d2h_bytes_per_step": int(bo), "path": "python API, pinned host buffers, stream-ordered copies"}
+               "d2h_bytes_per_step": int(bo), "host_enqueue_us_per_step": round(host_us, 2),
+               "one_stream_us": round(serial_us, 3),
+               "path": "sgmv_multi_host (C ABI): H2D of ids, x, y0 from pinned host memory, segmentation, SGMV, "
+                       "D2H of y, one library call per step; two streams take the steps in turn "
+                       "(one_stream_us: every step on one stream)"}
 
     # mixed vs single adapter on the same shape (Punica: almost no difference)
     mixed = None
@@ -430,6 +438,9 @@ def run_ours(args) -> None:
         out["mixed_vs_single_us"] = mixed
     if args.batch_curve:
         out["batch_curve_us"] = batch_curve(K, Wm, dev, lsg, args.max_copies)
+    if not args.no_slots and world == 1:
+        out["slot_pool_us"] = slots_measure(K, Wm, dev, lsg, args.max_copies, peak)
+        out["pool_loader"] = pool_loader_measure(g_step, K, dev, lsg)
     if rank == 0 and world == 1 and not args.no_cpu:
         threads = os.cpu_count() or 1
         inp_cpu = make_inputs(wl, "cpu")
@@ -532,6 +543,139 @@ def _time_ids(wl, ids, K, Wm, dev, lsg, max_copies):
     return round(t, 3)
 
 
+def _time_slots(h_in, h_out, ids, rank_of, n_slots, r_max, ranks, K, Wm, dev, lsg, max_copies, name):
+    """Microseconds per step (segment + sgmv_multi_slots, one projection)."""
+    import torch
+    from workloads import make_slot_inputs
+
+    P = len(rank_of)
+    used = np.unique(ids)
+    bytes_ = int(sum((h_in + h_out) * 2 * int(rank_of[a]) for a in used) + ids.size * (h_in + 2 * h_out) * 2)
+    NB = max(2, min(max_copies, int(np.ceil(2.2 * L2_BYTES / bytes_))))
+    copies = []
+    for c in range(NB):
+        si = make_slot_inputs(h_in, h_out, ids, rank_of, n_slots, r_max, dev, copy=c, name=name)
+        tab = lsg.SlotTable(si.slot_of, si.rank_of, n_slots, r_max, lsg.rank_mask(ranks))
+        cp = lsg.make_slot_projs([(si.x, si.A_arena, si.B_arena, si.y0, 1.0)], tab)
+        copies.append((si, tab, cp, lsg.Segments.empty(ids.size, P, dev)))
+    side = torch.cuda.Stream(dev)
+
+    def step(k):
+        si, tab, cp, seg = copies[k % NB]
+        lsg.lora_segment(si.ids, P, out=seg)
+        lsg.sgmv_multi_slots([(si.x, si.A_arena, si.B_arena, si.y0, 1.0)], tab, seg, c_projs=cp)
+
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for k in range(max(Wm, NB)):
+            step(k)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for k in range(K):
+            step(k)
+    t = _time_graph(g, side) / K * 1e3
+    del g, copies
+    torch.cuda.empty_cache()
+    return round(t, 3), bytes_
+
+
+def slots_measure(K, Wm, dev, lsg, max_copies, peak):
+    """Slot arenas (capacity r=64, 96 slots, pool of 64 adapters) on the
+    Llama2-7B decode projection 4096->4096, 32 tokens of 32 distinct adapters:
+    ranks 8/16/32/64 mixed in one launch, against the same batch with every
+    adapter at r=16 through the slot table (one-rank kernel)."""
+    P, n, n_slots, r_max = 64, 32, 96, 64
+    ids = np.asarray(distinct_ids(n, P, seed=0), np.int32)
+    mixed_r = np.array([(8, 16, 32, 64)[a % 4] for a in range(P)], np.int32)
+    out = {"workload": "Llama2-7B decode projection 4096->4096, 32 tokens, 32 distinct adapters of 64, "
+                       "96 slots of capacity r=64"}
+    us, b = _time_slots(4096, 4096, ids, mixed_r, n_slots, r_max, (8, 16, 32, 64), K, Wm, dev, lsg, max_copies,
+                        "slots_mixed")
+    out["mixed_ranks_8_16_32_64"] = {"us": us, "algorithmic_bytes": b, "gbs": round(b / us / 1e3, 1),
+                                     "frac_of_measured_hbm": round(b / us / 1e3 / peak, 4)}
+    us16, b16 = _time_slots(4096, 4096, ids, np.full(P, 16, np.int32), n_slots, r_max, (16,), K, Wm, dev, lsg,
+                            max_copies, "slots_r16")
+    out["all_rank_16"] = {"us": us16, "algorithmic_bytes": b16, "gbs": round(b16 / us16 / 1e3, 1),
+                          "frac_of_measured_hbm": round(b16 / us16 / 1e3 / peak, 4)}
+    return out
+
+
+def pool_loader_measure(g_step, K, dev, lsg, n_layers=32, reps=5):
+    """Loading one Llama2-7B adapter (r=16, 32 layers x 7 projections: 224 A
+    and 224 B matrices, 80 MB) from pinned host memory into free slots of the
+    layers' arenas (lora_slot_copy + lora_slot_assign on a loader stream), as
+    the pages' on-demand loads; alone, and while the bench's step graph runs
+    on the compute stream."""
+    import torch
+    from workloads import llama_projs
+
+    r, r_max, n_slots, P = 16, 16, 4, 64
+    projs = llama_projs("7b")
+    arenas, shapes = [], []
+    for _ in range(n_layers):
+        for pr in projs:
+            arenas.append((torch.empty(n_slots, pr.h_in * r_max, dtype=torch.bfloat16, device=dev),
+                           torch.empty(n_slots, r_max * pr.h_out, dtype=torch.bfloat16, device=dev)))
+            shapes.append((pr.h_in, pr.h_out))
+    total = sum(hi * r + r * ho for hi, ho in shapes)
+    host = torch.randn(total, dtype=torch.float32).to(torch.bfloat16).pin_memory()
+    srcs, off = [], 0
+    for (Aa, Ba), (hi, ho) in zip(arenas, shapes):
+        A_src = host[off: off + hi * r].view(hi, r)
+        off += hi * r
+        B_src = host[off: off + r * ho].view(r, ho)
+        off += r * ho
+        srcs.append((Aa, Ba, A_src, B_src))
+    c_srcs = lsg.make_slot_srcs(srcs, r_max)
+    table = lsg.SlotTable(torch.full((P,), -1, dtype=torch.int32, device=dev),
+                          torch.zeros(P, dtype=torch.int32, device=dev), n_slots, r_max, lsg.rank_mask([r]))
+    loader = torch.cuda.Stream(dev)
+    compute = torch.cuda.current_stream()
+
+    def load(i):
+        lsg.lora_slot_copy(None, n_slots, r_max, i % n_slots, r, stream=loader, c_srcs=c_srcs)
+        lsg.lora_slot_assign(table, i % P, i % n_slots, r, stream=loader)
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    load(0)
+    torch.cuda.synchronize()
+    alone, host_ms = [], []
+    for i in range(reps):
+        e0, e1 = ev(), ev()
+        e0.record(loader)
+        t0 = time.perf_counter()
+        load(i + 1)
+        host_ms.append((time.perf_counter() - t0) * 1e3)
+        e1.record(loader)
+        torch.cuda.synchronize()
+        alone.append(e0.elapsed_time(e1))
+    # the step graph alone, then with a load issued right after it
+    f0, f1 = ev(), ev()
+    f0.record(compute)
+    g_step.replay()
+    f1.record(compute)
+    torch.cuda.synchronize()
+    step_alone = f0.elapsed_time(f1) / K * 1e3
+    f0, f1, e0, e1 = ev(), ev(), ev(), ev()
+    f0.record(compute)
+    g_step.replay()
+    f1.record(compute)
+    e0.record(loader)
+    load(reps + 1)
+    e1.record(loader)
+    torch.cuda.synchronize()
+    step_during = f0.elapsed_time(f1) / K * 1e3
+    med = float(np.median(alone))
+    return {"adapter": "Llama2-7B, r=16, 32 layers x 7 projections", "bytes": int(total * 2),
+            "copies": 2 * len(srcs), "load_ms": round(med, 3), "gbs": round(total * 2 / med / 1e6, 1),
+            "host_enqueue_ms": round(float(np.median(host_ms)), 3),
+            "load_ms_during_steps": round(e0.elapsed_time(e1), 3),
+            "step_us_alone": round(step_alone, 3), "step_us_during_load": round(step_during, 3),
+            "how": "pinned host -> slot arenas, one cudaMemcpyAsync per matrix on a loader stream, then the "
+                   "table entry; CUDA events on the loader and compute streams"}
+
+
 def batch_curve(K, Wm, dev, lsg, max_copies):
     """Step latency against batch size, identical vs mixed adapters, for a
     decode projection (Llama2-7B 4096->4096, r=16) and a prefill projection
@@ -578,6 +722,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-mixed", action="store_true")
+    ap.add_argument("--no-slots", action="store_true", help="skip the slot-arena / mixed-rank measurement")
     ap.add_argument("--batch-curve", action="store_true",
                     help="add step latency against batch size (decode and prefill, identical vs mixed adapters)")
     args = ap.parse_args(argv)

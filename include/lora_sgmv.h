@@ -213,6 +213,26 @@ LORA_API lora_status sgmv_multi(const lora_proj* projs, int32_t n_proj, int32_t 
                        const lora_segments* seg, int32_t* err_flag, lora_stream_t stream);
 
 /*
+ * The whole step from host memory: token ids, x and y0 rows in host memory
+ * (pinned for an asynchronous call), adapter pools on the device.  Copies
+ * ids, every distinct x and every y to the device workspace, runs
+ * lora_segment and sgmv_multi on them and copies every y back, all ordered
+ * on `stream` with one cudaMemcpyAsync / cudaMemcpy2DAsync per buffer; the
+ * caller synchronises before reading y.  projs[i].x / .y are HOST pointers
+ * here (x [n][ldx], y [n][ldy]); A_pool / B_pool are device pointers.
+ * Projections that name the same host x share one device copy.  The
+ * workspace (device, 256-byte aligned, caller-owned) must hold
+ * sgmv_multi_host_workspace_bytes(...) bytes.  Errors: as lora_segment and
+ * sgmv_multi, plus ids_host NULL (LORA_ERR_INVALID_ARG), workspace missing or
+ * too small (LORA_ERR_WORKSPACE), a failed copy (LORA_ERR_CUDA).
+ */
+LORA_API size_t sgmv_multi_host_workspace_bytes(const lora_proj* projs, int32_t n_proj, int32_t n_tokens,
+                                                int32_t n_adapters);
+LORA_API lora_status sgmv_multi_host(const lora_proj* projs, int32_t n_proj, int32_t n_adapters, int32_t r,
+                                     const int32_t* ids_host, int32_t n_tokens, void* workspace,
+                                     size_t workspace_bytes, int32_t* err_flag, lora_stream_t stream);
+
+/*
  * Slot tables: adapter pools stored as arenas of fixed-size slots, so that
  * adapters are loaded into free slots and evicted while the pool is in use,
  * and adapters of different ranks share one launch.  Punica: Multi-Tenant
@@ -255,6 +275,50 @@ typedef struct {
  */
 LORA_API lora_status sgmv_multi_slots(const lora_proj* projs, int32_t n_proj, const lora_slot_table* table,
                                       const lora_segments* seg, int32_t* err_flag, lora_stream_t stream);
+
+/*
+ * Adapter loading into slot arenas.  Punica: Multi-Tenant LoRA Serving
+ * (research.elamur.ai summary), "Summary": an adapter is loaded on demand and
+ * the load takes milliseconds.  A load is a copy of the adapter's matrices
+ * into a free slot of every arena (lora_slot_copy, e.g. on a loader stream
+ * while SGMV runs on another), followed by the table entry that makes the
+ * adapter id point at the slot (lora_slot_assign, ordered after the copies).
+ * The caller orders the steps around the batches: a slot is reused only
+ * after the last batch that reads its old adapter, and a batch names a new
+ * adapter only after its lora_slot_assign.
+ */
+typedef struct {
+  lora_bf16* A_arena;     /* device [n_slots][h_in * r_max] */
+  lora_bf16* B_arena;     /* device [n_slots][r_max * h_out] */
+  const lora_bf16* A_src; /* [h_in][rank] row-major: pinned host memory (asynchronous) or device memory */
+  const lora_bf16* B_src; /* [rank][h_out] row-major */
+  int32_t h_in, h_out;
+} lora_slot_src;
+
+/*
+ * Copies adapter matrices into slot `slot` of each listed arena pair (any
+ * number of pairs: all projections of all layers), packed at the slot start
+ * as the slot layout requires, with one cudaMemcpyAsync per matrix on
+ * `stream` (cudaMemcpyDefault: host or device sources; a pageable host source
+ * makes the call wait for its copy).  Errors: srcs NULL or n_src < 1, a NULL
+ * pointer, slot outside [0, n_slots), rank not in {8,16,32,64} or above r_max,
+ * widths not multiples of 8 (LORA_ERR_INVALID_ARG / LORA_ERR_UNSUPPORTED),
+ * arenas not 16-byte aligned (LORA_ERR_MISALIGNED), a failed copy
+ * (LORA_ERR_CUDA; earlier copies of the call may have been issued).
+ */
+LORA_API lora_status lora_slot_copy(const lora_slot_src* srcs, int32_t n_src, int32_t n_slots, int32_t r_max,
+                                    int32_t slot, int32_t rank, lora_stream_t stream);
+
+/*
+ * Table entry of adapter `adapter`: slot_of[adapter] = slot, rank_of[adapter]
+ * = rank, written by a one-thread kernel on `stream`.  slot = -1 evicts the
+ * adapter (rank is then stored as 0): later batches that name it get
+ * LORA_ERR_BAD_ADAPTER_ID in their err_flag.  Errors: NULL or misaligned
+ * tables, adapter outside [0, n_adapters), slot < -1, rank invalid for a
+ * slot >= 0.
+ */
+LORA_API lora_status lora_slot_assign(int32_t* slot_of, int32_t* rank_of, int32_t n_adapters, int32_t adapter,
+                                      int32_t slot, int32_t rank, lora_stream_t stream);
 
 #ifdef __cplusplus
 }

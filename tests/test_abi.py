@@ -128,6 +128,53 @@ def test_slot_table_validation_without_gpu(lib):
     assert call(T(256, 256, 4, 8, 64, 0b1010), seg=zero) == 0
 
 
+def test_slot_loader_validation_without_gpu(lib):
+    """lora_slot_copy / lora_slot_assign reject bad arguments before any CUDA call."""
+    S = lsg.lora_sgmv.LoraSlotSrc
+    arr = (S * 1)()
+    arr[0] = S(256, 256, 256, 256, 64, 64)
+    assert lib.lora_slot_copy(None, 1, 4, 16, 0, 16, None) == -1
+    assert lib.lora_slot_copy(arr, 0, 4, 16, 0, 16, None) == -1
+    assert lib.lora_slot_copy(arr, 1, 4, 16, 4, 16, None) == -1     # slot outside
+    assert lib.lora_slot_copy(arr, 1, 4, 16, -1, 16, None) == -1
+    assert lib.lora_slot_copy(arr, 1, 4, 16, 0, 32, None) == -3     # rank above r_max
+    assert lib.lora_slot_copy(arr, 1, 4, 24, 0, 8, None) == -3      # r_max not a rank
+    bad = (S * 1)()
+    bad[0] = S(256, 264, 256, 256, 64, 64)
+    assert lib.lora_slot_copy(bad, 1, 4, 16, 0, 16, None) == -2      # B arena misaligned
+    bad[0] = S(256, 256, 0, 256, 64, 64)
+    assert lib.lora_slot_copy(bad, 1, 4, 16, 0, 16, None) == -1      # no source
+    bad[0] = S(256, 256, 256, 256, 60, 64)
+    assert lib.lora_slot_copy(bad, 1, 4, 16, 0, 16, None) == -3      # width
+    P = ctypes.c_void_p
+    assert lib.lora_slot_assign(None, P(256), 4, 0, 0, 16, None) == -1
+    assert lib.lora_slot_assign(P(256), P(258), 4, 0, 0, 16, None) == -2
+    assert lib.lora_slot_assign(P(256), P(256), 4, 4, 0, 16, None) == -1   # adapter outside
+    assert lib.lora_slot_assign(P(256), P(256), 4, 0, -2, 16, None) == -1  # slot below -1
+    assert lib.lora_slot_assign(P(256), P(256), 4, 0, 1, 12, None) == -3   # not a rank
+
+
+def test_host_step_validation_without_gpu(lib):
+    """sgmv_multi_host: workspace sizing and argument checks without a GPU."""
+    P = ctypes.c_void_p
+    arr = (lsg.lora_sgmv.LoraProj * 2)()
+    arr[0] = lsg.lora_sgmv.LoraProj(4096, 256, 256, 8192, 64, 64, 64, 64, 1.0)
+    arr[1] = lsg.lora_sgmv.LoraProj(4096, 256, 256, 16384, 64, 128, 64, 128, 1.0)  # same host x
+    need = lib.sgmv_multi_host_workspace_bytes(arr, 2, 32, 8)
+    # ids, perm, offsets, adapters, count, one x (shared), two y; 256-byte aligned pieces
+    assert need == 256 * 5 + 32 * 64 * 2 + 32 * 64 * 2 + 32 * 128 * 2
+    assert lib.sgmv_multi_host_workspace_bytes(arr, 9, 32, 8) == 0
+    assert lib.sgmv_multi_host(arr, 2, 8, 16, None, 32, P(256), need, None, None) == -1   # no ids
+    assert lib.sgmv_multi_host(arr, 2, 8, 12, P(64), 32, P(256), need, None, None) == -3  # rank
+    assert lib.sgmv_multi_host(arr, 2, 8, 16, P(64), 32, P(256), need - 1, None, None) == -5
+    assert lib.sgmv_multi_host(arr, 2, 8, 16, P(64), 32, None, need, None, None) == -5
+    assert lib.sgmv_multi_host(arr, 2, 8, 16, P(64), 32, P(272), need, None, None) == -2
+    assert lib.sgmv_multi_host(arr, 2, 8, 16, P(64), 0, None, 0, None, None) == 0       # empty batch
+    bad = (lsg.lora_sgmv.LoraProj * 1)()
+    bad[0] = lsg.lora_sgmv.LoraProj(4096, 256, 256, 8192, 60, 64, 64, 64, 1.0)          # ldx < h_in
+    assert lib.sgmv_multi_host(bad, 1, 8, 16, P(64), 32, P(256), need, None, None) == -1
+
+
 def test_product_path_fails_loudly_without_library(tmp_path):
     from adapter_gemm_02_b300 import lora_sgmv
 

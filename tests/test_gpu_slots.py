@@ -141,3 +141,104 @@ def test_relocated_adapters_give_the_same_result():
     c.yd = y_first.clone()
     _run([c], [1.0], P, table=c.table(slots=new))
     assert torch.equal(c.yd, out1)
+
+
+def _pinned(bits: np.ndarray) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    return t.pin_memory()
+
+
+def test_loader_fills_slots_from_pinned_host_and_device_memory():
+    """Empty arenas filled only by lora_slot_copy on a loader stream (sources in
+    pinned host memory for even adapters, device memory for odd ones), table
+    entries by lora_slot_assign; the compute stream waits for the loader's
+    event.  Arena bytes must equal the layout's, outputs the oracle's."""
+    rng = np.random.default_rng(8)
+    P, n, n_slots, h_in, h_out, r_max = 6, 30, 8, 512, 768, 64
+    ranks = [8, 16, 32, 64]
+    slots = rng.permutation(n_slots)[:P].astype(np.int32)
+    rank_of = rng.choice(ranks, P).astype(np.int32)
+    A_ref, B_ref, As, Bs = place_adapters(rng, slots, rank_of, n_slots, h_in, h_out, r_max)
+    A_gpu = torch.zeros(n_slots, h_in * r_max, dtype=torch.bfloat16, device="cuda")
+    B_gpu = torch.zeros(n_slots, r_max * h_out, dtype=torch.bfloat16, device="cuda")
+    # the oracle sees the same arenas, with zeros where nothing was copied
+    A_exp, B_exp = np.zeros_like(A_ref), np.zeros_like(B_ref)
+    for a in range(P):
+        r = int(rank_of[a])
+        A_exp[slots[a], : h_in * r] = A_ref[slots[a], : h_in * r]
+        B_exp[slots[a], : r * h_out] = B_ref[slots[a], : r * h_out]
+    table = lsg.SlotTable(torch.full((P,), -1, dtype=torch.int32, device="cuda"),
+                          torch.zeros(P, dtype=torch.int32, device="cuda"), n_slots, r_max, lsg.rank_mask(ranks))
+    loader = torch.cuda.Stream()
+    keep = []
+    with torch.cuda.stream(loader):
+        for a in range(P):
+            src = _pinned if a % 2 == 0 else _dev
+            As_t, Bs_t = src(As[a]), src(Bs[a])
+            keep += [As_t, Bs_t]
+            lsg.lora_slot_copy([(A_gpu, B_gpu, As_t, Bs_t)], n_slots, r_max, int(slots[a]), int(rank_of[a]))
+            lsg.lora_slot_assign(table, a, int(slots[a]), int(rank_of[a]))
+    done = torch.cuda.Event()
+    done.record(loader)
+    torch.cuda.current_stream().wait_event(done)
+    x = _dev(_b_normal(rng, (n, h_in)))
+    y0 = _b_normal(rng, (n, h_out))
+    y = _dev(y0)
+    ids = rng.integers(0, P, n).astype(np.int32)
+    seg = lsg.lora_segment(torch.from_numpy(ids).cuda(), P)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lsg.sgmv_multi_slots([(x, A_gpu, B_gpu, y, 1.0)], table, seg, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(A_gpu.cpu().view(torch.int16).numpy().view(np.uint16), A_exp)
+    assert np.array_equal(B_gpu.cpu().view(torch.int16).numpy().view(np.uint16), B_exp)
+    assert np.array_equal(table.slot_of.cpu().numpy(), slots)
+    ref = oracle.sgmv_slots_ref(x.cpu(), A_exp, B_exp, slots, rank_of, r_max, lsg.rank_mask(ranks), ids, 1.0, y0,
+                                threads=THREADS)
+    assert_within_tol(y, ref)
+
+
+def _b_normal(rng, shape):
+    from workloads import bf16_bits_from_f32
+
+    return bf16_bits_from_f32(rng.standard_normal(shape).astype(np.float32))
+
+
+def test_evicted_adapter_is_flagged_and_its_rows_untouched():
+    rng = np.random.default_rng(9)
+    P = 5
+    c = SlotCase(rng, 25, P, 6, 256, 512, 16, [8, 16])
+    c.ids[:3] = 2
+    tab = c.table()
+    lsg.lora_slot_assign(tab, 2, -1)
+    y0 = c.yd.clone()
+    _run([c], [1.0], P, table=tab, expect_err=-4)
+    slots = c.slots.copy()
+    slots[2] = -1
+    rows = torch.from_numpy(c.ids == 2).cuda()
+    assert torch.equal(c.yd[rows], y0[rows])
+    assert_within_tol(c.yd, c.ref(1.0, slots=slots))
+
+
+def test_load_on_a_second_stream_while_sgmv_runs():
+    """SGMV over adapters 0..P-2 on the compute stream while adapter P-1 is
+    copied into a free slot on a loader stream: both results are exact."""
+    rng = np.random.default_rng(10)
+    P, n_slots, h, r_max = 8, 10, 2048, 32
+    c = SlotCase(rng, 64, P, n_slots, h, h, r_max, [16, 32], ids=rng.integers(0, P - 1, 64).astype(np.int32))
+    tab = c.table()
+    lsg.lora_slot_assign(tab, P - 1, -1)
+    free = int(np.setdiff1d(np.arange(n_slots), c.slots)[0])
+    A_new = _pinned(_b_normal(rng, (h, 32)))
+    B_new = _pinned(_b_normal(rng, (32, h)))
+    torch.cuda.synchronize()
+    loader = torch.cuda.Stream()
+    with torch.cuda.stream(loader):
+        lsg.lora_slot_copy([(c.Ad, c.Bd, A_new, B_new)], n_slots, r_max, free, 32)
+    _run([c], [0.5], P, table=tab)
+    loader.synchronize()
+    slots = c.slots.copy()
+    slots[P - 1] = -1
+    assert_within_tol(c.yd, c.ref(0.5, slots=slots))
+    got = c.Ad[free, : h * 32].cpu().view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, A_new.view(torch.int16).numpy().view(np.uint16).reshape(-1))

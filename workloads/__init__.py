@@ -9,6 +9,7 @@ arithmetic (no shrink, expand, segmentation or reduction).
 from .gen import (  # noqa: F401
     LLAMA_DIMS,
     Proj,
+    SlotInputs,
     Workload,
     WORKLOADS,
     bf16_bits_from_f32,
@@ -16,6 +17,7 @@ from .gen import (  # noqa: F401
     f32_from_bf16_bits,
     llama_projs,
     make_inputs,
+    make_slot_inputs,
     normal_bf16,
     prefill_ids,
     same_ids,

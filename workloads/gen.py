@@ -212,3 +212,36 @@ def make_inputs(wl: Workload, device="cpu", copy: int = 0,
         B.append(normal_bf16((wl.P, wl.r, p.h_out), 1.0 / wl.r, seed_for(wl.seed_name, "B", p.name, copy), device))
         Y.append(normal_bf16((n, p.h_out), 1.0, seed_for(wl.seed_name, "y0", p.name, copy), device))
     return Inputs(wl, dev_ids, xs, A, B, Y)
+
+
+@dataclass
+class SlotInputs:
+    ids: torch.Tensor       # int32 [n]
+    x: torch.Tensor         # bf16 [n, h_in]
+    A_arena: torch.Tensor   # bf16 [n_slots, h_in * r_max]
+    B_arena: torch.Tensor   # bf16 [n_slots, r_max * h_out]
+    y0: torch.Tensor        # bf16 [n, h_out]
+    slot_of: torch.Tensor   # int32 [P]
+    rank_of: torch.Tensor   # int32 [P]
+
+
+def make_slot_inputs(h_in: int, h_out: int, ids: np.ndarray, rank_of: np.ndarray, n_slots: int, r_max: int,
+                     device="cpu", copy: int = 0, name: str = "slots") -> SlotInputs:
+    """Slot arenas for adapters of the given ranks (A ~ N(0, 1/h_in), B ~
+    N(0, 1/r) at the start of a shuffled slot each, the rest of the arena
+    N(0, 1) junk), with x ~ N(0, 1) and y0 ~ N(0, 1) rows for the tokens `ids`."""
+    P = int(len(rank_of))
+    rng = np.random.default_rng(seed_for(name, "slots", copy))
+    slots = rng.permutation(n_slots)[:P].astype(np.int32)
+    A_ar = normal_bf16((n_slots, h_in * r_max), 1.0, seed_for(name, "A_junk", copy), device)
+    B_ar = normal_bf16((n_slots, r_max * h_out), 1.0, seed_for(name, "B_junk", copy), device)
+    for a in range(P):
+        r = int(rank_of[a])
+        A_ar[int(slots[a]), : h_in * r] = normal_bf16((h_in * r,), 1.0 / h_in, seed_for(name, "A", a, copy), device)
+        B_ar[int(slots[a]), : r * h_out] = normal_bf16((r * h_out,), 1.0 / r, seed_for(name, "B", a, copy), device)
+    ids_np = np.asarray(ids, dtype=np.int32)
+    n = ids_np.size
+    return SlotInputs(torch.from_numpy(ids_np.copy()).to(device),
+                      normal_bf16((n, h_in), 1.0, seed_for(name, "x", copy), device), A_ar, B_ar,
+                      normal_bf16((n, h_out), 1.0, seed_for(name, "y0", copy), device),
+                      torch.from_numpy(slots).to(device), torch.from_numpy(np.asarray(rank_of, np.int32)).to(device))
