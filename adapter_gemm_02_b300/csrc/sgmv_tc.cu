@@ -653,6 +653,26 @@ bool sgmv_tc_applicable(const SgmvCall& call) {
 
 lora_status launch_sgmv_tc(const SgmvCall& call, cudaStream_t stream) {
   TcParams prm{};
+  // Column chunks per projection: about kChunkCols columns each, more when
+  // the batch has fewer (tile, projection) pairs than SMs (one wide
+  // projection over a few tiles), so that every SM gets an item; each extra
+  // chunk re-reads the tile's x and the adapter's A (from L2) for its shrink.
+  static int nsm = 0;
+  if (nsm == 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess)
+      return LORA_ERR_CUDA;
+    nsm = v;
+  }
+  const int tiles_est = std::max(1, ceil_div(call.seg.n_tokens, 128));
+  int64_t cols = 0;
+  int base_items = 0;
+  for (int i = 0; i < call.n_proj; ++i) {
+    cols += call.proj[i].h_out;
+    base_items += std::clamp(ceil_div(call.proj[i].h_out, kChunkCols), 1, 8);
+  }
+  const int want = std::clamp(nsm / tiles_est, 1, kMaxItemsPerTile);  // items per tile wanted: one round
   int ipt = 0;
   for (int i = 0; i < call.n_proj; ++i) {
     const ProjArgs& a = call.proj[i];
@@ -662,7 +682,12 @@ lora_status launch_sgmv_tc(const SgmvCall& call, cudaStream_t stream) {
     t.h_in = a.h_in;
     t.h_out = a.h_out;
     t.scale = a.scale;
-    const int nch = std::clamp(ceil_div(a.h_out, kChunkCols), 1, 8);
+    int nch = std::clamp(ceil_div(a.h_out, kChunkCols), 1, 8);
+    if (base_items < want) {
+      const int share = static_cast<int>((static_cast<int64_t>(want) * a.h_out + cols - 1) / cols);
+      nch = std::max(nch, std::min(share, ceil_div(a.h_out, 128)));
+      nch = std::min(nch, kMaxItemsPerTile / call.n_proj);
+    }
     t.chunk = round_up(ceil_div(a.h_out, nch), 128);
     const int nch_real = ceil_div(a.h_out, t.chunk);
     for (int c = 0; c < nch_real; ++c) {
