@@ -66,6 +66,7 @@ constexpr uint32_t kTmemV = 0;      // v accumulator: columns [0, r)
 constexpr uint32_t kTmemAcc = 128;  // expand accumulators: [128, 256), [256, 384)
 constexpr int kChunkCols = LSG_TC_CHUNK;  // expand columns per item, about
 constexpr int kMaxItemsPerTile = 64;
+constexpr int kMaxC = 8;  // CTAs per cluster (portable limit)
 constexpr uint64_t kTcWaitNs = 2000000000ull;
 
 struct TcProj {
@@ -90,6 +91,7 @@ struct TcTail {
   int32_t n_tokens;
   int32_t max_segments;
   int32_t n_adapters;
+  int32_t csplit;  // CTAs per item (cluster size C): split-K shrink, split-N expand
 };
 
 struct TcParams {
@@ -113,18 +115,25 @@ struct TcCfg {
   static constexpr uint32_t kSwM = kSwR / 16 - 1;
 };
 
-template <int R>
+// Shared memory.  CL: the cluster variant, which adds the partial-v receive
+// buffer and takes one stage from each ring to make room for it.
+template <int R, bool CL>
 struct TcSmem {
-  alignas(1024) uint8_t sh[kShStages][TcCfg<R>::kShBytes];
-  alignas(1024) uint8_t ex[kExStages][TcCfg<R>::kExBytes];
+  static constexpr int kSh = CL ? kShStages - 1 : kShStages;
+  static constexpr int kEx = CL ? kExStages - 1 : kExStages;
+  alignas(1024) uint8_t sh[kSh][TcCfg<R>::kShBytes];
+  alignas(1024) uint8_t ex[kEx][TcCfg<R>::kExBytes];
   alignas(1024) uint8_t vop[2][TcCfg<R>::kVop];  // hi, lo
+  alignas(16) float rbuf[CL ? 128 * R : 4];      // partial v rows this CTA owns: [source rank][row][r]
   alignas(16) TcTail t;
-  alignas(8) uint64_t sh_full[kShStages];
-  uint64_t sh_empty[kShStages];
-  uint64_t ex_full[kExStages];
-  uint64_t ex_empty[kExStages];
-  uint64_t v_full;
-  uint64_t vop_ready;
+  alignas(8) uint64_t sh_full[kSh];
+  uint64_t sh_empty[kSh];
+  uint64_t ex_full[kEx];
+  uint64_t ex_empty[kEx];
+  uint64_t v_full;     // shrink MMAs of the item done (v in TMEM)
+  uint64_t v_read;     // the epilogue has read v out of TMEM
+  uint64_t vop_ready;  // the v operand pair is complete in shared memory
+  uint64_t rs_full;    // (cluster) every rank's partial of the rows this CTA owns has arrived
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint32_t tmem_base;
@@ -211,13 +220,26 @@ __device__ __forceinline__ bool warp_wait(SM& sm, uint64_t* bar, uint32_t parity
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-template <int R>
+template <int R, bool CL>
 __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_constant__ TcParams p) {
   using Cfg = TcCfg<R>;
+  using SM = TcSmem<R, CL>;
+  constexpr int kSh = SM::kSh, kEx = SM::kEx;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  auto& sm = *reinterpret_cast<TcSmem<R>*>(smem_raw);
+  auto& sm = *reinterpret_cast<SM*>(smem_raw);
   const TcTail& q = sm.t;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // cluster split: the C CTAs of a cluster take the same items; CTA `crank`
+  // runs k-blocks [kb0, kb1) of the shrink and column blocks [b0, b1) of the
+  // item's chunk, and the partial v are summed across the cluster.
+  const int C = CL ? p.t.csplit : 1;
+  const int crank = CL ? static_cast<int>(blockIdx.x) % C : 0;
+  const int group = static_cast<int>(blockIdx.x) / C, ngroups = static_cast<int>(gridDim.x) / C;
+  auto split = [&](int n, int& lo, int& hi) {
+    const int per = (n + C - 1) / C;
+    lo = min(n, crank * per);
+    hi = min(n, lo + per);
+  };
 
   {
     static_assert(sizeof(TcTail) % 4 == 0, "tail size");
@@ -235,16 +257,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
     prefetch_tmap(&p.tmYs[lane]);
   }
   if (tid == 0) {
-    for (int s = 0; s < kShStages; ++s) {
+    for (int s = 0; s < kSh; ++s) {
       mbar_init(&sm.sh_full[s], 1);
       mbar_init(&sm.sh_empty[s], 1);
     }
-    for (int s = 0; s < kExStages; ++s) {
+    for (int s = 0; s < kEx; ++s) {
       mbar_init(&sm.ex_full[s], 1);
-      mbar_init(&sm.ex_empty[s], 1);
+      mbar_init(&sm.ex_empty[s], 4);  // each epilogue warp, once its y stores have read the slot
     }
     mbar_init(&sm.v_full, 1);
-    mbar_init(&sm.vop_ready, 4);
+    mbar_init(&sm.v_read, 4);
+    mbar_init(&sm.vop_ready, CL ? 1 : 4);  // cluster: one local arrival + the gathered bytes
+    mbar_init(&sm.rs_full, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.acc_full[b], 1);
       mbar_init(&sm.acc_empty[b], 4);
@@ -256,9 +280,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // our mbarriers exist before any peer pushes into this CTA
+  if (CL) cluster_arrive_relaxed();
   const uint32_t tmem = sm.tmem_base;
   pdl_launch_dependents();
   pdl_wait();
+  if (CL) cluster_wait_acquire();
   // the operand swizzle below is computed on absolute shared addresses
   const bool aligned = (smem_u32(sm.sh) & 1023u) == 0;
   if (!aligned && tid == 0) set_err(q.err_flag, LORA_ERR_UNSUPPORTED);
@@ -269,15 +296,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
     uint32_t ph = 0;
     TcCursor cur;
     cur.init(q, lane);
-    for (int item = blockIdx.x;; item += gridDim.x) {
+    for (int item = group;; item += ngroups) {
       const int tile = item / q.ipt, is = item - tile * q.ipt;
       int tlen, a, row;
       if (!cur.find(q, lane, tile, tlen, a, row)) break;
       if (a < 0 || a >= q.n_adapters) continue;
       const int pj = q.item_proj[is];
-      const int nkb = (q.proj[pj].h_in + 63) >> 6;
+      int kb0, kb1;
+      split((q.proj[pj].h_in + 63) >> 6, kb0, kb1);
       bool ok = true;
-      for (int kb = 0; kb < nkb && ok; ++kb) {
+      for (int kb = kb0; kb < kb1 && ok; ++kb) {
         ok = warp_wait(sm, &sm.sh_empty[slot], ph ^ 1u, lane);
         if (!ok) break;
         if (lane == 0) {
@@ -286,7 +314,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
           tma_load_2d(st, &p.tmX[pj], kb * 64, row, &sm.sh_full[slot]);
           tma_load_3d(st + 16384, &p.tmA[pj], 0, kb * 64, a, &sm.sh_full[slot]);
         }
-        if (++slot == kShStages) {
+        if (++slot == kSh) {
           slot = 0;
           ph ^= 1u;
         }
@@ -299,7 +327,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
     uint32_t ph = 0;
     TcCursor cur;
     cur.init(q, lane);
-    for (int item = blockIdx.x;; item += gridDim.x) {
+    for (int item = group;; item += ngroups) {
       const int tile = item / q.ipt, is = item - tile * q.ipt;
       int tlen, a, row;
       if (!cur.find(q, lane, tile, tlen, a, row)) break;
@@ -307,9 +335,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       const int pj = q.item_proj[is], ch = q.item_chunk[is];
       const TcProj& pr = q.proj[pj];
       const int c0 = ch * pr.chunk;
-      const int nblk = (min(pr.chunk, pr.h_out - c0) + kBN - 1) / kBN;
+      int b0, b1;
+      split((min(pr.chunk, pr.h_out - c0) + kBN - 1) / kBN, b0, b1);
       bool ok = true;
-      for (int b = 0; b < nblk && ok; ++b) {
+      for (int b = b0; b < b1 && ok; ++b) {
         ok = warp_wait(sm, &sm.ex_empty[slot], ph ^ 1u, lane);
         if (!ok) break;
         if (lane == 0) {
@@ -322,7 +351,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
             tma_load_2d(st + Cfg::kExY + h * R * 128, &p.tmB[pj], c + h * 64, a * R, &sm.ex_full[slot]);
           }
         }
-        if (++slot == kExStages) {
+        if (++slot == kEx) {
           slot = 0;
           ph ^= 1u;
         }
@@ -330,24 +359,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       if (!ok || sm.abort) break;
     }
   } else if (aligned && warp == 6) {
-    // ============================== shrink MMA issuer: v = x . A
+    // ============================== shrink MMA issuer: v = x . A (this CTA's k-blocks)
     constexpr uint32_t kIdSh = umma_idesc_bf16(128, R, 0, 1);
     int sslot = 0, it = 0;
     uint32_t sph = 0;
     TcCursor cur;
     cur.init(q, lane);
-    for (int item = blockIdx.x;; item += gridDim.x) {
+    for (int item = group;; item += ngroups) {
       const int tile = item / q.ipt, is = item - tile * q.ipt;
       int tlen, a, row;
       if (!cur.find(q, lane, tile, tlen, a, row)) break;
       if (a < 0 || a >= q.n_adapters) continue;
       const TcProj& pr = q.proj[q.item_proj[is]];
-      const int nkb = (pr.h_in + 63) >> 6;
+      int kb0, kb1;
+      split((pr.h_in + 63) >> 6, kb0, kb1);
       // the epilogue has read the previous item's v out of TMEM
-      bool ok = it == 0 || warp_wait(sm, &sm.vop_ready, (it - 1) & 1, lane);
+      bool ok = it == 0 || warp_wait(sm, &sm.v_read, (it - 1) & 1, lane);
       if (!ok) break;
       tc_fence_after();
-      for (int kb = 0; kb < nkb && ok; ++kb) {
+      for (int kb = kb0; kb < kb1 && ok; ++kb) {
         ok = warp_wait(sm, &sm.sh_full[sslot], sph, lane);
         if (!ok) break;
         tc_fence_after();
@@ -357,12 +387,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
           for (int k = 0; k < 4; ++k) {
             const uint64_t ad = umma_desc(xs + k * 32, 16, 1024, 2);
             const uint64_t bd = umma_desc(as + k * 16 * R * 2, Cfg::kShA, 8 * R * 2, umma_layout(R * 2));
-            umma_bf16(tmem + kTmemV, ad, bd, kIdSh, kb > 0 || k > 0);
+            umma_bf16(tmem + kTmemV, ad, bd, kIdSh, kb > kb0 || k > 0);
           }
           umma_commit(&sm.sh_empty[sslot]);  // the stage is free once these MMAs have read it
         }
         __syncwarp();
-        if (++sslot == kShStages) {
+        if (++sslot == kSh) {
           sslot = 0;
           sph ^= 1u;
         }
@@ -380,18 +410,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
     uint32_t xph = 0;
     TcCursor cur;
     cur.init(q, lane);
-    for (int item = blockIdx.x;; item += gridDim.x) {
+    for (int item = group;; item += ngroups) {
       const int tile = item / q.ipt, is = item - tile * q.ipt;
       int tlen, a, row;
       if (!cur.find(q, lane, tile, tlen, a, row)) break;
       if (a < 0 || a >= q.n_adapters) continue;
       const TcProj& pr = q.proj[q.item_proj[is]];
-      bool ok = warp_wait(sm, &sm.vop_ready, it & 1, lane);
-      if (!ok) break;
-      tc_fence_after();
       const int c0 = q.item_chunk[is] * pr.chunk;
-      const int nblk = (min(pr.chunk, pr.h_out - c0) + kBN - 1) / kBN;
-      for (int b = 0; b < nblk && ok; ++b) {
+      int b0, b1;
+      split((min(pr.chunk, pr.h_out - c0) + kBN - 1) / kBN, b0, b1);
+      bool ok = true;
+      if (b0 < b1) {
+        // (an item without blocks here is not waited for: the epilogue waits
+        // for its operand itself, so this wait never falls two phases behind)
+        ok = warp_wait(sm, &sm.vop_ready, it & 1, lane);
+        if (!ok) break;
+        if (CL) fence_proxy_async_smem();  // operand rows written by st.async, read by the tensor core
+        tc_fence_after();
+      }
+      for (int b = b0; b < b1 && ok; ++b) {
         const int buf = ae & 1;
         ok = warp_wait(sm, &sm.acc_empty[buf], ((ae >> 1) & 1) ^ 1u, lane) &&
              warp_wait(sm, &sm.ex_full[xslot], xph, lane);
@@ -412,7 +449,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
         }
         __syncwarp();
         ++ae;
-        if (++xslot == kExStages) {
+        if (++xslot == kEx) {
           xslot = 0;
           xph ^= 1u;
         }
@@ -426,31 +463,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
     const uint32_t tq = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     int xslot = 0, ae = 0, it = 0;
     uint32_t xph = 0;
+    int pend = -1;  // (lane 0) ring slot whose y stores may still be reading it
     TcCursor cur;
     cur.init(q, lane);
-    for (int item = blockIdx.x;; item += gridDim.x) {
+    for (int item = group;; item += ngroups) {
       const int tile = item / q.ipt, is = item - tile * q.ipt;
       int tlen, a, row;
       if (!cur.find(q, lane, tile, tlen, a, row)) break;
       if (a < 0 || a >= q.n_adapters) {
-        if (tid == 0) set_err(q.err_flag, LORA_ERR_BAD_ADAPTER_ID);
+        if (tid == 0 && crank == 0) set_err(q.err_flag, LORA_ERR_BAD_ADAPTER_ID);
         continue;
       }
       const int pj = q.item_proj[is], ch = q.item_chunk[is];
       const TcProj& pr = q.proj[pj];
       const float scale = pr.scale;
+      int kb0, kb1;
+      split((pr.h_in + 63) >> 6, kb0, kb1);
       // ---- v (fp32, TMEM) -> bf16 operands hi, lo (K-major, 2r-byte swizzle)
       bool ok = warp_wait(sm, &sm.v_full, it & 1, lane);
       if (!ok) break;
       tc_fence_after();
-      {
-        uint32_t v[R];
+      uint32_t v[R];
+      if (kb0 < kb1) {
         if constexpr (R == 16) {
-          uint32_t r16[16];
-          tmem_ld16(tq + kTmemV, r16);
+          tmem_ld16(tq + kTmemV, v);
           tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = r16[i];
         } else {
 #pragma unroll
           for (int c = 0; c < R / 32; ++c) {
@@ -461,20 +498,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
             for (int i = 0; i < 32; ++i) v[c * 32 + i] = r32[i];
           }
         }
+      } else {
+#pragma unroll
+        for (int i = 0; i < R; ++i) v[i] = 0u;  // no k-blocks here: a zero partial
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.v_read);  // TMEM v may take the next item's shrink
+      // one 16-byte chunk (8 ranks) of a row as the hi / lo operand words
+      auto split_hl = [](const float (&f)[8], uint32_t (&hi)[4], uint32_t (&lo)[4]) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * e], f[2 * e + 1]);
+          const float2 hf = __bfloat1622float2(h);
+          const __nv_bfloat162 l = __floats2bfloat162_rn(f[2 * e] - hf.x, f[2 * e + 1] - hf.y);
+          hi[e] = *reinterpret_cast<const uint32_t*>(&h);
+          lo[e] = *reinterpret_cast<const uint32_t*>(&l);
+        }
+      };
+      if constexpr (!CL) {
         const uint32_t hrow = smem_u32(sm.vop[0]) + static_cast<uint32_t>(m) * (R * 2);
         const uint32_t lrow = smem_u32(sm.vop[1]) + static_cast<uint32_t>(m) * (R * 2);
 #pragma unroll
         for (int j = 0; j < R / 8; ++j) {
-          uint32_t hi[4], lo[4];
+          float f[8];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float f0 = __uint_as_float(v[j * 8 + 2 * e]), f1 = __uint_as_float(v[j * 8 + 2 * e + 1]);
-            const __nv_bfloat162 h = __floats2bfloat162_rn(f0, f1);
-            const float2 hf = __bfloat1622float2(h);
-            const __nv_bfloat162 l = __floats2bfloat162_rn(f0 - hf.x, f1 - hf.y);
-            hi[e] = *reinterpret_cast<const uint32_t*>(&h);
-            lo[e] = *reinterpret_cast<const uint32_t*>(&l);
-          }
+          for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[j * 8 + e]);
+          uint32_t hi[4], lo[4];
+          split_hl(f, hi, lo);
           const uint32_t ha = swz<Cfg::kSwM>(hrow + j * 16), la = swz<Cfg::kSwM>(lrow + j * 16);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(ha), "r"(hi[0]), "r"(hi[1]), "r"(hi[2]),
                        "r"(hi[3])
@@ -483,16 +534,71 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
                        "r"(lo[3])
                        : "memory");
         }
+        fence_proxy_async_smem();  // the tensor core reads the operands through the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.vop_ready);
+      } else {
+        // ---- reduce-scatter: row m's partial to the CTA that owns the row
+        const int rpo = 128 / C;  // rows per owner
+        const int own = m / rpo, ml = m - own * rpo;
+        if (tid == 0) {
+          mbar_arrive_expect_tx(&sm.rs_full, 128u * R * 4u);    // C ranks x rpo rows x r fp32
+          mbar_arrive_expect_tx(&sm.vop_ready, 128u * R * 4u);  // 128 rows x r x (hi + lo) bf16
+        }
+        {
+          const uint32_t dst = mapa_shared(smem_u32(&sm.rbuf[(crank * rpo + ml) * R]), own);
+          const uint32_t bar = mapa_shared(smem_u32(&sm.rs_full), own);
+#pragma unroll
+          for (int j = 0; j < R / 4; ++j)
+            st_async_v4(dst + j * 16,
+                        make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                    __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])),
+                        bar);
+        }
+        ok = warp_wait(sm, &sm.rs_full, it & 1, lane);
+        if (!ok) break;
+        // ---- sum the C partials of the owned rows (fixed order: the same v in
+        // every CTA), split into hi / lo and all-gather into every CTA's operand
+        for (int w = tid; w < rpo * (R / 8); w += kTcEpiThreads) {
+          const int lr = w / (R / 8), j = w - lr * (R / 8);
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = 0.f;
+          for (int src = 0; src < C; ++src) {
+            const float4* pp = reinterpret_cast<const float4*>(&sm.rbuf[(src * rpo + lr) * R + j * 8]);
+            const float4 u0 = pp[0], u1 = pp[1];
+            f[0] += u0.x;
+            f[1] += u0.y;
+            f[2] += u0.z;
+            f[3] += u0.w;
+            f[4] += u1.x;
+            f[5] += u1.y;
+            f[6] += u1.z;
+            f[7] += u1.w;
+          }
+          uint32_t hi[4], lo[4];
+          split_hl(f, hi, lo);
+          const uint32_t mrow = static_cast<uint32_t>(crank * rpo + lr) * (R * 2) + j * 16;
+          const uint32_t ha = swz<Cfg::kSwM>(smem_u32(sm.vop[0]) + mrow);
+          const uint32_t la = swz<Cfg::kSwM>(smem_u32(sm.vop[1]) + mrow);
+          const uint32_t bar = smem_u32(&sm.vop_ready);
+          for (int d = 0; d < C; ++d) {
+            const uint32_t rb = mapa_shared(bar, d);
+            st_async_u4(mapa_shared(ha, d), hi[0], hi[1], hi[2], hi[3], rb);
+            st_async_u4(mapa_shared(la, d), lo[0], lo[1], lo[2], lo[3], rb);
+          }
+        }
+        // the whole operand is here before the next item's expectations are
+        // registered (and the expand MMAs of this item may start)
+        ok = warp_wait(sm, &sm.vop_ready, it & 1, lane);
+        if (!ok) break;
       }
-      fence_proxy_async_smem();  // the tensor core reads the operands through the async proxy
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.vop_ready);
       // ---- expand blocks: y = bf16(y + s * acc)
       const int c0 = ch * pr.chunk;
-      const int nblk = (min(pr.chunk, pr.h_out - c0) + kBN - 1) / kBN;
+      int b0, b1;
+      split((min(pr.chunk, pr.h_out - c0) + kBN - 1) / kBN, b0, b1);
       const int full_rows = (tlen >> 5) << 5;
-      for (int b = 0; b < nblk && ok; ++b) {
+      for (int b = b0; b < b1 && ok; ++b) {
         const int buf = ae & 1;
         ok = warp_wait(sm, &sm.acc_full[buf], (ae >> 1) & 1, lane);
         if (!ok) break;
@@ -500,14 +606,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
         uint8_t* st = sm.ex[xslot];
         const int c = c0 + b * kBN;
 #pragma unroll 1
-        for (int c32 = 0; c32 < kBN / 32; ++c32) {
-          uint32_t acc[32];
-          tmem_ld32(tq + kTmemAcc + buf * kBN + c32 * 32, acc);
+        for (int c64 = 0; c64 < kBN / 64; ++c64) {
+          // both 32-column loads in flight before one wait
+          uint32_t acc[64];
+          tmem_ld32(tq + kTmemAcc + buf * kBN + c64 * 64, *reinterpret_cast<uint32_t(*)[32]>(&acc[0]));
+          tmem_ld32(tq + kTmemAcc + buf * kBN + c64 * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&acc[32]));
           tmem_ld_wait();
-          const uint32_t rbase = smem_u32(st + (c32 >> 1) * 16384) + static_cast<uint32_t>(m) * 128;
+          const uint32_t rbase = smem_u32(st + c64 * 16384) + static_cast<uint32_t>(m) * 128;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int j = (c32 & 1) * 4 + i;  // 16-byte chunk of the 64-column half
+          for (int j = 0; j < 8; ++j) {  // 16-byte chunk of the 64-column half
             const uint32_t addr = rbase + ((static_cast<uint32_t>(j) ^ (m & 7u)) << 4);
             uint32_t yw[4];
             asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
@@ -516,8 +623,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float2 yf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&yw[e]));
-              const __nv_bfloat162 o = __floats2bfloat162_rn(yf.x + scale * __uint_as_float(acc[i * 8 + 2 * e]),
-                                                             yf.y + scale * __uint_as_float(acc[i * 8 + 2 * e + 1]));
+              const __nv_bfloat162 o = __floats2bfloat162_rn(yf.x + scale * __uint_as_float(acc[j * 8 + 2 * e]),
+                                                             yf.y + scale * __uint_as_float(acc[j * 8 + 2 * e + 1]));
               yw[e] = *reinterpret_cast<const uint32_t*>(&o);
             }
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(yw[0]), "r"(yw[1]), "r"(yw[2]),
@@ -546,17 +653,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
           }
         }
         fence_proxy_async_smem();  // our y updates, visible to the tensor stores
-        named_bar_sync(2, kTcEpiThreads);
-        if (tid == 0) {
-          for (int g = 0; g < full_rows; g += 32)
+        __syncwarp();
+        if (lane == 0) {
+          // each warp stores its own 32 rows (one box per 64-column half)
+          const int g = warp * 32;
+          if (g + 32 <= full_rows)
             for (int h = 0; h < kBH; ++h)
               if (c + h * 64 < pr.h_out) tma_store_2d(&p.tmYs[pj], c + h * 64, row + g, st + h * 16384 + g * 128);
           bulk_commit();
-          bulk_wait_read0();
-          mbar_arrive(&sm.ex_empty[xslot]);  // y tile read by the stores, B tile read by the MMAs
+          // the previous block's stores have read their slot (this block's may
+          // still be reading): this warp's share of that slot goes back
+          if (pend >= 0) {
+            bulk_wait_read1();
+            mbar_arrive(&sm.ex_empty[pend]);  // y rows read by the stores, B tile read by the MMAs
+          }
+          pend = xslot;
         }
         ++ae;
-        if (++xslot == kExStages) {
+        if (++xslot == kEx) {
           xslot = 0;
           xph ^= 1u;
         }
@@ -565,8 +679,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       ++it;
     }
   }
+  if (aligned && warp < 4 && lane == 0) bulk_wait_read0();  // the last y stores have read shared memory
   tc_fence_before();
   __syncthreads();
+  if (CL) {
+    // no CTA leaves while a peer may still write into its shared memory
+    cluster_arrive_relaxed();
+    cluster_wait_acquire();
+  }
   if (warp == 6) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -577,10 +697,52 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
 
 namespace {
 
-template <int R>
-lora_status launch_tc_r(TcParams& prm, const SgmvCall& call, int tiles_bound, cudaStream_t stream) {
-  auto kern = sgmv_tc_kernel<R>;
-  const size_t smem = sizeof(TcSmem<R>);
+// Co-resident CTA groups of C CTAs (one CTA per SM) of the rank-R kernel on
+// the current device (clusters of C when CL); sets the kernel's shared-memory
+// attribute on first use.
+template <int R, bool CL>
+lora_status tc_groups(int C, int& groups) {
+  static std::mutex mu;
+  static int cache[64][kMaxC + 1];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    groups = cache[dev & 63][C];
+  }
+  if (groups > 0) return LORA_OK;
+  auto kern = sgmv_tc_kernel<R, CL>;
+  const size_t smem = sizeof(TcSmem<R, CL>);
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+      cudaSuccess)
+    return LORA_ERR_CUDA;
+  if (CL) {
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute at[1];
+    cfg.gridDim = dim3(C * 64);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = C;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&groups, kern, &cfg) != cudaSuccess) return LORA_ERR_CUDA;
+  } else if (cudaDeviceGetAttribute(&groups, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    return LORA_ERR_CUDA;
+  }
+  groups = std::max(1, groups);
+  std::lock_guard<std::mutex> lk(mu);
+  cache[dev & 63][C] = groups;
+  return LORA_OK;
+}
+
+template <int R, bool CL>
+lora_status launch_tc_rc(TcParams& prm, const SgmvCall& call, int tiles_bound, cudaStream_t stream) {
+  auto kern = sgmv_tc_kernel<R, CL>;
+  const size_t smem = sizeof(TcSmem<R, CL>);
+  const int C = prm.t.csplit;
   for (int i = 0; i < call.n_proj; ++i) {
     const ProjArgs& a = call.proj[i];
     lora_status s;
@@ -612,30 +774,120 @@ lora_status launch_tc_r(TcParams& prm, const SgmvCall& call, int tiles_bound, cu
     }
   }
 
-  static std::once_flag once[64];
-  static int nsm_cache[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
-  cudaError_t aerr = cudaSuccess;
-  std::call_once(once[dev & 63], [&] {
-    aerr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (aerr == cudaSuccess) aerr = cudaDeviceGetAttribute(&nsm_cache[dev & 63], cudaDevAttrMultiProcessorCount, dev);
-  });
-  if (aerr != cudaSuccess) return LORA_ERR_CUDA;
+  int max_groups = 0;
+  if (const lora_status st = tc_groups<R, CL>(C, max_groups); st != LORA_OK) return st;
   const int64_t items = static_cast<int64_t>(tiles_bound) * prm.t.ipt;
-  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(nsm_cache[dev & 63], items)));
+  const int groups = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(max_groups, items)));
 
   cudaLaunchConfig_t cfg{};
-  cudaLaunchAttribute at[1];
-  cfg.gridDim = dim3(grid);
+  cudaLaunchAttribute at[2];
+  int na = 0;
+  cfg.gridDim = dim3(groups * C);
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
+  if (CL) {
+    at[na].id = cudaLaunchAttributeClusterDimension;
+    at[na].val.clusterDim.x = C;
+    at[na].val.clusterDim.y = 1;
+    at[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = na;
   return cuda_status(cudaLaunchKernelEx(&cfg, kern, prm));
+}
+
+// Work plan: items are (tile, projection, column chunk) taken by groups of C
+// CTAs.  For each C in {1, 2, 4, 8} the columns are cut into enough chunks
+// for one round of items over the co-resident groups (at least one chunk of
+// about kChunkCols columns per projection; each extra chunk re-reads the
+// tile's x and the A slab for its own shrink); the plan with the fewest bytes
+// per CTA over all rounds wins (ties: the smaller C).
+template <int R>
+lora_status plan_and_launch(const SgmvCall& call, cudaStream_t stream) {
+  TcParams prm{};
+  const int n = call.seg.n_tokens;
+  const int tiles_est = std::max(1, ceil_div(n, 128));
+  int64_t cols = 0;
+  int min_kb = 1 << 30;
+  for (int i = 0; i < call.n_proj; ++i) {
+    cols += call.proj[i].h_out;
+    min_kb = std::min(min_kb, ceil_div(call.proj[i].h_in, 64));
+  }
+  struct Plan {
+    int C = 0, nch[kMaxProj] = {}, ipt = 0;
+    double cost = 0;
+  } best;
+  for (int C = 1; C <= kMaxC && C <= min_kb; C *= 2) {
+    int G = 0;
+    const lora_status st = C == 1 ? tc_groups<R, false>(1, G) : tc_groups<R, true>(C, G);
+    if (st != LORA_OK) return st;
+    const int target = std::clamp(G / tiles_est, 1, kMaxItemsPerTile);  // items per tile
+    Plan pl;
+    pl.C = C;
+    int base = 0;
+    for (int i = 0; i < call.n_proj; ++i) base += std::clamp(ceil_div(call.proj[i].h_out, kChunkCols), 1, 8);
+    bool ok = true;
+    double bytes = 0;
+    for (int i = 0; i < call.n_proj && ok; ++i) {
+      const ProjArgs& a = call.proj[i];
+      int nch = std::clamp(ceil_div(a.h_out, kChunkCols), 1, 8);
+      if (base < target) {
+        const int share = static_cast<int>((static_cast<int64_t>(target) * a.h_out + cols - 1) / cols);
+        nch = std::max(nch, std::min(share, std::max(1, a.h_out / (128 * C))));
+        nch = std::min(nch, kMaxItemsPerTile / call.n_proj);
+      }
+      const int chunk = round_up(ceil_div(a.h_out, nch), 128);
+      nch = ceil_div(a.h_out, chunk);
+      pl.nch[i] = nch;
+      pl.ipt += nch;
+      // every CTA of a cluster needs an expand block of every item
+      if (ceil_div(a.h_out - (nch - 1) * chunk, kBN) < C) ok = false;
+      bytes += static_cast<double>(nch) * (128.0 * a.h_in * 2 + a.h_in * R * 2) +
+               static_cast<double>(a.h_out) * (128 * 4 + R * 2);
+    }
+    if (!ok) continue;
+    const int64_t items = static_cast<int64_t>(tiles_est) * pl.ipt;
+    const int64_t rounds = (items + G - 1) / G;
+    pl.cost = static_cast<double>(rounds) * bytes / pl.ipt / C;
+    if (best.C == 0 || pl.cost < best.cost * 0.999) best = pl;
+  }
+  if (best.C == 0) return LORA_ERR_UNSUPPORTED;
+  int ipt = 0;
+  for (int i = 0; i < call.n_proj; ++i) {
+    const ProjArgs& a = call.proj[i];
+    TcProj& t = prm.t.proj[i];
+    t.y = a.y;
+    t.ldy = a.ldy;
+    t.h_in = a.h_in;
+    t.h_out = a.h_out;
+    t.scale = a.scale;
+    t.chunk = round_up(ceil_div(a.h_out, best.nch[i]), 128);
+    for (int c = 0; c < best.nch[i]; ++c) {
+      prm.t.item_proj[ipt] = static_cast<int8_t>(i);
+      prm.t.item_chunk[ipt] = static_cast<int8_t>(c);
+      ++ipt;
+    }
+  }
+  prm.t.csplit = best.C;
+  prm.t.perm = call.seg.perm;
+  prm.t.seg_offsets = call.seg.seg_offsets;
+  prm.t.seg_adapter = call.seg.seg_adapter;
+  prm.t.num_segments = call.seg.num_segments;
+  prm.t.err_flag = call.err_flag;
+  prm.t.n_proj = call.n_proj;
+  prm.t.ipt = ipt;
+  prm.t.n_tokens = n;
+  prm.t.max_segments = call.seg.max_segments;
+  prm.t.n_adapters = call.n_adapters;
+  // upper bound of the tiles of segments of at least kLongSeg tokens
+  const int tiles_bound = ceil_div(n, 128) + n / kLongSeg;
+  if (best.C > 1) return launch_tc_rc<R, true>(prm, call, tiles_bound, stream);
+  return launch_tc_rc<R, false>(prm, call, tiles_bound, stream);
 }
 
 }  // namespace
@@ -652,66 +904,10 @@ bool sgmv_tc_applicable(const SgmvCall& call) {
 }
 
 lora_status launch_sgmv_tc(const SgmvCall& call, cudaStream_t stream) {
-  TcParams prm{};
-  // Column chunks per projection: about kChunkCols columns each, more when
-  // the batch has fewer (tile, projection) pairs than SMs (one wide
-  // projection over a few tiles), so that every SM gets an item; each extra
-  // chunk re-reads the tile's x and the adapter's A (from L2) for its shrink.
-  static int nsm = 0;
-  if (nsm == 0) {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) !=
-                                                  cudaSuccess)
-      return LORA_ERR_CUDA;
-    nsm = v;
-  }
-  const int tiles_est = std::max(1, ceil_div(call.seg.n_tokens, 128));
-  int64_t cols = 0;
-  int base_items = 0;
-  for (int i = 0; i < call.n_proj; ++i) {
-    cols += call.proj[i].h_out;
-    base_items += std::clamp(ceil_div(call.proj[i].h_out, kChunkCols), 1, 8);
-  }
-  const int want = std::clamp(nsm / tiles_est, 1, kMaxItemsPerTile);  // items per tile wanted: one round
-  int ipt = 0;
-  for (int i = 0; i < call.n_proj; ++i) {
-    const ProjArgs& a = call.proj[i];
-    TcProj& t = prm.t.proj[i];
-    t.y = a.y;
-    t.ldy = a.ldy;
-    t.h_in = a.h_in;
-    t.h_out = a.h_out;
-    t.scale = a.scale;
-    int nch = std::clamp(ceil_div(a.h_out, kChunkCols), 1, 8);
-    if (base_items < want) {
-      const int share = static_cast<int>((static_cast<int64_t>(want) * a.h_out + cols - 1) / cols);
-      nch = std::max(nch, std::min(share, ceil_div(a.h_out, 128)));
-      nch = std::min(nch, kMaxItemsPerTile / call.n_proj);
-    }
-    t.chunk = round_up(ceil_div(a.h_out, nch), 128);
-    const int nch_real = ceil_div(a.h_out, t.chunk);
-    for (int c = 0; c < nch_real; ++c) {
-      prm.t.item_proj[ipt] = static_cast<int8_t>(i);
-      prm.t.item_chunk[ipt] = static_cast<int8_t>(c);
-      ++ipt;
-    }
-  }
-  prm.t.perm = call.seg.perm;
-  prm.t.seg_offsets = call.seg.seg_offsets;
-  prm.t.seg_adapter = call.seg.seg_adapter;
-  prm.t.num_segments = call.seg.num_segments;
-  prm.t.err_flag = call.err_flag;
-  prm.t.n_proj = call.n_proj;
-  prm.t.ipt = ipt;
-  prm.t.n_tokens = call.seg.n_tokens;
-  prm.t.max_segments = call.seg.max_segments;
-  prm.t.n_adapters = call.n_adapters;
-  // upper bound of the tiles of segments of at least kLongSeg tokens
-  const int tiles_bound = ceil_div(call.seg.n_tokens, 128) + call.seg.n_tokens / kLongSeg;
   switch (call.r) {
-    case 16: return launch_tc_r<16>(prm, call, tiles_bound, stream);
-    case 32: return launch_tc_r<32>(prm, call, tiles_bound, stream);
-    case 64: return launch_tc_r<64>(prm, call, tiles_bound, stream);
+    case 16: return plan_and_launch<16>(call, stream);
+    case 32: return plan_and_launch<32>(call, stream);
+    case 64: return plan_and_launch<64>(call, stream);
     default: return LORA_ERR_UNSUPPORTED;
   }
 }

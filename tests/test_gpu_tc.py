@@ -137,3 +137,46 @@ def test_exact_arithmetic_prefill_is_bit_exact():
     seg = lsg.lora_segment(torch.from_numpy(ids).cuda(), P)
     lsg.sgmv_fused(xt, At, Bt, seg, yt, 2.0)
     assert np.array_equal(yt.float().cpu().numpy(), y_ref)
+
+
+@pytest.mark.parametrize("r", [16, 64])
+def test_small_prefill_batches_split_over_a_cluster(r):
+    """A few 128-token tiles of one wide projection: the items are shared by
+    the CTAs of a cluster (split-K shrink, split-N expand, partial v summed
+    across the cluster), with ragged tiles and a segment below the tile size."""
+    rng = np.random.default_rng(40 + r)
+    ids = np.concatenate([np.full(300, 1, np.int32), np.full(70, 0, np.int32)])
+    n, P, h_in, h_out = ids.size, 2, 1024, 2048
+    x = _bf16(rng.standard_normal((n, h_in)))
+    A = _bf16(rng.standard_normal((P, h_in, r)) / np.sqrt(h_in))
+    B = _bf16(rng.standard_normal((P, r, h_out)) / np.sqrt(r))
+    y = _bf16(rng.standard_normal((n, h_out)))
+    y0 = y.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    seg = lsg.lora_segment(torch.from_numpy(ids).cuda(), P, err_flag=err)
+    lsg.sgmv_fused(x, A, B, seg, y, 0.5, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_within_tol(y, oracle_rows(x, A, B, ids, 0.5, y0))
+
+
+def test_many_items_take_one_cta_per_item():
+    """Ten tiles x eight projections fill the machine without a cluster."""
+    rng = np.random.default_rng(41)
+    ids = np.concatenate([np.full(l, a, np.int32) for a, l in [(0, 500), (2, 380), (1, 320)]])
+    n, P, r, h = ids.size, 3, 32, 256
+    projs, refs = [], []
+    x = _bf16(rng.standard_normal((n, h)))
+    for i in range(8):
+        A = _bf16(rng.standard_normal((P, h, r)) / np.sqrt(h))
+        B = _bf16(rng.standard_normal((P, r, 512)) / np.sqrt(r))
+        y = _bf16(rng.standard_normal((n, 512)))
+        refs.append((A, B, y.clone()))
+        projs.append((x, A, B, y, 0.25 * (i + 1)))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    seg = lsg.lora_segment(torch.from_numpy(ids).cuda(), P, err_flag=err)
+    lsg.sgmv_multi(projs, seg, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for i, ((A, B, y0), p) in enumerate(zip(refs, projs)):
+        assert_within_tol(p[3], oracle_rows(x, A, B, ids, p[4], y0), f"projection {i}")
