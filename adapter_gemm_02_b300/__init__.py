@@ -29,6 +29,8 @@ from .lora_sgmv import (  # noqa: F401
     sgmv_multi,
     sgmv_multi_host,
     sgmv_multi_host_workspace_bytes,
+    sgmv_multi_segment,
+    sgmv_fused_segment,
     sgmv_multi_slots,
     sgmv_shrink,
 )
@@ -37,5 +39,6 @@ __all__ = [
     "Segments", "load_library", "lora_segment", "lora_segment_noalloc", "lora_segment_workspace_bytes", "sgmv_shrink", "sgmv_expand",
     "sgmv_fused", "sgmv_multi", "make_projs", "SlotTable", "rank_mask", "make_slot_projs", "sgmv_multi_slots",
     "sgmv_fused_slots", "lora_slot_copy", "lora_slot_assign", "make_slot_srcs",
-    "sgmv_multi_host", "sgmv_multi_host_workspace_bytes", "make_host_projs",
+    "sgmv_multi_host", "sgmv_multi_host_workspace_bytes", "make_host_projs", "sgmv_multi_segment",
+    "sgmv_fused_segment",
 ]

@@ -59,6 +59,11 @@ struct SgmvCall {
   int n_slots;
   int r_max;
   unsigned rank_mask;
+  // One-launch step: the adapter ids of the batch; the call segments them
+  // into seg's buffers itself (inside the SGMV launch when the batch is small,
+  // else with lora_segment first, using seg_hist as its workspace).
+  const int32_t* ids;
+  int32_t* seg_hist;
 };
 
 lora_status launch_sgmv_cc(const SgmvCall& call, cudaStream_t stream);

@@ -293,14 +293,10 @@ lora_status sgmv_multi_host(const lora_proj* projs, int32_t n_proj, int32_t n_ad
   seg.num_segments = reinterpret_cast<int32_t*>(at(h.nseg));
   seg.n_tokens = n_tokens;
   seg.max_segments = std::min(n_tokens, n_adapters);
-  lora_status s = launch_segment(ids, n_tokens, n_adapters, const_cast<int32_t*>(seg.perm),
-                                 const_cast<int32_t*>(seg.seg_offsets), const_cast<int32_t*>(seg.seg_adapter),
-                                 const_cast<int32_t*>(seg.num_segments),
-                                 seg_plan(n_tokens, n_adapters).gmem ? reinterpret_cast<int32_t*>(at(h.hist))
-                                                                     : nullptr,
-                                 err_flag, st);
-  if (s != LORA_OK) return s;
+  // segmentation inside the SGMV launch when the batch is small (else its own kernel first)
   SgmvCall c{};
+  c.ids = ids;
+  c.seg_hist = seg_plan(n_tokens, n_adapters).gmem ? reinterpret_cast<int32_t*>(at(h.hist)) : nullptr;
   c.mode = kModeFused;
   for (int i = 0; i < n_proj; ++i) {
     const lora_proj& q = projs[i];
@@ -312,7 +308,7 @@ lora_status sgmv_multi_host(const lora_proj* projs, int32_t n_proj, int32_t n_ad
   c.n_adapters = n_adapters;
   c.seg = seg;
   c.err_flag = err_flag;
-  s = launch_sgmv_cc(c, st);
+  const lora_status s = launch_sgmv_cc(c, st);
   if (s != LORA_OK) return s;
   for (int i = 0; i < n_proj; ++i) {
     const lora_proj& q = projs[i];
@@ -321,6 +317,41 @@ lora_status sgmv_multi_host(const lora_proj* projs, int32_t n_proj, int32_t n_ad
       return LORA_ERR_CUDA;
   }
   return LORA_OK;
+}
+
+lora_status sgmv_multi_segment(const lora_proj* projs, int32_t n_proj, int32_t n_adapters, int32_t r,
+                               const int32_t* ids, int32_t n_tokens, int32_t* perm, int32_t* seg_offsets,
+                               int32_t* seg_adapter, int32_t* num_segments, void* workspace, size_t workspace_bytes,
+                               int32_t* err_flag, lora_stream_t stream) {
+  if (!projs || n_proj < 1 || n_tokens < 0 || n_adapters < 1) return LORA_ERR_INVALID_ARG;
+  if (n_proj > LORA_MAX_PROJ) return LORA_ERR_UNSUPPORTED;
+  if (!rank_ok(r)) return LORA_ERR_UNSUPPORTED;
+  if (!seg_offsets || !num_segments) return LORA_ERR_INVALID_ARG;
+  if (n_tokens > 0 && (!ids || !perm || !seg_adapter)) return LORA_ERR_INVALID_ARG;
+  if (!al4(seg_offsets) || !al4(num_segments) || (n_tokens > 0 && (!al4(ids) || !al4(perm) || !al4(seg_adapter))))
+    return LORA_ERR_MISALIGNED;
+  const SegPlan pl = seg_plan(n_tokens, n_adapters);
+  if (pl.gmem && (workspace == nullptr || workspace_bytes < pl.ws_bytes)) return LORA_ERR_WORKSPACE;
+  if (pl.gmem && !al4(workspace)) return LORA_ERR_MISALIGNED;
+  if (n_tokens == 0)
+    return launch_segment(ids, 0, n_adapters, perm, seg_offsets, seg_adapter, num_segments, nullptr, err_flag,
+                          reinterpret_cast<cudaStream_t>(stream));
+  SgmvCall c{};
+  c.mode = kModeFused;
+  for (int i = 0; i < n_proj; ++i) {
+    const lora_proj& q = projs[i];
+    lora_status s = check_proj(q.x, q.ldx, q.A_pool, q.B_pool, q.y, q.ldy, q.h_in, q.h_out, true, true);
+    if (s != LORA_OK) return s;
+    c.proj[i] = ProjArgs{q.x, q.A_pool, q.B_pool, q.y, q.ldx, q.ldy, q.h_in, q.h_out, q.scale};
+  }
+  c.n_proj = n_proj;
+  c.r = r;
+  c.n_adapters = n_adapters;
+  c.seg = lora_segments{perm, seg_offsets, seg_adapter, num_segments, n_tokens, std::min(n_tokens, n_adapters)};
+  c.err_flag = err_flag;
+  c.ids = ids;
+  c.seg_hist = pl.gmem ? static_cast<int32_t*>(workspace) : nullptr;
+  return launch_sgmv_cc(c, reinterpret_cast<cudaStream_t>(stream));
 }
 
 lora_status sgmv_fused(const lora_bf16* x, int64_t ldx, const lora_bf16* A_pool, const lora_bf16* B_pool,

@@ -56,6 +56,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "seg_warp.cuh"
 
 namespace lsg {
 
@@ -152,6 +153,10 @@ struct CCTail {
   int32_t map_of[kMaxProj][4];     // tensor-map pair of (projection, rank class), -1: none
   int32_t map_bw[kMaxProj];        // B box width of a map pair (columns, an odd multiple of 8)
   int32_t map_nb[kMaxProj];        // B boxes per expand stage of a map pair
+  // One-launch step: the producer warp of every CTA segments ids itself (in
+  // the shared memory past CCSmem) and CTA 0 writes the segmentation to
+  // perm / seg_offsets / seg_adapter / num_segments.  Null: segmentation given.
+  const int32_t* ids;
 };
 
 // Map pair m serves one (projection, rank r): tmA views the projection's A
@@ -360,6 +365,40 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
     uint32_t phase = 0;
     bool failed = !ring_ok;
     if (!ring_ok && lane == 0) set_err(q.err_flag, LORA_ERR_UNSUPPORTED);
+    if (q.ids != nullptr) {
+      const int n = q.n_tokens, P = q.n_adapters, ms = q.max_segments;
+      // the sort's temporaries (ids, key cursors) in ring stage 0, which no
+      // copy has touched yet; the result past CCSmem, kept for the cursor
+      int32_t* ids_s = reinterpret_cast<int32_t*>(sm.ring[0]);
+      int32_t* cnt = ids_s + n;
+      int32_t* perm_s = reinterpret_cast<int32_t*>(smem_raw + sizeof(CCSmem<RM, T>));
+      int32_t* offs_s = perm_s + n;
+      int32_t* adap_s = offs_s + ms + 1;
+      int32_t* count_s = adap_s + max(ms, 1);
+      const WarpSegOut so = warp_segment(q.ids, n, P, ids_s, cnt, perm_s, offs_s, adap_s, lane);
+      fence_proxy_async_smem();  // stage 0 is next written by the tensor copies
+      if (lane == 0) *count_s = so.S;
+      if (blockIdx.x == 0) {
+        // the caller's segmentation buffers, as lora_segment fills them
+        int32_t* perm_g = const_cast<int32_t*>(q.perm);
+        int32_t* offs_g = const_cast<int32_t*>(q.seg_offsets);
+        int32_t* adap_g = const_cast<int32_t*>(q.seg_adapter);
+        for (int i = lane; i < n; i += 32) perm_g[i] = perm_s[i];
+        for (int x = lane; x <= ms; x += 32) offs_g[x] = x <= so.S ? offs_s[x] : so.n_valid;
+        for (int x = lane; x < ms; x += 32) adap_g[x] = x < so.S ? adap_s[x] : -1;
+        if (lane == 0) *const_cast<int32_t*>(q.num_segments) = so.S;
+        if (__any_sync(0xffffffffu, so.bad) && lane == 0) set_err(q.err_flag, LORA_ERR_BAD_ADAPTER_ID);
+      }
+      __syncwarp();
+      // the cursor reads the shared-memory copy
+      if (lane == 0) {
+        sm.t.perm = perm_s;
+        sm.t.seg_offsets = offs_s;
+        sm.t.seg_adapter = adap_s;
+        sm.t.num_segments = count_s;
+      }
+      __syncwarp();
+    }
     SegCursor<T> cur;
     cur.init(q, lane);
     int last_tile = -1, a = -1, sl = -1, rk = 0, t0 = 0, tlen = 0, tok = -1, ntok = 0, tk = -1;
@@ -864,6 +903,27 @@ struct KernelInfo {
   int max_groups = 0;  // co-resident clusters (or CTA groups) on the device
 };
 
+// One-launch step limits (build-time knobs, set by measurement): the sort's
+// temporaries (n + P + 1 ints) fit ring stage 0, and its result (permutation,
+// offsets, adapters, count) adds at most kSegExtraMaxBytes of shared memory
+// per CTA, small enough to keep the CTAs per SM of the decode shapes.
+#ifndef LSG_SEG_IN_KERNEL_MAX_TOKENS
+#define LSG_SEG_IN_KERNEL_MAX_TOKENS 128
+#endif
+#ifndef LSG_SEG_IN_KERNEL_MAX_ADAPTERS
+#define LSG_SEG_IN_KERNEL_MAX_ADAPTERS 1024
+#endif
+constexpr int kSegInKernelMaxTokens = LSG_SEG_IN_KERNEL_MAX_TOKENS;
+constexpr int kSegInKernelMaxAdapters = LSG_SEG_IN_KERNEL_MAX_ADAPTERS;
+constexpr size_t kSegExtraMaxBytes = 2 * 1024;
+size_t seg_extra_bytes(int n, int P) {
+  const int ms = std::min(n, P);
+  return static_cast<size_t>(n + (ms + 1) + std::max(ms, 1) + 1) * sizeof(int32_t);
+}
+static_assert((LSG_SEG_IN_KERNEL_MAX_TOKENS * 3 + 3) * 4 <= kSegExtraMaxBytes, "segmentation result size");
+static_assert((LSG_SEG_IN_KERNEL_MAX_TOKENS + LSG_SEG_IN_KERNEL_MAX_ADAPTERS + 1) * 4 <= LSG_CC_KB_SMALL * 1024,
+              "sort temporaries in ring stage 0");
+
 // Stage shape of rank r in the ring of a kernel whose largest rank is RM.
 struct RankShape {
   int BA, WS, SWA;
@@ -881,10 +941,15 @@ RankShape rank_shape(int r) {
 // Encodes the tensor-map pairs of every (projection, rank of `ranks`) and
 // launches.  prm.t holds the projections, the tables and rmax / n_slots.
 template <int RSET, int T, int MODE>
-lora_status launch_rtm(CCParams& prm, const int* ranks, int n_ranks, int items_bound, cudaStream_t stream) {
+lora_status launch_rtm(CCParams& prm, const int* ranks, int n_ranks, int items_bound, size_t extra_smem,
+                       cudaStream_t stream) {
   constexpr int RM = set_max_rank(RSET);
   auto kern = sgmv_cc_kernel<RSET, T, MODE>;
-  const size_t smem = sizeof(CCSmem<RM, T>);
+  const size_t smem = sizeof(CCSmem<RM, T>) + extra_smem;
+  // occupancy with the segmentation result rounded up to 256 bytes (cached per size class)
+  const int var = static_cast<int>((extra_smem + 255) / 256);
+  const size_t smem_occ = sizeof(CCSmem<RM, T>) + static_cast<size_t>(var) * 256;
+  if (extra_smem > kSegExtraMaxBytes) return LORA_ERR_UNSUPPORTED;
   const int C = prm.t.csplit;
   const bool cluster = (MODE & kModeShrink) && C > 1;
   if (prm.t.n_proj * n_ranks > kMaxProj) return LORA_ERR_UNSUPPORTED;
@@ -945,24 +1010,24 @@ lora_status launch_rtm(CCParams& prm, const int* ranks, int n_ranks, int items_b
   }
 
   static std::mutex mu;
-  static KernelInfo info[64][kMaxC + 1];
+  static KernelInfo info[64][kMaxC + 1][kSegExtraMaxBytes / 256 + 1];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
   KernelInfo ki;
   {
     std::lock_guard<std::mutex> lk(mu);
-    ki = info[dev & 63][C];
+    ki = info[dev & 63][C][var];
   }
   if (ki.max_groups == 0) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(CCSmem<RM, T>) + kSegExtraMaxBytes)) != cudaSuccess)
       return LORA_ERR_CUDA;
     if (cluster) {
       cudaLaunchConfig_t cfg{};
       cudaLaunchAttribute at[1];
       cfg.gridDim = dim3(C * 1024);
       cfg.blockDim = dim3(kThreads);
-      cfg.dynamicSmemBytes = smem;
+      cfg.dynamicSmemBytes = smem_occ;
       at[0].id = cudaLaunchAttributeClusterDimension;
       at[0].val.clusterDim.x = C;
       at[0].val.clusterDim.y = 1;
@@ -974,13 +1039,13 @@ lora_status launch_rtm(CCParams& prm, const int* ranks, int n_ranks, int items_b
       ki.max_groups = std::max(1, nclusters);
     } else {
       int per_sm = 0, nsm = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess)
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem_occ) != cudaSuccess)
         return LORA_ERR_CUDA;
       if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return LORA_ERR_CUDA;
       ki.max_groups = std::max(1, per_sm * nsm / C);
     }
     std::lock_guard<std::mutex> lk(mu);
-    info[dev & 63][C] = ki;
+    info[dev & 63][C][var] = ki;
   }
   const int groups = std::max(1, std::min(items_bound, ki.max_groups));
 
@@ -1007,22 +1072,22 @@ lora_status launch_rtm(CCParams& prm, const int* ranks, int n_ranks, int items_b
 }
 
 template <int R, int T>
-lora_status dispatch_mode(Mode m, CCParams& prm, int items_bound, cudaStream_t st) {
+lora_status dispatch_mode(Mode m, CCParams& prm, int items_bound, size_t extra, cudaStream_t st) {
   const int ranks[1] = {R};
   switch (m) {
-    case kModeShrink: return launch_rtm<rank_bit(R), T, kModeShrink>(prm, ranks, 1, items_bound, st);
-    case kModeExpand: return launch_rtm<rank_bit(R), T, kModeExpand>(prm, ranks, 1, items_bound, st);
-    default: return launch_rtm<rank_bit(R), T, kModeFused>(prm, ranks, 1, items_bound, st);
+    case kModeShrink: return launch_rtm<rank_bit(R), T, kModeShrink>(prm, ranks, 1, items_bound, 0, st);
+    case kModeExpand: return launch_rtm<rank_bit(R), T, kModeExpand>(prm, ranks, 1, items_bound, 0, st);
+    default: return launch_rtm<rank_bit(R), T, kModeFused>(prm, ranks, 1, items_bound, extra, st);
   }
 }
 
 template <int T>
-lora_status dispatch_r(int r, Mode m, CCParams& prm, int items_bound, cudaStream_t st) {
+lora_status dispatch_r(int r, Mode m, CCParams& prm, int items_bound, size_t extra, cudaStream_t st) {
   switch (r) {
-    case 8: return dispatch_mode<8, T>(m, prm, items_bound, st);
-    case 16: return dispatch_mode<16, T>(m, prm, items_bound, st);
-    case 32: return dispatch_mode<32, T>(m, prm, items_bound, st);
-    case 64: return dispatch_mode<64, T>(m, prm, items_bound, st);
+    case 8: return dispatch_mode<8, T>(m, prm, items_bound, extra, st);
+    case 16: return dispatch_mode<16, T>(m, prm, items_bound, extra, st);
+    case 32: return dispatch_mode<32, T>(m, prm, items_bound, extra, st);
+    case 64: return dispatch_mode<64, T>(m, prm, items_bound, extra, st);
     default: return LORA_ERR_UNSUPPORTED;
   }
 }
@@ -1039,7 +1104,7 @@ lora_status dispatch_mixed(CCParams& base, const int* ranks, int n_ranks, int it
     for (int i = 0; i < np; ++i) prm.t.proj[i] = base.t.proj[p0 + i];
     prm.t.n_proj = np;
     const int items = static_cast<int>(std::min<int64_t>(static_cast<int64_t>(items_per_proj) * np, 1 << 30));
-    const lora_status s = launch_rtm<kAllRanks, T, kModeFused>(prm, ranks, n_ranks, items, st);
+    const lora_status s = launch_rtm<kAllRanks, T, kModeFused>(prm, ranks, n_ranks, items, 0, st);
     if (s != LORA_OK) return s;
   }
   return LORA_OK;
@@ -1095,7 +1160,24 @@ lora_status launch_sgmv_cc(const SgmvCall& call, cudaStream_t stream) {
   prm.t.rank_of = call.rank_of;
   prm.t.n_slots = slots ? call.n_slots : call.n_adapters;
   prm.t.rmax = slots ? call.r_max : call.r;
-  if (!slots && sgmv_tc_applicable(call)) {
+  const bool tc = !slots && sgmv_tc_applicable(call);
+  size_t extra = 0;
+  if (call.ids != nullptr) {
+    // segmentation first: inside this launch when it fits, else its own kernel
+    if (!slots && !tc && call.mode == kModeFused && n <= kSegInKernelMaxTokens &&
+        call.n_adapters <= kSegInKernelMaxAdapters) {
+      prm.t.ids = call.ids;
+      extra = seg_extra_bytes(n, call.n_adapters);
+    } else {
+      const lora_status s = launch_segment(call.ids, n, call.n_adapters, const_cast<int32_t*>(call.seg.perm),
+                                           const_cast<int32_t*>(call.seg.seg_offsets),
+                                           const_cast<int32_t*>(call.seg.seg_adapter),
+                                           const_cast<int32_t*>(call.seg.num_segments), call.seg_hist,
+                                           call.err_flag, stream);
+      if (s != LORA_OK) return s;
+    }
+  }
+  if (tc) {
     // long contiguous segments on tcgen05 tiles, the rest of the batch here
     const lora_status s = launch_sgmv_tc(call, stream);
     if (s != LORA_OK) return s;
@@ -1117,8 +1199,8 @@ lora_status launch_sgmv_cc(const SgmvCall& call, cudaStream_t stream) {
   }
   const int r = slots ? ranks[0] : call.r;
   const int items_bound = static_cast<int>(std::min<int64_t>(tiles * call.n_proj, 1 << 30));
-  if (T == 4) return dispatch_r<4>(r, call.mode, prm, items_bound, stream);
-  return dispatch_r<16>(r, call.mode, prm, items_bound, stream);
+  if (T == 4) return dispatch_r<4>(r, call.mode, prm, items_bound, extra, stream);
+  return dispatch_r<16>(r, call.mode, prm, items_bound, extra, stream);
 }
 
 }  // namespace lsg

@@ -27,7 +27,8 @@ STATUS = {
 # exported symbols declared in include/lora_sgmv.h
 SYMBOLS = ("lora_status_str", "lora_abi_version", "lora_segment_workspace_bytes", "lora_segment",
            "lora_segment_noalloc", "sgmv_shrink", "sgmv_expand", "sgmv_fused", "sgmv_multi", "sgmv_multi_slots",
-           "lora_slot_copy", "lora_slot_assign", "sgmv_multi_host_workspace_bytes", "sgmv_multi_host")
+           "lora_slot_copy", "lora_slot_assign", "sgmv_multi_host_workspace_bytes", "sgmv_multi_host",
+           "sgmv_multi_segment")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -87,6 +88,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sgmv_multi_host_workspace_bytes.argtypes = [ctypes.POINTER(LoraProj), i32, i32, i32]
     lib.sgmv_multi_host.restype = ctypes.c_int
     lib.sgmv_multi_host.argtypes = [ctypes.POINTER(LoraProj), i32, i32, i32, p, i32, p, sz, p, p]
+    lib.sgmv_multi_segment.restype = ctypes.c_int
+    lib.sgmv_multi_segment.argtypes = [ctypes.POINTER(LoraProj), i32, i32, i32, p, i32, p, p, p, p, p, sz, p, p]
     lib.lora_slot_copy.restype = ctypes.c_int
     lib.lora_slot_copy.argtypes = [ctypes.POINTER(LoraSlotSrc), i32, i32, i32, i32, i32, p]
     lib.lora_slot_assign.restype = ctypes.c_int
@@ -443,3 +446,36 @@ def sgmv_multi_host(projs: Sequence, ids_host: torch.Tensor, *, workspace: Optio
     _check(lib.sgmv_multi_host(arr, len(arr), P, r, _ptr(ids_host), n, _ptr(workspace), workspace.numel(),
                                _ptr(err_flag), _stream(stream)), "sgmv_multi_host")
     return workspace
+
+
+def sgmv_multi_segment(projs: Sequence, ids: torch.Tensor, n_adapters: int, *, out: Optional[Segments] = None,
+                       workspace: Optional[torch.Tensor] = None, err_flag: Optional[torch.Tensor] = None,
+                       stream=None, c_projs=None) -> Segments:
+    """lora_segment + sgmv_multi as one call (one launch for small batches):
+    returns the segmentation, written into `out` when given."""
+    lib = load_library()
+    _req(ids, "ids", torch.int32, 1)
+    if not 1 <= len(projs) <= LORA_MAX_PROJ:
+        raise ValueError("1..8 projections")
+    n = ids.shape[0]
+    seg = out if out is not None else Segments.empty(n, n_adapters, ids.device)
+    if seg.n_tokens != n or seg.n_adapters != n_adapters:
+        raise ValueError("out was sized for another batch")
+    arr = c_projs if c_projs is not None else make_projs(projs)
+    r = projs[0][1].shape[2]
+    need = lora_segment_workspace_bytes(n, n_adapters)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=ids.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.sgmv_multi_segment(arr, len(arr), int(n_adapters), int(r), _ptr(ids), n, _ptr(seg.perm),
+                                  _ptr(seg.seg_offsets), _ptr(seg.seg_adapter), _ptr(seg.num_segments),
+                                  _ptr(workspace), ws_bytes, _ptr(err_flag), _stream(stream)), "sgmv_multi_segment")
+    return seg
+
+
+def sgmv_fused_segment(x: torch.Tensor, A_pool: torch.Tensor, B_pool: torch.Tensor, ids: torch.Tensor,
+                       y: torch.Tensor, scale: float, *, out: Optional[Segments] = None,
+                       err_flag: Optional[torch.Tensor] = None, stream=None) -> Segments:
+    """One projection of sgmv_multi_segment (y updated in place)."""
+    return sgmv_multi_segment([(x, A_pool, B_pool, y, scale)], ids, A_pool.shape[0], out=out, err_flag=err_flag,
+                              stream=stream)

@@ -213,6 +213,23 @@ LORA_API lora_status sgmv_multi(const lora_proj* projs, int32_t n_proj, int32_t 
                        const lora_segments* seg, int32_t* err_flag, lora_stream_t stream);
 
 /*
+ * lora_segment followed by sgmv_multi on its result, as one call: the
+ * segmentation is written to perm / seg_offsets / seg_adapter /
+ * num_segments exactly as lora_segment writes it (for later calls of the
+ * same batch) and the projections are updated as sgmv_multi updates them.
+ * Small decode-like batches (n_tokens <= 128, n_adapters <= 1024, no
+ * segment long enough for the tensor-tile kernel) are segmented inside the
+ * SGMV launch itself, so the step is one kernel; other batches run
+ * lora_segment's kernel first (with `workspace`, sized as
+ * lora_segment_workspace_bytes says) and then the SGMV kernels.  Errors: as
+ * lora_segment and sgmv_multi.
+ */
+LORA_API lora_status sgmv_multi_segment(const lora_proj* projs, int32_t n_proj, int32_t n_adapters, int32_t r,
+                                        const int32_t* ids, int32_t n_tokens, int32_t* perm, int32_t* seg_offsets,
+                                        int32_t* seg_adapter, int32_t* num_segments, void* workspace,
+                                        size_t workspace_bytes, int32_t* err_flag, lora_stream_t stream);
+
+/*
  * The whole step from host memory: token ids, x and y0 rows in host memory
  * (pinned for an asynchronous call), adapter pools on the device.  Copies
  * ids, every distinct x and every y to the device workspace, runs

@@ -175,6 +175,25 @@ def test_host_step_validation_without_gpu(lib):
     assert lib.sgmv_multi_host(bad, 1, 8, 16, P(64), 32, P(256), need, None, None) == -1
 
 
+def test_one_call_step_validation_without_gpu(lib):
+    """sgmv_multi_segment rejects bad arguments before any CUDA call."""
+    P = ctypes.c_void_p
+    arr = (lsg.lora_sgmv.LoraProj * 1)()
+    arr[0] = lsg.lora_sgmv.LoraProj(256, 256, 256, 256, 64, 64, 64, 64, 1.0)
+    f = lib.sgmv_multi_segment
+    ok = (P(256), 32, P(256), P(256), P(256), P(256), None, 0, None, None)
+    assert f(arr, 0, 8, 16, *ok) == -1
+    assert f(arr, 9, 8, 16, *ok) == -3
+    assert f(arr, 1, 8, 12, *ok) == -3                                                        # rank
+    assert f(arr, 1, 0, 16, *ok) == -1                                                        # no adapters
+    assert f(arr, 1, 8, 16, None, 32, P(256), P(256), P(256), P(256), None, 0, None, None) == -1  # no ids
+    assert f(arr, 1, 8, 16, P(258), 32, P(256), P(256), P(256), P(256), None, 0, None, None) == -2
+    assert f(arr, 1, 60000, 16, *ok) == -5                                                    # workspace
+    bad = (lsg.lora_sgmv.LoraProj * 1)()
+    bad[0] = lsg.lora_sgmv.LoraProj(258, 256, 256, 256, 64, 64, 64, 64, 1.0)                 # x misaligned
+    assert f(bad, 1, 8, 16, *ok) == -2
+
+
 def test_product_path_fails_loudly_without_library(tmp_path):
     from adapter_gemm_02_b300 import lora_sgmv
 
