@@ -72,17 +72,23 @@ def oracle_rows(x, A, B, ids: np.ndarray, scale: float, y0, rows=None):
 
 
 class Run:
-    """One workload through lora_segment + sgmv_fused / sgmv_multi."""
+    """One workload through the call the benchmark times (sgmv_multi_segment:
+    segmentation and SGMV, one launch for small batches), or, with
+    one_call=False, through lora_segment + sgmv_fused / sgmv_multi."""
 
-    def __init__(self, wl, ids=None, copy=0):
+    def __init__(self, wl, ids=None, copy=0, one_call=True):
         self.wl = wl
         self.inp = make_inputs(wl, "cuda", copy=copy, ids=ids)
         self.ids = self.inp.ids.cpu().numpy()
         self.y0 = [y.clone() for y in self.inp.y0]
         self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
-        self.seg = lsg.lora_segment(self.inp.ids, wl.P, err_flag=self.err)
         projs = [(self.inp.x[p.x_key], self.inp.A[i], self.inp.B[i], self.inp.y0[i], wl.scale)
                  for i, p in enumerate(wl.projs)]
+        if one_call:
+            self.seg = lsg.sgmv_multi_segment(projs, self.inp.ids, wl.P, err_flag=self.err)
+            torch.cuda.synchronize()
+            return
+        self.seg = lsg.lora_segment(self.inp.ids, wl.P, err_flag=self.err)
         if len(projs) == 1:
             x, A, B, y, s = projs[0]
             lsg.sgmv_fused(x, A, B, self.seg, y, s, err_flag=self.err)

@@ -293,3 +293,16 @@ def test_host_validation_raises():
     seg = lsg.lora_segment(torch.zeros(4, dtype=torch.int32, device="cuda"), 4)
     with pytest.raises(RuntimeError, match="UNSUPPORTED"):
         lsg.sgmv_fused(x, A, B, seg, x.clone(), 1.0)
+
+
+@pytest.mark.parametrize("name", ["7b_proj_distinct", "7b_proj_zipf", "7b_layer", "70b_decode_r16"])
+def test_one_call_and_two_calls_agree_bit_for_bit(name):
+    """The benchmark's call (segmentation inside the launch for small
+    batches) and the two-call path compute the same bits at full size."""
+    wl = WORKLOADS[name]
+    a = Run(wl, one_call=True)
+    b = Run(wl, one_call=False)
+    assert int(a.err.item()) == 0 and int(b.err.item()) == 0
+    assert torch.equal(a.seg.perm, b.seg.perm) and torch.equal(a.seg.seg_offsets, b.seg.seg_offsets)
+    for i in range(len(wl.projs)):
+        assert torch.equal(a.y(i), b.y(i)), f"projection {i}"
