@@ -892,15 +892,17 @@ lora_status plan_and_launch(const SgmvCall& call, cudaStream_t stream) {
 
 }  // namespace
 
-// Launched when segments are long on average (tokens per possible segment,
-// known on the host without reading the segmentation); a long segment in a
-// batch of short ones is then left to the split-K kernel, which handles any
-// segment.
+// Launched when segments can be long: tokens per possible segment >= 64
+// (known on the host without reading the segmentation), or a batch of at
+// least kTcMinTokens tokens, where one extra launch that may find no long
+// segment costs little next to the step.  Segments it does not take are left
+// to the split-K kernel, which handles any segment.
+constexpr int kTcMinTokens = 512;
 bool sgmv_tc_applicable(const SgmvCall& call) {
   const int n = call.seg.n_tokens;
   const int max_seg = std::max(1, std::min(n, call.n_adapters));
   return call.mode == kModeFused && (call.r == 16 || call.r == 32 || call.r == 64) && n >= kLongSeg &&
-         n / max_seg >= kLongSeg;
+         (n / max_seg >= kLongSeg || n >= kTcMinTokens);
 }
 
 lora_status launch_sgmv_tc(const SgmvCall& call, cudaStream_t stream) {

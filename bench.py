@@ -70,10 +70,11 @@ def flops(wl, ids: np.ndarray) -> int:
 def dominant_kernel(wl) -> str:
     """The kernel that does the call's work: the tensor-tile kernel when
     segments are long on average (prefill), else the split-K decode kernel.
-    Mirrors the library's dispatch rule (tokens per possible segment >= 64,
-    r in {16, 32, 64}); the measured time covers the whole call either way."""
+    Mirrors the library's dispatch rule (tokens per possible segment >= 64 or
+    at least 512 tokens, r in {16, 32, 64}); the measured time covers the whole
+    call either way."""
     n = wl.n
-    if wl.r in (16, 32, 64) and n >= 64 and n // max(1, min(n, wl.P)) >= 64:
+    if wl.r in (16, 32, 64) and n >= 64 and (n // max(1, min(n, wl.P)) >= 64 or n >= 512):
         return "sgmv_tc_kernel"
     return "sgmv_cc_kernel"
 
