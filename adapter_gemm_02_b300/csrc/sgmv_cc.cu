@@ -145,6 +145,7 @@ struct CCTail {
   int32_t n_adapters;
   int32_t csplit;     // C
   int32_t skip_long;  // segments of >= kLongSeg contiguous tokens belong to the tensor-tile kernel
+  int32_t tc_ranks;   // slot arenas: ranks (rank_bit) whose long segments the tensor-tile kernel took
   const int32_t* slot_of;  // slot of each adapter (null: adapter a lives in slot a)
   const int32_t* rank_of;  // rank of each adapter (null: every adapter has the kernel's rank)
   int32_t n_slots;
@@ -256,14 +257,16 @@ struct SegCursor {
       ad = q.seg_adapter[s];
       off = o;
       len = (o >= 0 && e <= q.n_tokens && e >= o) ? e - o : 0;
-      if (q.skip_long && len >= kLongSeg) {
-        const int f = q.perm[o], b = q.perm[e - 1];
-        if (f >= 0 && b < q.n_tokens && b - f == len - 1) len = 0;  // taken by the tensor-tile kernel
-      }
       sl = ad;
       if (q.slot_of != nullptr && ad >= 0 && ad < q.n_adapters) {
         sl = q.slot_of[ad];
         rk = q.rank_of[ad];
+      }
+      if (q.skip_long && len >= kLongSeg) {
+        const int f = q.perm[o], b = q.perm[e - 1];
+        // taken by the tensor-tile kernel (with slot arenas: valid slot, a rank it ran)
+        const bool tc_took = q.slot_of == nullptr || (sl >= 0 && sl < q.n_slots && (rank_bit(rk) & q.tc_ranks));
+        if (f >= 0 && b < q.n_tokens && b - f == len - 1 && tc_took) len = 0;
       }
     }
   }
@@ -1160,7 +1163,7 @@ lora_status launch_sgmv_cc(const SgmvCall& call, cudaStream_t stream) {
   prm.t.rank_of = call.rank_of;
   prm.t.n_slots = slots ? call.n_slots : call.n_adapters;
   prm.t.rmax = slots ? call.r_max : call.r;
-  const bool tc = !slots && sgmv_tc_applicable(call);
+  const bool tc = sgmv_tc_applicable(call);
   size_t extra = 0;
   if (call.ids != nullptr) {
     // segmentation first: inside this launch when it fits, else its own kernel
@@ -1177,11 +1180,22 @@ lora_status launch_sgmv_cc(const SgmvCall& call, cudaStream_t stream) {
       if (s != LORA_OK) return s;
     }
   }
-  if (tc) {
+  if (tc && !slots) {
     // long contiguous segments on tcgen05 tiles, the rest of the batch here
     const lora_status s = launch_sgmv_tc(call, stream);
     if (s != LORA_OK) return s;
     prm.t.skip_long = 1;
+  } else if (tc && slots) {
+    // one tensor-tile launch per rank of the mask it serves (16, 32, 64)
+    for (int r = 16; r <= 64; r *= 2) {
+      if (!(call.rank_mask & static_cast<unsigned>(rank_bit(r)) ) || r > call.r_max) continue;
+      SgmvCall cr = call;
+      cr.r = r;
+      const lora_status s = launch_sgmv_tc(cr, stream);
+      if (s != LORA_OK) return s;
+      prm.t.tc_ranks |= rank_bit(r);
+    }
+    prm.t.skip_long = prm.t.tc_ranks != 0;
   }
 
   // upper bound of the number of tiles: sum over segments of ceil(len/T)

@@ -92,12 +92,20 @@ struct TcTail {
   int32_t max_segments;
   int32_t n_adapters;
   int32_t csplit;  // CTAs per item (cluster size C): split-K shrink, split-N expand
+  // Slot arenas (null slot_of: contiguous pool, slab = adapter id): a long
+  // segment is taken when its adapter's slot is valid and its rank is this
+  // kernel's rank; the slab index is then the slot.
+  const int32_t* slot_of;
+  const int32_t* rank_of;
+  int32_t n_slabs;  // slabs in the pool / slots in the arenas
+  int32_t rmax;     // B rows per slab (the contiguous pool: r)
+  int32_t rank;     // this kernel's rank
 };
 
 struct TcParams {
   CUtensorMap tmX[kMaxProj];   // x [n][h_in], box {64, 128}, 128 B swizzle
-  CUtensorMap tmA[kMaxProj];   // A_pool [P][h_in][r], box {r, 64, 1}, 2r B swizzle
-  CUtensorMap tmB[kMaxProj];   // B_pool [P*r][h_out], box {64, r}, 128 B swizzle
+  CUtensorMap tmA[kMaxProj];   // A slabs [n_slabs][h_in][r] (slab stride h_in*rmax), box {r, 64, 1}, 2r B swizzle
+  CUtensorMap tmB[kMaxProj];   // B rows [n_slabs*rmax][h_out], box {64, r}, 128 B swizzle
   CUtensorMap tmYl[kMaxProj];  // y [n][h_out], box {64, 128}, 128 B swizzle (load)
   CUtensorMap tmYs[kMaxProj];  // y, box {64, 32}, 128 B swizzle (store)
   TcTail t;
@@ -160,7 +168,19 @@ struct TcCursor {
       const int l = (o >= 0 && e <= q.n_tokens && e >= o) ? e - o : 0;
       if (l >= kLongSeg) {
         const int f = q.perm[o], b = q.perm[e - 1];
-        if (f >= 0 && b < q.n_tokens && b - f == l - 1) {
+        bool take = f >= 0 && b < q.n_tokens && b - f == l - 1;
+        if (take && q.slot_of != nullptr) {
+          // slot arenas: the slab is the slot; other ranks and invalid entries
+          // stay with the split-K kernel
+          int slab = -1;
+          if (ad >= 0 && ad < q.n_adapters) {
+            const int sl = q.slot_of[ad], rk = q.rank_of[ad];
+            if (sl >= 0 && sl < q.n_slabs && rk == q.rank) slab = sl;
+          }
+          take = slab >= 0;
+          ad = slab;
+        }
+        if (take) {
           off = o;
           len = l;
           row0 = f;
@@ -300,7 +320,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       const int tile = item / q.ipt, is = item - tile * q.ipt;
       int tlen, a, row;
       if (!cur.find(q, lane, tile, tlen, a, row)) break;
-      if (a < 0 || a >= q.n_adapters) continue;
+      if (a < 0 || a >= q.n_slabs) continue;
       const int pj = q.item_proj[is];
       int kb0, kb1;
       split((q.proj[pj].h_in + 63) >> 6, kb0, kb1);
@@ -331,7 +351,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       const int tile = item / q.ipt, is = item - tile * q.ipt;
       int tlen, a, row;
       if (!cur.find(q, lane, tile, tlen, a, row)) break;
-      if (a < 0 || a >= q.n_adapters) continue;
+      if (a < 0 || a >= q.n_slabs) continue;
       const int pj = q.item_proj[is], ch = q.item_chunk[is];
       const TcProj& pr = q.proj[pj];
       const int c0 = ch * pr.chunk;
@@ -348,7 +368,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
 #pragma unroll
           for (int h = 0; h < kBH; ++h) {
             tma_load_2d(st + h * 16384, &p.tmYl[pj], c + h * 64, row, &sm.ex_full[slot]);
-            tma_load_2d(st + Cfg::kExY + h * R * 128, &p.tmB[pj], c + h * 64, a * R, &sm.ex_full[slot]);
+            tma_load_2d(st + Cfg::kExY + h * R * 128, &p.tmB[pj], c + h * 64, a * q.rmax, &sm.ex_full[slot]);
           }
         }
         if (++slot == kEx) {
@@ -369,7 +389,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       const int tile = item / q.ipt, is = item - tile * q.ipt;
       int tlen, a, row;
       if (!cur.find(q, lane, tile, tlen, a, row)) break;
-      if (a < 0 || a >= q.n_adapters) continue;
+      if (a < 0 || a >= q.n_slabs) continue;
       const TcProj& pr = q.proj[q.item_proj[is]];
       int kb0, kb1;
       split((pr.h_in + 63) >> 6, kb0, kb1);
@@ -414,7 +434,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       const int tile = item / q.ipt, is = item - tile * q.ipt;
       int tlen, a, row;
       if (!cur.find(q, lane, tile, tlen, a, row)) break;
-      if (a < 0 || a >= q.n_adapters) continue;
+      if (a < 0 || a >= q.n_slabs) continue;
       const TcProj& pr = q.proj[q.item_proj[is]];
       const int c0 = q.item_chunk[is] * pr.chunk;
       int b0, b1;
@@ -470,7 +490,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       const int tile = item / q.ipt, is = item - tile * q.ipt;
       int tlen, a, row;
       if (!cur.find(q, lane, tile, tlen, a, row)) break;
-      if (a < 0 || a >= q.n_adapters) {
+      if (a < 0 || a >= q.n_slabs) {
         if (tid == 0 && crank == 0) set_err(q.err_flag, LORA_ERR_BAD_ADAPTER_ID);
         continue;
       }
@@ -754,13 +774,13 @@ lora_status launch_tc_rc(TcParams& prm, const SgmvCall& call, int tiles_bound, c
     }
     {
       const uint64_t dims[3] = {static_cast<uint64_t>(R), static_cast<uint64_t>(a.h_in),
-                                static_cast<uint64_t>(call.n_adapters)};
-      const uint64_t str[2] = {static_cast<uint64_t>(R) * 2, static_cast<uint64_t>(a.h_in) * R * 2};
+                                static_cast<uint64_t>(prm.t.n_slabs)};
+      const uint64_t str[2] = {static_cast<uint64_t>(R) * 2, static_cast<uint64_t>(a.h_in) * prm.t.rmax * 2};
       const uint32_t box[3] = {static_cast<uint32_t>(R), 64, 1};
       if ((s = encode_tmap_bf16(&prm.tmA[i], a.A, 3, dims, str, box, R * 2)) != LORA_OK) return s;
     }
     {
-      const uint64_t dims[2] = {static_cast<uint64_t>(a.h_out), static_cast<uint64_t>(call.n_adapters) * R};
+      const uint64_t dims[2] = {static_cast<uint64_t>(a.h_out), static_cast<uint64_t>(prm.t.n_slabs) * prm.t.rmax};
       const uint64_t str[1] = {static_cast<uint64_t>(a.h_out) * 2};
       const uint32_t box[2] = {64, static_cast<uint32_t>(R)};
       if ((s = encode_tmap_bf16(&prm.tmB[i], a.B, 2, dims, str, box, 128)) != LORA_OK) return s;
@@ -874,6 +894,11 @@ lora_status plan_and_launch(const SgmvCall& call, cudaStream_t stream) {
     }
   }
   prm.t.csplit = best.C;
+  prm.t.slot_of = call.slot_of;
+  prm.t.rank_of = call.rank_of;
+  prm.t.n_slabs = call.slot_of ? call.n_slots : call.n_adapters;
+  prm.t.rmax = call.slot_of ? call.r_max : R;
+  prm.t.rank = R;
   prm.t.perm = call.seg.perm;
   prm.t.seg_offsets = call.seg.seg_offsets;
   prm.t.seg_adapter = call.seg.seg_adapter;

@@ -281,8 +281,9 @@ typedef struct {
  * slot_of[a] of projection p's arenas.  One rank in rank_mask: one launch
  * for all projections; several ranks: each launch takes the projections
  * whose (projection, rank) pairs fit 8, i.e. 8 / popcount(rank_mask)
- * projections.  Long segments go through the split-K kernel here (the
- * tensor-tile kernel serves contiguous pools only).
+ * projections.  Prefill-like batches also run the tensor-tile kernel once
+ * per rank of the mask among 16, 32 and 64, for the long contiguous segments
+ * of that rank.
  * Host errors as sgmv_multi, plus: table NULL, a table pointer NULL or not
  * 4-byte aligned, n_slots < 1, r_max or rank_mask invalid
  * (LORA_ERR_INVALID_ARG / LORA_ERR_UNSUPPORTED), n_slots*r_max*max(h_in,

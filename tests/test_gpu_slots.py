@@ -242,3 +242,45 @@ def test_load_on_a_second_stream_while_sgmv_runs():
     assert_within_tol(c.yd, c.ref(0.5, slots=slots))
     got = c.Ad[free, : h * 32].cpu().view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(got, A_new.view(torch.int16).numpy().view(np.uint16).reshape(-1))
+
+
+@pytest.mark.parametrize("r_max,ranks", [(64, [8, 16, 32, 64]), (32, [16, 32])])
+def test_prefill_segments_in_slot_arenas(r_max, ranks):
+    """Long contiguous segments of ranks 16/32/64 go to one tensor-tile launch
+    per rank, rank-8 ones and short ones to the split-K kernel; a long segment
+    whose slot is invalid is left to the split-K kernel, which flags it."""
+    rng = np.random.default_rng(50 + r_max)
+    P, n_slots, h_in, h_out = 7, 10, 512, 640
+    lens = [300, 3, 130, 64, 200, 40, 90]
+    ids = np.concatenate([np.full(l, a, np.int32) for a, l in enumerate(lens)])
+    c = SlotCase(rng, ids.size, P, n_slots, h_in, h_out, r_max, ranks, ids=ids)
+    # every rank of the mask on some long segment
+    for a, rk in zip([0, 2, 4, 6], (ranks * 2)[:4]):
+        c.rank_of[a] = rk
+    c.A, c.B, _, _ = place_adapters(rng, c.slots, c.rank_of, n_slots, h_in, h_out, r_max)
+    c.Ad, c.Bd = _dev(c.A), _dev(c.B)
+    slots = c.slots.copy()
+    slots[4] = n_slots  # invalid slot on a 200-token segment
+    y0 = c.yd.clone()
+    _run([c], [0.5], P, table=c.table(slots=slots), expect_err=-4)
+    rows = torch.from_numpy(c.ids == 4).cuda()
+    assert torch.equal(c.yd[rows], y0[rows])
+    assert_within_tol(c.yd, c.ref(0.5, slots=slots))
+
+
+def test_prefill_one_rank_slot_table_matches_contiguous_pool():
+    """A one-rank slot table over a permuted pool gives the same bits as the
+    contiguous pool through the tensor-tile kernel."""
+    rng = np.random.default_rng(60)
+    P, n_slots, h_in, h_out, r = 4, 6, 1024, 768, 64
+    ids = np.concatenate([np.full(l, a, np.int32) for a, l in enumerate([700, 260, 128, 513])])
+    c = SlotCase(rng, ids.size, P, n_slots, h_in, h_out, r, [r], ids=ids)
+    y_ref = c.yd.clone()
+    _run([c], [1.0], P)
+    # the same adapters as a contiguous pool
+    A = torch.stack([c.Ad[int(c.slots[a])].view(h_in, r) for a in range(P)])
+    B = torch.stack([c.Bd[int(c.slots[a])].view(r, h_out) for a in range(P)])
+    seg = lsg.lora_segment(torch.from_numpy(ids).cuda(), P)
+    lsg.sgmv_fused(c.xd, A.contiguous(), B.contiguous(), seg, y_ref, 1.0)
+    torch.cuda.synchronize()
+    assert torch.equal(c.yd, y_ref)
