@@ -216,7 +216,9 @@ def barrier(world: int) -> None:
 
 def time_oracle(wl, inp_cpu, seconds: float, threads: int, max_calls: int = 10 ** 9):
     """Seconds per full call of the CPU oracle (segmentation + per-token
-    SGMV over every projection) on this host; returns (s_per_call, calls)."""
+    SGMV over every projection) on this host, over max_calls calls or until
+    `seconds` have passed (whichever comes first; at least one call);
+    returns (s_per_call, calls)."""
     import oracle  # test infrastructure: the CPU baseline leg only
 
     ids = inp_cpu.ids.numpy()
@@ -245,9 +247,10 @@ def run_reference(args) -> None:
     wl = WORKLOADS[args.workload]
     threads = os.cpu_count() or 1
     inp = make_inputs(wl, "cpu")
-    for _ in range(args.warmup):
-        time_oracle(wl, inp, 0.0, threads, max_calls=1)
-    per, calls = time_oracle(wl, inp, 0.0, threads, max_calls=max(1, args.steps))
+    # warm-up calls, then K timed calls (fewer if they pass the time cap: the
+    # oracle of a prefill batch takes seconds per call)
+    time_oracle(wl, inp, args.ref_seconds / 4, threads, max_calls=args.warmup)
+    per, calls = time_oracle(wl, inp, args.ref_seconds, threads, max_calls=max(1, args.steps))
     us = per * 1e6
     out = {
         "impl": "reference", "metric": METRIC, "value": round(us, 3), "unit": "us", "n_gpus": args.gpus,
@@ -743,6 +746,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-mixed", action="store_true")
     ap.add_argument("--no-slots", action="store_true", help="skip the slot-arena / mixed-rank measurement")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="time cap of the reference arm's timed calls")
     ap.add_argument("--batch-curve", action="store_true",
                     help="add step latency against batch size (decode and prefill, identical vs mixed adapters)")
     args = ap.parse_args(argv)
