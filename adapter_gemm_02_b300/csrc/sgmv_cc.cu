@@ -74,6 +74,9 @@ namespace lsg {
 #ifndef LSG_CC_STAGES_BIG
 #define LSG_CC_STAGES_BIG 3
 #endif
+#ifndef LSG_CC_STAGES_R8
+#define LSG_CC_STAGES_R8 LSG_CC_STAGES_SMALL
+#endif
 #ifndef LSG_CC_KB_BIG
 #define LSG_CC_KB_BIG 28
 #endif
@@ -173,7 +176,7 @@ struct CCParams {
 // Rank R's stage contents in a ring shaped for rank RM >= R.
 template <int R, int T, int RM = R>
 struct CCCfg {
-  static constexpr int kStages = RM >= 64 ? LSG_CC_STAGES_BIG : LSG_CC_STAGES_SMALL;
+  static constexpr int kStages = RM >= 64 ? LSG_CC_STAGES_BIG : RM == 8 ? LSG_CC_STAGES_R8 : LSG_CC_STAGES_SMALL;
   static constexpr int kStageBytes = (RM >= 64 ? LSG_CC_KB_BIG : LSG_CC_KB_SMALL) * 1024;
   // shrink: A rows per stage (A part + x part fit a stage), whole k-steps of
   // 16, made of NBA TMA boxes of BA rows (a box extent is at most 256)

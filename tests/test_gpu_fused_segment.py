@@ -41,6 +41,8 @@ CASES = {
     "over_limit_tokens": (np.random.default_rng(2).integers(0, 40, 1500).astype(np.int32), 40, 128, 128, 16),
     "over_limit_pool": (np.random.default_rng(3).integers(0, 5000, 64).astype(np.int32), 5000, 128, 128, 8),
     "prefill_long_segments": (np.repeat(np.array([1, 0], np.int32), [300, 200]), 2, 512, 640, 32),
+    "all_invalid": (np.array([3, 3, -1, 7, 3], np.int32), 3, 256, 256, 16),
+    "one_adapter_pool": (np.zeros(37, np.int32), 1, 512, 256, 32),
 }
 
 
@@ -86,3 +88,15 @@ def test_multi_projection_one_call():
     check_segments(seg, ids, P)
     for i, ((x, A, B, y, s), y0) in enumerate(zip(projs, refs)):
         assert_within_tol(y, oracle_rows(x, A, B, ids, s, y0), f"projection {i}")
+
+
+def test_zero_tokens_writes_an_empty_segmentation():
+    rng = np.random.default_rng(3)
+    x, A, B, y = _problem(rng, np.zeros(1, np.int32), 4, 256, 256, 16)
+    ids = torch.zeros(0, dtype=torch.int32, device="cuda")
+    seg = lsg.Segments.empty(0, 4, "cuda")
+    seg.num_segments.fill_(-1)
+    lsg.sgmv_multi_segment([(x[:0], A, B, y[:0], 1.0)], ids, 4, out=seg)
+    torch.cuda.synchronize()
+    assert int(seg.num_segments.item()) == 0
+    assert int(seg.seg_offsets[0].item()) == 0
