@@ -57,7 +57,7 @@ constexpr int kTcEpiThreads = 128;
 #define LSG_TC_BN 64
 #endif
 constexpr int kShStages = LSG_TC_SH_STAGES;
-constexpr int kBN = LSG_TC_BN;       // expand block columns (MMA N): 64 or 128
+constexpr int kBN = LSG_TC_BN;       // expand block columns (MMA N): 64 (128: one-CTA rings only)
 constexpr int kBH = kBN / 64;        // 64-column halves per block
 static_assert(kBN == 64 || kBN == 128, "expand block");
 constexpr int kExStages = kBN == 64 ? 4 : 2;
@@ -129,6 +129,9 @@ template <int R, bool CL>
 struct TcSmem {
   static constexpr int kSh = CL ? kShStages - 1 : kShStages;
   static constexpr int kEx = CL ? kExStages - 1 : kExStages;
+  // the epilogue hands a slot back one block late, so each ring needs two
+  // stages (an expand block of 128 columns leaves the cluster variant one)
+  static_assert(kSh >= 2 && kEx >= 2, "ring depth");
   alignas(1024) uint8_t sh[kSh][TcCfg<R>::kShBytes];
   alignas(1024) uint8_t ex[kEx][TcCfg<R>::kExBytes];
   alignas(1024) uint8_t vop[2][TcCfg<R>::kVop];  // hi, lo
