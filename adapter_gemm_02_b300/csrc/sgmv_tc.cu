@@ -57,7 +57,7 @@ constexpr int kTcEpiThreads = 128;
 #define LSG_TC_BN 64
 #endif
 constexpr int kShStages = LSG_TC_SH_STAGES;
-constexpr int kBN = LSG_TC_BN;       // expand block columns (MMA N): 64 (128: one-CTA rings only)
+constexpr int kBN = LSG_TC_BN;       // expand block columns (MMA N): 64 (128 leaves the cluster ring one stage: rejected below)
 constexpr int kBH = kBN / 64;        // 64-column halves per block
 static_assert(kBN == 64 || kBN == 128, "expand block");
 constexpr int kExStages = kBN == 64 ? 4 : 2;
