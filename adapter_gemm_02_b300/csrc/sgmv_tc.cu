@@ -45,8 +45,8 @@
 
 namespace lsg {
 
-constexpr int kTcThreads = 256;
-constexpr int kTcEpiThreads = 128;
+constexpr int kTcThreads = 384;
+constexpr int kTcEpiThreads = 128;  // one epilogue group: 4 warps, one per TMEM lane quarter
 #ifndef LSG_TC_SH_STAGES
 #define LSG_TC_SH_STAGES 4
 #endif
@@ -59,7 +59,7 @@ constexpr int kTcEpiThreads = 128;
 constexpr int kShStages = LSG_TC_SH_STAGES;
 constexpr int kBN = LSG_TC_BN;       // expand block columns (MMA N): 64 (128 leaves the cluster ring one stage: rejected below)
 constexpr int kBH = kBN / 64;        // 64-column halves per block
-static_assert(kBN == 64 || kBN == 128, "expand block");
+static_assert(kBN == 64, "expand block: two epilogue groups of 32 columns");
 constexpr int kExStages = kBN == 64 ? 4 : 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemV = 0;      // v accumulator: columns [0, r)
@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
     mbar_init(&sm.rs_full, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.acc_full[b], 1);
-      mbar_init(&sm.acc_empty[b], 4);
+      mbar_init(&sm.acc_empty[b], 8);  // both epilogue groups' warps
     }
     sm.abort = 0;
     fence_mbar_init();
@@ -480,10 +480,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       if (!ok || sm.abort) break;
       ++it;
     }
-  } else if (aligned && warp < 4) {
-    // ============================== epilogue (row m = TMEM lane m)
-    const int m = tid;
-    const uint32_t tq = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  } else if (aligned && (warp < 4 || warp >= 8)) {
+    // ============================== epilogue (row m = TMEM lane m): two groups
+    // of four warps (0-3, 8-11); group eg turns v into the operand (group 0)
+    // and updates columns [32 eg, 32 eg + 32) of every 64-column block
+    const int eg = warp >> 3, wq = warp & 3;
+    const int m = wq * 32 + lane;
+    const uint32_t tq = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     int xslot = 0, ae = 0, it = 0;
     uint32_t xph = 0;
     int pend = -1;  // (lane 0) ring slot whose y stores may still be reading it
@@ -502,8 +505,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       const float scale = pr.scale;
       int kb0, kb1;
       split((pr.h_in + 63) >> 6, kb0, kb1);
+      bool ok = true;
+      if (eg == 0) {
       // ---- v (fp32, TMEM) -> bf16 operands hi, lo (K-major, 2r-byte swizzle)
-      bool ok = warp_wait(sm, &sm.v_full, it & 1, lane);
+      ok = warp_wait(sm, &sm.v_full, it & 1, lane);
       if (!ok) break;
       tc_fence_after();
       uint32_t v[R];
@@ -616,6 +621,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
         ok = warp_wait(sm, &sm.vop_ready, it & 1, lane);
         if (!ok) break;
       }
+      }  // eg == 0
       // ---- expand blocks: y = bf16(y + s * acc)
       const int c0 = ch * pr.chunk;
       int b0, b1;
@@ -628,16 +634,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
         tc_fence_after();
         uint8_t* st = sm.ex[xslot];
         const int c = c0 + b * kBN;
-#pragma unroll 1
-        for (int c64 = 0; c64 < kBN / 64; ++c64) {
-          // both 32-column loads in flight before one wait
-          uint32_t acc[64];
-          tmem_ld32(tq + kTmemAcc + buf * kBN + c64 * 64, *reinterpret_cast<uint32_t(*)[32]>(&acc[0]));
-          tmem_ld32(tq + kTmemAcc + buf * kBN + c64 * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&acc[32]));
+        {
+          // this group's 32 columns of the block
+          uint32_t acc[32];
+          tmem_ld32(tq + kTmemAcc + buf * kBN + eg * 32, acc);
           tmem_ld_wait();
-          const uint32_t rbase = smem_u32(st + c64 * 16384) + static_cast<uint32_t>(m) * 128;
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.acc_empty[buf]);  // accumulator in registers: TMEM buffer free
+          const uint32_t rbase = smem_u32(st) + static_cast<uint32_t>(m) * 128;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {  // 16-byte chunk of the 64-column half
+          for (int i = 0; i < 4; ++i) {
+            const int j = eg * 4 + i;  // 16-byte chunk of the 64-column block
             const uint32_t addr = rbase + ((static_cast<uint32_t>(j) ^ (m & 7u)) << 4);
             uint32_t yw[4];
             asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
@@ -646,8 +654,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float2 yf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&yw[e]));
-              const __nv_bfloat162 o = __floats2bfloat162_rn(yf.x + scale * __uint_as_float(acc[j * 8 + 2 * e]),
-                                                             yf.y + scale * __uint_as_float(acc[j * 8 + 2 * e + 1]));
+              const __nv_bfloat162 o = __floats2bfloat162_rn(yf.x + scale * __uint_as_float(acc[i * 8 + 2 * e]),
+                                                             yf.y + scale * __uint_as_float(acc[i * 8 + 2 * e + 1]));
               yw[e] = *reinterpret_cast<const uint32_t*>(&o);
             }
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(yw[0]), "r"(yw[1]), "r"(yw[2]),
@@ -655,18 +663,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
                          : "memory");
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.acc_empty[buf]);  // TMEM buffer free for the next block
         // rows past the last whole group of 32: written directly (16-byte stores)
         if (m >= full_rows && m < tlen) {
           uint16_t* yrow = pr.y + static_cast<int64_t>(row + m) * pr.ldy;
 #pragma unroll 1
-          for (int j = 0; j < kBN / 8; ++j) {
+          for (int j = eg * 4; j < eg * 4 + 4; ++j) {
             const int col = c + j * 8;
             if (col < pr.h_out) {
-              const uint32_t addr = smem_u32(st + (j >> 3) * 16384) + static_cast<uint32_t>(m) * 128 +
-                                    ((static_cast<uint32_t>(j & 7) ^ (m & 7u)) << 4);
+              const uint32_t addr =
+                  smem_u32(st) + static_cast<uint32_t>(m) * 128 + ((static_cast<uint32_t>(j) ^ (m & 7u)) << 4);
               uint4 w;
               asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                            : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
@@ -676,16 +681,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
           }
         }
         fence_proxy_async_smem();  // our y updates, visible to the tensor stores
-        __syncwarp();
-        if (lane == 0) {
-          // each warp stores its own 32 rows (one box per 64-column half)
-          const int g = warp * 32;
-          if (g + 32 <= full_rows)
-            for (int h = 0; h < kBH; ++h)
-              if (c + h * 64 < pr.h_out) tma_store_2d(&p.tmYs[pj], c + h * 64, row + g, st + h * 16384 + g * 128);
+        named_bar_sync(3 + wq, 64);  // the two warps of this lane quarter are done with the block
+        if (eg == 0 && lane == 0) {
+          // each lane quarter stores its own 32 rows (one 64-column box)
+          const int g = wq * 32;
+          if (g + 32 <= full_rows && c < pr.h_out) tma_store_2d(&p.tmYs[pj], c, row + g, st + g * 128);
           bulk_commit();
           // the previous block's stores have read their slot (this block's may
-          // still be reading): this warp's share of that slot goes back
+          // still be reading): this quarter's share of that slot goes back
           if (pend >= 0) {
             bulk_wait_read1();
             mbar_arrive(&sm.ex_empty[pend]);  // y rows read by the stores, B tile read by the MMAs
