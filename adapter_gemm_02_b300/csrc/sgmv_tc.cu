@@ -10,30 +10,35 @@
 //   shrink  v[128][r]   = x[128][h_in] . A[h_in][r]            (K = h_in)
 //   expand  y[128][c]  += s * v[128][r] . B[r][c], c in chunk  (K = r)
 //
-// One CTA per SM, persistent, seven warps with fixed roles:
-//   warps 0-3  epilogue: TMEM lane quarter w; turn v (fp32, TMEM) into the
-//              expand's bf16 operand pair v = hi + lo in shared memory, then
-//              add s * acc to the y tile in shared memory and store it
+// One CTA per SM, persistent, twelve warps with fixed roles:
+//   warps 0-3, 8-11  epilogue, two groups of four (warp w: TMEM lane quarter
+//              w % 4).  Group 0 turns v (fp32, TMEM) into the expand's bf16
+//              operand pair v = hi + lo in shared memory; both groups then add
+//              s * acc to their 32 columns of each 64-column y block in shared
+//              memory, and group 0 stores the block (one TMA box per quarter)
 //   warp 4     shrink producer: TMA x tiles [128][64] (K-major, 128 B swizzle)
 //              and A tiles [64][r] (MN-major, 2r-byte swizzle), 4 stages
-//   warp 5     expand producer: TMA y tiles [128][128] (two 64-column 128 B
-//              swizzled halves) and B tiles [r][128] (MN-major), 2 stages
+//   warp 5     expand producer: TMA y tiles [128][64] (128 B swizzle) and B
+//              tiles [r][64] (MN-major), 4 stages
 //   warp 6     TMEM allocation; one thread issues the shrink MMAs
 //   warp 7     one thread issues the expand MMAs
 //              (tcgen05.mma kind::f16, fp32 accumulators in TMEM: v in columns
-//              0..r-1, two 128-column expand buffers, so the epilogue of one
+//              0..r-1, two 64-column expand buffers, so the epilogue of one
 //              block overlaps the MMAs of the next).  With one issuer per
 //              stream the shrink of item i+1 streams x and A while item i is
-//              expanded; the epilogue orders the two: it reads v(i) before it
-//              releases the shrink of item i+1 (vop_ready), and it rewrites the
-//              v operand only after the last expand MMAs of item i completed.
+//              expanded; the epilogue orders the two: it reads v(i) out of
+//              TMEM before the shrink of item i+1 may overwrite it (v_read),
+//              and it rewrites the v operand only after the last expand MMAs
+//              of item i completed.
 //
 // Work item = (128-token tile of a segment, projection, column chunk of
-// h_out), round robin over the CTAs.  Each item recomputes its tile's shrink (x is re-read from L2 by
-// the items of the same tile), which keeps items of similar size for load
-// balance.  Only segments of at least kLongSeg tokens whose rows are
-// contiguous in x / y (true for prefill requests) are taken here; the
-// decode kernel handles the rest of the batch (it skips these segments).
+// h_out), round robin over the CTAs (or over clusters of C CTAs that share an
+// item: split-K shrink, split-N expand, partial v summed through distributed
+// shared memory).  Each item recomputes its tile's shrink (x is re-read from
+// L2 by the items of the same tile), which keeps items of similar size for
+// load balance.  Only segments of at least kLongSeg tokens whose rows are
+// contiguous in x / y (true for prefill requests) are taken here; the decode
+// kernel handles the rest of the batch (it skips these segments).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
