@@ -65,7 +65,10 @@ constexpr int kShStages = LSG_TC_SH_STAGES;
 constexpr int kBN = LSG_TC_BN;       // expand block columns (MMA N): 64 (128 leaves the cluster ring one stage: rejected below)
 constexpr int kBH = kBN / 64;        // 64-column halves per block
 static_assert(kBN == 64, "expand block: two epilogue groups of 32 columns");
-constexpr int kExStages = kBN == 64 ? 4 : 2;
+#ifndef LSG_TC_EX_STAGES
+#define LSG_TC_EX_STAGES 4
+#endif
+constexpr int kExStages = LSG_TC_EX_STAGES;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemV = 0;      // v accumulator: columns [0, r)
 constexpr uint32_t kTmemAcc = 128;  // expand accumulators: [128, 256), [256, 384)
