@@ -247,9 +247,11 @@ def run_reference(args) -> None:
     wl = WORKLOADS[args.workload]
     threads = os.cpu_count() or 1
     inp = make_inputs(wl, "cpu")
-    # warm-up calls, then K timed calls (fewer if they pass the time cap: the
-    # oracle of a prefill batch takes seconds per call)
+    # warm-up: W calls and at least 2 s of calls (the OpenMP pool and the
+    # caches reach steady state), then K timed calls (fewer if they pass the
+    # time cap: the oracle of a prefill batch takes seconds per call)
     time_oracle(wl, inp, args.ref_seconds / 4, threads, max_calls=args.warmup)
+    time_oracle(wl, inp, min(2.0, args.ref_seconds / 4), threads)
     per, calls = time_oracle(wl, inp, args.ref_seconds, threads, max_calls=max(1, args.steps))
     us = per * 1e6
     out = {
