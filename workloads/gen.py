@@ -141,6 +141,11 @@ def _build_workloads() -> Dict[str, Workload]:
                                  1.0, lambda: prefill_ids(n_requests=2),
                                  "Llama2-13B prefill, 7 projections, r=64, 2 requests of U[128,2048] tokens, "
                                  "2 adapters of pool 32, sorted by adapter (a smaller case of the 8-request batch)")
+    h13, _ = LLAMA_DIMS["13b"]
+    w["13b_proj_2048"] = _mk("13b_proj_2048", [Proj("proj", h13, h13, "x")], 64, 32, 2048, 1.0,
+                             lambda: same_ids(2048, 32),
+                             "Llama2-13B prefill projection 5120->5120, r=64, one request of 2048 tokens, pool 32 "
+                             "(a few 128-token tiles: the cluster-split case)")
     for r in (8, 16, 32, 64):
         nm = f"70b_decode_r{r}"
         w[nm] = _mk(nm, llama_projs("70b"), r, 1000, 256, 1.0, lambda: zipf_ids(256, 1000, 0.8),
