@@ -242,6 +242,15 @@ def _mask(ranks):
     return m
 
 
+def pin_golden_slots(mutant=0):
+    """Hand-worked slot-arena example with its derivation (tests/golden)."""
+    g = _golden("slots_handworked.json")
+    y = oracle.sgmv_slots_ref(_b(g["x"]), _b(g["A_arena"]), _b(g["B_arena"]), g["slot_of"], g["rank_of"],
+                              g["r_max"], _mask(g["ranks_allowed"]), np.array(g["ids"], np.int32), g["s"],
+                              _b(g["y0"]), mutant=mutant)
+    assert np.array_equal(y, np.array(g["y"], np.float32)), y
+
+
 def pin_slots_dense_bruteforce(mutant=0):
     """Mixed ranks in shuffled slots against y0 + s * x . (A_a . B_a) in fp64
     (the other association), within the fp32 forward error bound."""
@@ -326,6 +335,7 @@ ALL_PINS = [
     pin_permutation,
     pin_linear_in_s,
     pin_rank1_closed_form,
+    pin_golden_slots,
     pin_slots_dense_bruteforce,
     pin_slots_zero_padding,
     pin_slots_invalid_entries,
