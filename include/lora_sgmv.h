@@ -69,7 +69,7 @@ typedef enum {
   LORA_ERR_INVALID_ARG = -1,    /* null pointer, negative size, ld < width ... */
   LORA_ERR_MISALIGNED = -2,     /* pointer or leading dimension not 16-byte aligned */
   LORA_ERR_UNSUPPORTED = -3,    /* rank or width outside the supported set */
-  LORA_ERR_BAD_ADAPTER_ID = -4, /* device: adapter id or permutation entry out of range */
+  LORA_ERR_BAD_ADAPTER_ID = -4, /* device: adapter id, permutation entry, slot or rank out of range */
   LORA_ERR_WORKSPACE = -5,      /* workspace missing or smaller than required */
   LORA_ERR_CUDA = -6,           /* a CUDA runtime call or launch failed */
   LORA_ERR_TIMEOUT = -7         /* device: a bounded wait inside a kernel ran out */
