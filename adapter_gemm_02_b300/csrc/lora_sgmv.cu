@@ -59,7 +59,8 @@ const char* lora_status_str(int s) {
     case LORA_ERR_INVALID_ARG: return "LORA_ERR_INVALID_ARG: invalid argument";
     case LORA_ERR_MISALIGNED: return "LORA_ERR_MISALIGNED: pointer or leading dimension not 16-byte aligned";
     case LORA_ERR_UNSUPPORTED: return "LORA_ERR_UNSUPPORTED: rank or width not supported";
-    case LORA_ERR_BAD_ADAPTER_ID: return "LORA_ERR_BAD_ADAPTER_ID: adapter id or permutation entry out of range";
+    case LORA_ERR_BAD_ADAPTER_ID:
+      return "LORA_ERR_BAD_ADAPTER_ID: adapter id, permutation entry, slot or rank out of range";
     case LORA_ERR_WORKSPACE: return "LORA_ERR_WORKSPACE: workspace missing or too small";
     case LORA_ERR_CUDA: return "LORA_ERR_CUDA: CUDA runtime error";
     case LORA_ERR_TIMEOUT: return "LORA_ERR_TIMEOUT: a bounded wait in a kernel ran out";
