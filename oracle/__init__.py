@@ -64,6 +64,8 @@ def load(mutant: int = 0) -> ctypes.CDLL:
     lib.oracle_sgmv_slots_f32.restype = i32
     lib.oracle_sgmv_slots_f32.argtypes = [p, i64, p, p, p, p, i32, i32, ctypes.c_uint32, p, i32, i32, i32, i32,
                                           ctypes.c_float, p, i64, p, i32]
+    lib.oracle_gemm_lora_f32.restype = i32
+    lib.oracle_gemm_lora_f32.argtypes = [p, i64, p, p, p, p, i32, i32, i32, i32, i32, ctypes.c_float, p, i32]
     lib.oracle_mutant.restype = i32
     assert lib.oracle_mutant() == mutant
     _loaded[mutant] = lib
@@ -148,3 +150,21 @@ def sgmv_slots_ref(x, A_arena, B_arena, slot_of, rank_of, r_max: int, rank_mask:
                                              _ptr(rank_of), n_slots, int(r_max), int(rank_mask), _ptr(ids), n, P,
                                              h_in, h_out, float(s), _ptr(yb), yb.shape[1], _ptr(y), int(threads))
     return (y, int(bad)) if return_invalid else y
+
+
+def gemm_lora_ref(x, W, A_pool, B_pool, ids, s: float, *, threads: int = 1, mutant: int = 0):
+    """y = x.W + s*((x.A[a_i]).B[a_i]) per token, unrounded fp32 (see the C file).
+
+    x: [n, >=h_in] bf16; W: [h_in, h_out]; A_pool: [P, h_in, r];
+    B_pool: [P, r, h_out]; ids: int32 [n].  Returns y [n, h_out]."""
+    xb, Wb, Ab, Bb = bits(x), bits(W), bits(A_pool), bits(B_pool)
+    ids = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    P, h_in, r = Ab.shape
+    h_in2, h_out = Wb.shape
+    assert h_in2 == h_in and Bb.shape == (P, r, h_out)
+    n = int(ids.size)
+    assert xb.ndim == 2 and xb.shape[0] == n and xb.shape[1] >= h_in
+    y = np.empty((n, h_out), np.float32)
+    load(mutant).oracle_gemm_lora_f32(_ptr(xb), xb.shape[1], _ptr(Wb), _ptr(Ab), _ptr(Bb), _ptr(ids), n, P, h_in,
+                                      h_out, r, float(s), _ptr(y), int(threads))
+    return y

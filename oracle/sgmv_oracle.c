@@ -291,3 +291,62 @@ int oracle_sgmv_slots_f32(const uint16_t* x, int64_t ldx, const uint16_t* A_aren
   }
   return n_invalid;
 }
+
+/*
+ * The backbone projection with its LoRA delta, as a GEMM epilogue would
+ * produce it (Punica: Multi-Tenant LoRA Serving, "Summary": the backbone runs
+ * as one GEMM and the per-adapter low-rank additions are computed beside it):
+ *
+ *   y[i,:] = x[i,:] . W + s * ((x[i,:] . A[a_i]) . B[a_i])
+ *
+ * W is [h_in][h_out] row-major.  Per token: base[c] = sum_j x[j]*W[j][c]
+ * (j ascending, fp32), the delta d[c] with the same steps as
+ * oracle_sgmv_f32, y[c] = base[c] + s*d[c] (unrounded fp32).  A token whose
+ * id is outside [0, P) gets y = base.  Returns the number of such tokens.
+ */
+int oracle_gemm_lora_f32(const uint16_t* x, int64_t ldx, const uint16_t* W, const uint16_t* A_pool,
+                         const uint16_t* B_pool, const int32_t* ids, int32_t n, int32_t P, int32_t h_in,
+                         int32_t h_out, int32_t r, float s, float* y, int32_t n_threads) {
+  int32_t n_invalid = 0;
+  if (n_threads < 1) n_threads = 1;
+#pragma omp parallel num_threads(n_threads) reduction(+ : n_invalid)
+  {
+    float* v = (float*)malloc(sizeof(float) * (size_t)(r > 0 ? r : 1));
+#pragma omp for schedule(static)
+    for (int32_t i = 0; i < n; ++i) {
+      const uint16_t* xi = x + (int64_t)i * ldx;
+      float* yi = y + (int64_t)i * h_out;
+      const int32_t a = ids[i];
+      const int ok = a >= 0 && a < P;
+      n_invalid += !ok;
+      const uint16_t* A = ok ? A_pool + (int64_t)a * h_in * r : NULL;
+      const uint16_t* B = ok ? B_pool + (int64_t)a * r * h_out : NULL;
+      if (ok)
+        for (int32_t k = 0; k < r; ++k) {
+          float acc = 0.0f;
+          for (int32_t j = 0; j < h_in; ++j) acc = acc + bf16_to_f32(xi[j]) * bf16_to_f32(A[(int64_t)j * r + k]);
+          v[k] = acc;
+        }
+      for (int32_t c = 0; c < h_out; ++c) {
+        float base = 0.0f;
+        for (int32_t j = 0; j < h_in; ++j) {
+#if ORACLE_MUTANT == 10 /* W indexed transposed */
+          const float w = bf16_to_f32(W[((int64_t)c * h_in + j) % ((int64_t)h_in * h_out)]);
+#else
+          const float w = bf16_to_f32(W[(int64_t)j * h_out + c]);
+#endif
+          base = base + bf16_to_f32(xi[j]) * w;
+        }
+        if (ok) {
+          float d = 0.0f;
+          for (int32_t k = 0; k < r; ++k) d = d + v[k] * bf16_to_f32(B[(int64_t)k * h_out + c]);
+          yi[c] = base + s * d;
+        } else {
+          yi[c] = base;
+        }
+      }
+    }
+    free(v);
+  }
+  return n_invalid;
+}

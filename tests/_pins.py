@@ -325,6 +325,38 @@ def pin_slots_relocation(mutant=0):
     assert np.array_equal(y, y2)
 
 
+# ------------------------------------------------------------------ backbone GEMM with the LoRA delta
+
+def pin_gemm_lora_zero_W(mutant=0):
+    """W = 0 leaves exactly the delta the (pinned) SGMV oracle computes on y0 = 0."""
+    rng = np.random.default_rng(31)
+    x, A, B, y0, ids = rand_problem(rng, 12, 4, 48, 40, 8, p_invalid=0.2)
+    W = np.zeros((48, 40), np.uint16)
+    y = oracle.gemm_lora_ref(x, W, A, B, ids, 1.5, mutant=mutant)
+    ref = oracle.sgmv_ref(x, A, B, ids, 1.5, np.zeros_like(y0))
+    assert np.array_equal(y, ref)
+
+
+def pin_gemm_lora_dense(mutant=0):
+    """Against y = x.(W + s*A_a.B_a) in fp64 (the dense association), within
+    the fp32 forward error bound; invalid ids give the plain product x.W."""
+    rng = np.random.default_rng(32)
+    for n, P, h_in, h_out, r in [(10, 3, 64, 48, 8), (6, 2, 40, 24, 16)]:
+        x, A, B, _, ids = rand_problem(rng, n, P, h_in, h_out, r, p_invalid=0.2)
+        W = _b(rng.standard_normal((h_in, h_out)) / np.sqrt(h_in))
+        s = float(rng.choice([0.5, -2.0, 1.0]))
+        y = oracle.gemm_lora_ref(x, W, A, B, ids, s, mutant=mutant)
+        xf, Wf, Af, Bf = (f32_from_bf16_bits(t).astype(np.float64) for t in (x, W, A, B))
+        ref = xf @ Wf
+        mag = np.abs(xf) @ np.abs(Wf)
+        for i, a in enumerate(ids):
+            if 0 <= a < P:
+                ref[i] += s * (xf[i] @ (Af[a] @ Bf[a]))
+                mag[i] += abs(s) * ((np.abs(xf[i]) @ np.abs(Af[a])) @ np.abs(Bf[a]))
+        bound = (h_in + r + 3) * U32 * mag * 1.01
+        assert np.all(np.abs(y - ref) <= bound), np.max(np.abs(y - ref) - bound)
+
+
 ALL_PINS = [
     pin_golden_segment,
     pin_golden_sgmv,
@@ -340,4 +372,6 @@ ALL_PINS = [
     pin_slots_zero_padding,
     pin_slots_invalid_entries,
     pin_slots_relocation,
+    pin_gemm_lora_zero_W,
+    pin_gemm_lora_dense,
 ]

@@ -25,6 +25,7 @@ MUTANTS = {
     7: "empty adapters kept as segments",
     8: "slot stride from the adapter's rank",
     9: "slot adapters read at the slot capacity's rank",
+    10: "backbone W indexed transposed",
 }
 
 
