@@ -41,14 +41,27 @@ def stale() -> bool:
     return any(os.path.getmtime(f) > t for f in sources() + headers())
 
 
-def build(verbose: bool = False, extra=()) -> str:
-    cmd = [_nvcc(), *ARCH, *NVCC_FLAGS, *extra, *sources(), "-o", LIB + ".tmp"]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-        print(" ".join(cmd))
-    subprocess.run(cmd, check=True)
-    os.replace(LIB + ".tmp", LIB)
-    return LIB
+def build(verbose: bool = False, extra=(), out: str = LIB) -> str:
+    """Compiles every .cu file to an object (in parallel, under _build/) and
+    links them into `out`."""
+    objdir = os.path.join(ROOT, "_build", "obj" + ("" if out == LIB else "_" + os.path.basename(out)))
+    os.makedirs(objdir, exist_ok=True)
+    flags = [f for f in NVCC_FLAGS if f != "--shared"]
+    jobs, objs = [], []
+    for src in sources():
+        obj = os.path.join(objdir, os.path.basename(src) + ".o")
+        objs.append(obj)
+        cmd = [_nvcc(), *ARCH, *flags, *extra, "-c", src, "-o", obj]
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+            print(" ".join(cmd))
+        jobs.append((cmd, subprocess.Popen(cmd)))
+    failed = [cmd for cmd, p in jobs if p.wait() != 0]
+    if failed:
+        raise subprocess.CalledProcessError(1, failed[0])
+    subprocess.run([_nvcc(), *ARCH, "--shared", "-Xcompiler", "-fPIC", *objs, "-o", out + ".tmp"], check=True)
+    os.replace(out + ".tmp", out)
+    return out
 
 
 if __name__ == "__main__":

@@ -10,9 +10,14 @@
 // holds it until the process exits.  All calls share it (it keeps whatever the
 // last call left; the kernel clears the part it uses on entry), so two calls
 // whose kernels overlap on the GPU race on it.  Host code cannot use the
-// array's name as a device address, so the address is looked up once per
-// device with cudaGetSymbolAddress, with that device current, on the first
-// call made on that device.
+// array's name as a device address, so its address is looked up with
+// cudaGetSymbolAddress, with the device current, on the first call made in a
+// CUDA context; the address is cached per context (by the driver's unique
+// context id), so a context created later (after cudaDeviceReset, or one made
+// current through the driver API) looks it up again instead of reusing an
+// address that belonged to a destroyed or foreign context.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -27,22 +32,62 @@ static_assert(kNoAllocScratchBytes % 256 == 0, "scratch size");
 
 static __device__ __align__(256) int32_t g_segment_scratch[kNoAllocScratchBytes / sizeof(int32_t)];
 
-constexpr int kMaxDevices = 64;
+struct ScratchEntry {
+  unsigned long long ctx_id;  // 0: unused (the driver's context ids start at 1)
+  int32_t* ptr;
+};
+constexpr int kEntries = 64;
 std::mutex g_mu;
-int32_t* g_scratch_ptr[kMaxDevices] = {};
+ScratchEntry g_cache[kEntries] = {};
+int g_next = 0;
 
-// Device address of g_segment_scratch on the current device (looked up once).
-lora_status scratch_on_current_device(int32_t** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return LORA_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_segment_scratch) != cudaSuccess || p == nullptr) return LORA_ERR_CUDA;
-    g_scratch_ptr[dev] = static_cast<int32_t*>(p);
+PFN_cuCtxGetCurrent_v4000 g_get_current = nullptr;
+PFN_cuCtxGetId_v12000 g_get_id = nullptr;
+std::once_flag g_once;
+
+// Unique id of the CUDA context current on this thread (after the runtime has
+// made the device's primary context current if none was).
+lora_status current_context_id(unsigned long long* id) {
+  std::call_once(g_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+  });
+  if (g_get_current == nullptr || g_get_id == nullptr) return LORA_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (g_get_current(&ctx) != CUDA_SUCCESS) return LORA_ERR_CUDA;
+  if (ctx == nullptr) {
+    // no context current on this thread yet: make the device's primary context current
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) return LORA_ERR_CUDA;
+    if (g_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return LORA_ERR_CUDA;
   }
-  *out = g_scratch_ptr[dev];
+  if (g_get_id(ctx, id) != CUDA_SUCCESS || *id == 0) return LORA_ERR_CUDA;
+  return LORA_OK;
+}
+
+// Device address of g_segment_scratch in the current context (looked up on
+// the first call in each context).
+lora_status scratch_in_current_context(int32_t** out) {
+  unsigned long long id = 0;
+  if (const lora_status s = current_context_id(&id); s != LORA_OK) return s;
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (const ScratchEntry& e : g_cache)
+    if (e.ctx_id == id) {
+      *out = e.ptr;
+      return LORA_OK;
+    }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_segment_scratch) != cudaSuccess || p == nullptr) return LORA_ERR_CUDA;
+  g_cache[g_next] = ScratchEntry{id, static_cast<int32_t*>(p)};
+  g_next = (g_next + 1) % kEntries;
+  *out = static_cast<int32_t*>(p);
   return LORA_OK;
 }
 
@@ -61,7 +106,7 @@ extern "C" lora_status lora_segment_noalloc(const int32_t* ids, int32_t n_tokens
   int32_t* scratch = nullptr;
   if (pl.gmem) {
     if (pl.ws_bytes > kNoAllocScratchBytes) return LORA_ERR_WORKSPACE;
-    const lora_status s = scratch_on_current_device(&scratch);
+    const lora_status s = scratch_in_current_context(&scratch);
     if (s != LORA_OK) return s;
   }
   return launch_segment(ids, n_tokens, n_adapters, perm, seg_offsets, seg_adapter, num_segments, scratch,

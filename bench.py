@@ -92,6 +92,22 @@ def launches_per_step(wl) -> int:
     return 3 if dominant_kernel(wl) == "sgmv_tc_kernel" else 2
 
 
+def config_of(wl, ids: np.ndarray, world: int) -> dict:
+    """The workload description both arms print (identical keys and values)."""
+    return {"workload": wl.description, "name": wl.name, "n_tokens": wl.n, "rank": wl.r, "pool": wl.P,
+            "distinct_adapters": int(np.unique(ids[(ids >= 0) & (ids < wl.P)]).size),
+            "projections": len(wl.projs), "parallelism": "replicas" if world > 1 else "single"}
+
+
+def n_copies(step_bytes: int, max_copies: int) -> int:
+    """Independent input copies the timed graphs rotate over so that the bytes
+    touched per cycle exceed 2.2x the L2 (every step reads HBM); one copy when
+    a single step already moves more than four L2s."""
+    if step_bytes > 4 * L2_BYTES:
+        return 1
+    return max(2, min(max_copies, int(np.ceil(2.2 * L2_BYTES / step_bytes))))
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -258,8 +274,7 @@ def run_reference(args) -> None:
         "impl": "reference", "metric": METRIC, "value": round(us, 3), "unit": "us", "n_gpus": args.gpus,
         "steps": calls, "warmup": args.warmup, "ms_per_step": round(per * 1e3, 4), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": wl.description, "name": wl.name, "n_tokens": wl.n, "rank": wl.r,
-                   "pool": wl.P, "projections": len(wl.projs)},
+        "config": config_of(wl, wl.ids(), world),
         "cpu_baseline": {"value": round(us, 3), "unit": "us", "cores": threads, "kind": "oracle",
                          "sample": f"{calls} full calls (segmentation + per-token fp32 SGMV, all tokens)"},
         "e2e": {"value": round(us, 3), "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -289,7 +304,7 @@ def run_ours(args) -> None:
     abytes = algorithmic_bytes(wl, ids_np)
     nflop = flops(wl, ids_np)
     copy_bytes = abytes  # bytes one step touches
-    NB = max(2, min(args.max_copies, int(np.ceil(2.2 * L2_BYTES / copy_bytes))))
+    NB = n_copies(copy_bytes, args.max_copies)
 
     copies = []
     for c in range(NB):
@@ -417,21 +432,25 @@ def run_ours(args) -> None:
 
     if one_launch(wl):
         # the step is one launch of the SGMV kernel (segmentation inside)
-        kern_avg_ms = reduce_max(_time_graph(g_step, side) / K, world)
+        kern_avg_ms = reduce_max(_time_graph_median(g_step, side)[0] / K, world)
         seg_avg_ms = None
     else:
-        kern_avg_ms = reduce_max(_time_graph(g_kern, side) / K, world)
-        seg_avg_ms = reduce_max(_time_graph(g_seg, side) / K, world)
+        kern_avg_ms = reduce_max(_time_graph_median(g_kern, side)[0] / K, world)
+        seg_avg_ms = reduce_max(_time_graph_median(g_seg, side)[0] / K, world)
     clocks = sampler.stop()
     assert int(err.item()) == 0, f"device error flag {int(err.item())}"
 
     # mixed vs single adapter on the same shape (Punica: almost no difference)
     mixed = None
     if args.workload.startswith("7b_proj_") and not args.no_mixed:
-        mixed = {}
+        mixed = {"how": "us per step (segment + fused, one call); median of 7 replays of a K-step graph after "
+                        "0.2 s of replays; [min, max] of the 7 beside it"}
         for pat in ("same", "zipf", "distinct"):
-            mixed[pat] = round(_time_variant(f"7b_proj_{pat}", K, Wm, dev, lsg, args.max_copies), 3)
+            med, lo, hi = _time_variant(f"7b_proj_{pat}", K, Wm, dev, lsg, args.max_copies)
+            mixed[pat] = round(med, 3)
+            mixed[pat + "_range"] = [round(lo, 3), round(hi, 3)]
         mixed["distinct_over_same"] = round(mixed["distinct"] / mixed["same"], 3)
+        mixed["zipf_over_same"] = round(mixed["zipf"] / mixed["same"], 3)
 
     peak, peak_kind = hbm_peak()
     achieved = abytes / (kern_avg_ms * 1e-3) / 1e9
@@ -441,12 +460,11 @@ def run_ours(args) -> None:
         "metric": METRIC, "value": round(ms_step * 1e3, 3), "unit": "us", "n_gpus": world, "steps": K,
         "warmup": Wm, "ms_per_step": round(ms_step, 5), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.description, "name": wl.name, "n_tokens": wl.n, "rank": wl.r, "pool": wl.P,
-                   "distinct_adapters": int(np.unique(ids_np).size), "projections": len(wl.projs),
-                   "parallelism": "replicas" if world > 1 else "single",
-                   "l2": f"rotating {NB} input copies (x, ids, y, pool); {NB * copy_bytes / L2_BYTES:.1f}x L2 "
+        "config": config_of(wl, ids_np, world),
+        "timing": {"l2": f"rotating {NB} input copies (x, ids, y, pool); {NB * copy_bytes / L2_BYTES:.1f}x L2 "
                          "touched per cycle",
-                   "timing": "CUDA graph of K steps, CUDA events around the replay"},
+                   "value": "CUDA graph of K steps, CUDA events around one replay after 0.5 s of replays",
+                   "kernel": "median of 7 replays of a K-launch graph"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_kind,
                      "kernel": kname, "kernel_us": round(kern_avg_ms * 1e3, 3),
@@ -463,7 +481,9 @@ def run_ours(args) -> None:
     }
     if mixed is not None:
         out["mixed_vs_single_us"] = mixed
-    if args.batch_curve:
+    if not args.no_per_config and world == 1:
+        out["per_config"] = per_config(K, Wm, dev, lsg, args.max_copies, peak)
+    if not args.no_batch_curve and world == 1:
         out["batch_curve_us"] = batch_curve(K, Wm, dev, lsg, args.max_copies)
     if not args.no_slots and world == 1:
         out["slot_pool_us"] = slots_measure(K, Wm, dev, lsg, args.max_copies, peak)
@@ -483,20 +503,29 @@ def run_ours(args) -> None:
         dist.destroy_process_group()
 
 
-def _time_graph(g, stream) -> float:
-    """Milliseconds of one replay of graph `g`, timed with CUDA events on the
-    stream it replays on (after one untimed replay)."""
+def _time_graph_median(g, stream, reps: int = 7, settle_s: float = 0.0):
+    """(median, min, max) milliseconds of one replay of graph `g` over `reps`
+    replays, each timed with CUDA events on the stream it replays on (after
+    one untimed replay, and `settle_s` seconds of untimed replays)."""
     import torch
 
+    times = []
     with torch.cuda.stream(stream):
         g.replay()
         stream.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        g.replay()
-        e1.record(stream)
+        t_end = time.perf_counter() + settle_s
+        while time.perf_counter() < t_end:
+            g.replay()
+            stream.synchronize()
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            stream.synchronize()
+            times.append(e0.elapsed_time(e1))
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1)
+    return statistics.median(times), min(times), max(times)
 
 
 def _time_variant(name, K, Wm, dev, lsg, max_copies):
@@ -505,7 +534,7 @@ def _time_variant(name, K, Wm, dev, lsg, max_copies):
 
     wl = WORKLOADS[name]
     ids_np = wl.ids()
-    NB = max(2, min(max_copies, int(np.ceil(2.2 * L2_BYTES / algorithmic_bytes(wl, ids_np)))))
+    NB = n_copies(algorithmic_bytes(wl, ids_np), max_copies)
     copies = []
     for c in range(NB):
         inp = make_inputs(wl, dev, copy=c)
@@ -525,14 +554,10 @@ def _time_variant(name, K, Wm, dev, lsg, max_copies):
     with torch.cuda.graph(g, stream=side):
         for k in range(K):
             step(k)
-    g.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    g.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / K * 1e3
+    med, lo, hi = _time_graph_median(g, side, reps=7, settle_s=0.2)
+    del g, copies
+    torch.cuda.empty_cache()
+    return med / K * 1e3, lo / K * 1e3, hi / K * 1e3
 
 
 def _time_ids(wl, ids, K, Wm, dev, lsg, max_copies):
@@ -541,7 +566,7 @@ def _time_ids(wl, ids, K, Wm, dev, lsg, max_copies):
     import torch
 
     ids = np.asarray(ids, np.int32)
-    NB = max(2, min(max_copies, int(np.ceil(2.2 * L2_BYTES / algorithmic_bytes(wl, ids)))))
+    NB = n_copies(algorithmic_bytes(wl, ids), max_copies)
     copies = []
     for c in range(NB):
         inp = make_inputs(wl, dev, copy=c, ids=ids)
@@ -562,7 +587,7 @@ def _time_ids(wl, ids, K, Wm, dev, lsg, max_copies):
     with torch.cuda.graph(g, stream=side):
         for k in range(K):
             step(k)
-    t = _time_graph(g, side) / K * 1e3
+    t = _time_graph_median(g, side, reps=5)[0] / K * 1e3
     del g, copies
     torch.cuda.empty_cache()
     return round(t, 3)
@@ -576,7 +601,7 @@ def _time_slots(h_in, h_out, ids, rank_of, n_slots, r_max, ranks, K, Wm, dev, ls
     P = len(rank_of)
     used = np.unique(ids)
     bytes_ = int(sum((h_in + h_out) * 2 * int(rank_of[a]) for a in used) + ids.size * (h_in + 2 * h_out) * 2)
-    NB = max(2, min(max_copies, int(np.ceil(2.2 * L2_BYTES / bytes_))))
+    NB = n_copies(bytes_, max_copies)
     copies = []
     for c in range(NB):
         si = make_slot_inputs(h_in, h_out, ids, rank_of, n_slots, r_max, dev, copy=c, name=name)
@@ -599,7 +624,7 @@ def _time_slots(h_in, h_out, ids, rank_of, n_slots, r_max, ranks, K, Wm, dev, ls
     with torch.cuda.graph(g, stream=side):
         for k in range(K):
             step(k)
-    t = _time_graph(g, side) / K * 1e3
+    t = _time_graph_median(g, side, reps=5)[0] / K * 1e3
     del g, copies
     torch.cuda.empty_cache()
     return round(t, 3), bytes_
@@ -701,6 +726,74 @@ def pool_loader_measure(g_step, K, dev, lsg, n_layers=32, reps=5):
                    "table entry; CUDA events on the loader and compute streams"}
 
 
+PER_CONFIG = ("7b_layer", "13b_prefill", "70b_decode_r8", "70b_decode_r16", "70b_decode_r32", "70b_decode_r64")
+
+
+def per_config(K, Wm, dev, lsg, max_copies, peak):
+    """Times and roofline fractions of the multi-projection workloads (the
+    Llama2-7B decode layer, the Llama2-13B prefill batch, the Llama2-70B
+    decode batches at ranks 8-64), each with its own L2 rotation.
+    step_us: one sgmv_multi_segment call (segmentation + SGMV); sgmv_us: the
+    SGMV launches alone (segmentation given); kernel_us: the step when it is
+    one launch, else the SGMV launches.  Each is the median of 7 replays of a
+    K-call graph, timed with CUDA events on the replay stream."""
+    import torch
+
+    out = {"how": "median of 7 replays of a K-call graph (CUDA events on the replay stream); frac = "
+                  "algorithmic bytes / kernel_us / measured HBM peak"}
+    for name in PER_CONFIG:
+        wl = WORKLOADS[name]
+        ids = wl.ids()
+        ab, nf = algorithmic_bytes(wl, ids), flops(wl, ids)
+        NB = n_copies(ab, max_copies)
+        copies = []
+        for c in range(NB):
+            inp = make_inputs(wl, dev, copy=c)
+            projs = [(inp.x[p.x_key], inp.A[i], inp.B[i], inp.y0[i], wl.scale) for i, p in enumerate(wl.projs)]
+            copies.append((inp, lsg.Segments.empty(wl.n, wl.P, dev), projs, lsg.make_projs(projs)))
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        ws_bytes = lsg.lora_segment_workspace_bytes(wl.n, wl.P)
+        ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev) if ws_bytes else None
+        side = torch.cuda.Stream(dev)
+
+        def step(k):
+            inp, seg, projs, cp = copies[k % NB]
+            lsg.sgmv_multi_segment(projs, inp.ids, wl.P, out=seg, workspace=ws, err_flag=err, c_projs=cp)
+
+        def sgmv(k):
+            inp, seg, projs, cp = copies[k % NB]
+            lsg.sgmv_multi(projs, seg, err_flag=err, c_projs=cp)
+
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for k in range(max(Wm, NB)):
+                step(k)
+        torch.cuda.synchronize()
+        graphs = []
+        for fn in (step, sgmv):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for k in range(K):
+                    fn(k)
+            graphs.append(g)
+        step_ms = _time_graph_median(graphs[0], side, settle_s=0.2)[0] / K
+        sgmv_ms = _time_graph_median(graphs[1], side)[0] / K
+        assert int(err.item()) == 0, f"{name}: device error flag {int(err.item())}"
+        kern_ms = step_ms if one_launch(wl) else sgmv_ms
+        kname = dominant_kernel(wl)
+        gbs = ab / (kern_ms * 1e-3) / 1e9
+        out[name] = {"step_us": round(step_ms * 1e3, 3), "sgmv_us": round(sgmv_ms * 1e3, 3),
+                     "kernel_us": round(kern_ms * 1e3, 3), "kernel": kname,
+                     "launches_per_step": launches_per_step(wl), "algorithmic_bytes": int(ab), "flops": int(nf),
+                     "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                     "tflops": round(nf / (kern_ms * 1e-3) / 1e12, 3),
+                     "distinct_adapters": int(np.unique(ids).size), "input_copies": NB,
+                     "traffic": recorded_traffic(kname, name)}
+        del graphs, copies, ws
+        torch.cuda.empty_cache()
+    return out
+
+
 def batch_curve(K, Wm, dev, lsg, max_copies):
     """Step latency against batch size, identical vs mixed adapters, for a
     decode projection (Llama2-7B 4096->4096, r=16) and a prefill projection
@@ -750,8 +843,10 @@ def main(argv=None):
     ap.add_argument("--no-slots", action="store_true", help="skip the slot-arena / mixed-rank measurement")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="time cap of the reference arm's timed calls")
-    ap.add_argument("--batch-curve", action="store_true",
-                    help="add step latency against batch size (decode and prefill, identical vs mixed adapters)")
+    ap.add_argument("--no-batch-curve", action="store_true",
+                    help="skip step latency against batch size (decode and prefill, identical vs mixed adapters)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-workload kernel times of the 7B layer, 13B prefill and 70B decode batches")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

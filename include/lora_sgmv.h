@@ -144,11 +144,17 @@ LORA_API lora_status lora_segment(const int32_t* ids, int32_t n_tokens, int32_t 
  * workspace: when the pool is too large for shared-memory histograms the
  * scratch comes from a library-owned device array of
  * LORA_SEGMENT_NOALLOC_SCRATCH_BYTES (8 MiB) that every GPU which loads the
- * library holds until the process exits.  Pools needing more scratch than that
+ * library holds until the process exits (under CUDA's lazy module loading the
+ * array is reserved when the first call in a context loads the module that
+ * holds it).  Pools needing more scratch than that
  * (more than about 63,500 adapters) return LORA_ERR_WORKSPACE without a launch.
  * The call allocates nothing.
- *  - The first call on a device (with that device current) looks up the
- *    array's device address; make that first call before any stream capture.
+ *  - The first call in each CUDA context (with its device current) looks up
+ *    the array's device address and caches it for that context; make that
+ *    first call before any stream capture.  A context created later (after
+ *    cudaDeviceReset, or another context made current through the driver API)
+ *    gets its own lookup on its first call: a cached address is never reused
+ *    in another context.
  *  - All calls share the array and it keeps the last call's contents (each
  *    kernel clears the part it uses), so calls whose kernels overlap on the
  *    GPU (different streams, or concurrent graphs) race on it: order them.

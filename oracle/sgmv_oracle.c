@@ -13,7 +13,7 @@
  *   segmentation:  stable sort of the token indices by adapter id
  *   delta:         y[i,:] = y0[i,:] + s * ((x[i,:] . A[a_i]) . B[a_i])
  *
- * Readings where the pages are silent (each is listed in the design notes):
+ * Readings taken where the pages are silent:
  *  - the scale s multiplies the expanded product, after the B contraction;
  *  - the association is (x.A).B (shrink to rank r, then expand);
  *  - A[a] is [h_in][r] row-major, B[a] is [r][h_out] row-major, pools are

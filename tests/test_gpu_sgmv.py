@@ -61,36 +61,50 @@ def test_7b_layer_all_projections():
         assert_within_tol(r.y(i), r.ref(i), p.name)
 
 
-def test_13b_prefill_sampled_and_full_crosscheck():
+def test_13b_prefill_every_row():
+    """All 6224 rows of all seven projections against the oracle (the
+    oracle's threaded entry point), plus an extra cross-check of every row
+    against fp32 torch.matmul."""
     wl = WORKLOADS["13b_prefill"]
     r = Run(wl)
-    ref = check_segments(r.seg, r.ids, wl.P)
+    check_segments(r.seg, r.ids, wl.P)
     assert int(r.err.cpu()[0]) == 0
-    offs = ref["seg_offsets"][: ref["num_segments"] + 1]
-    rng = np.random.default_rng(0)
-    rows = np.unique(np.concatenate([offs[:-1], offs[1:] - 1, offs[:-1] + 127, offs[:-1] + 128,
-                                     rng.integers(0, wl.n, 24)]))
-    rows = rows[rows < wl.n]
     for i, p in enumerate(wl.projs):
-        assert_within_tol(r.y(i)[torch.from_numpy(rows).cuda()], r.ref(i, rows), p.name)
-    # every row, against fp32 torch.matmul
+        assert_within_tol(r.y(i), r.ref(i), p.name)
     for i, p in enumerate(wl.projs):
         full = _torch_fp32_reference(r.inp.x[p.x_key], r.inp.A[i], r.inp.B[i], r.ids, wl.scale, r.y0[i])
         assert_within_tol(r.y(i), full, p.name + " (all rows vs fp32 matmul)")
+    del r
+    torch.cuda.empty_cache()
 
 
 @pytest.mark.parametrize("rank", [8, 16, 32, 64])
 def test_70b_decode(rank):
+    """All 256 rows of all seven projections against the oracle."""
     wl = WORKLOADS[f"70b_decode_r{rank}"]
     r = Run(wl)
     check_segments(r.seg, r.ids, wl.P)
     assert int(r.err.cpu()[0]) == 0
-    rows = None if rank <= 16 else np.random.default_rng(rank).choice(wl.n, 96, replace=False)
     for i, p in enumerate(wl.projs):
-        y = r.y(i) if rows is None else r.y(i)[torch.from_numpy(rows).cuda()]
-        assert_within_tol(y, r.ref(i, rows), p.name)
+        assert_within_tol(r.y(i), r.ref(i), p.name)
     del r
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("mixed", [False, True], ids=["one_adapter", "16_requests"])
+def test_13b_projection_4096_tokens(mixed):
+    """The largest prefill point of the batch-size curve: one Llama2-13B
+    projection (5120 -> 5120, r=64) over 4096 tokens, of one adapter or of 16
+    requests of 256 tokens with their own adapters; every row."""
+    from workloads import Proj, Workload
+
+    n, P = 4096, 32
+    wl = Workload("curve_pre", (Proj("proj", 5120, 5120, "x"),), 64, P, n, 1.0, lambda: None, "", "curve_pre")
+    ids = np.repeat(np.arange(16, dtype=np.int32), n // 16) if mixed else np.zeros(n, np.int32)
+    r = Run(wl, ids=ids)
+    check_segments(r.seg, r.ids, P)
+    assert int(r.err.cpu()[0]) == 0
+    assert_within_tol(r.y(0), r.ref(0))
 
 
 # ------------------------------------------------------------ shrink / expand

@@ -35,6 +35,12 @@ def test_noalloc_equals_lora_segment_on_two_calls_in_a_row(n, P):
         assert lsg.lora_segment_workspace_bytes(n, P) > 0
     rng = np.random.default_rng(n + P)
     out = lsg.Segments.empty(n, P)
+    # warm-up call: with CUDA's lazy module loading, the first call in a
+    # context loads the library module that holds the scratch array, which
+    # reserves its 8 MiB then (a module load, not an allocation by the call)
+    warm_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert _noalloc(lib, torch.zeros(n, dtype=torch.int32, device="cuda"), P, out, warm_err) == 0
+    torch.cuda.synchronize()
     for call in range(2):
         ids_np = rng.integers(0, P, n).astype(np.int32)
         ids_np[rng.random(n) < 0.01] = -1  # a few invalid ids as well
@@ -43,8 +49,14 @@ def test_noalloc_equals_lora_segment_on_two_calls_in_a_row(n, P):
         ref = lsg.lora_segment(ids, P, err_flag=err_ref)
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
         out.num_segments.fill_(-7)
+        torch.cuda.synchronize()
+        # the call allocates no device memory: neither the driver's free memory
+        # nor torch's allocator moves across it
+        free0, torch0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
         assert _noalloc(lib, ids, P, out, err) == 0
         torch.cuda.synchronize()
+        assert torch.cuda.mem_get_info()[0] >= free0, call
+        assert torch.cuda.memory_allocated() == torch0, call
         ms = min(n, P)
         assert int(out.num_segments.item()) == int(ref.num_segments.item()), call
         assert torch.equal(out.perm[:n], ref.perm[:n]), call
