@@ -12,6 +12,8 @@ from .lora_sgmv import (  # noqa: F401
     SYMBOLS,
     Segments,
     SlotTable,
+    gemm_lora,
+    gemm_lora_workspace_bytes,
     load_library,
     lora_segment,
     lora_segment_noalloc,
@@ -40,5 +42,5 @@ __all__ = [
     "sgmv_fused", "sgmv_multi", "make_projs", "SlotTable", "rank_mask", "make_slot_projs", "sgmv_multi_slots",
     "sgmv_fused_slots", "lora_slot_copy", "lora_slot_assign", "make_slot_srcs",
     "sgmv_multi_host", "sgmv_multi_host_workspace_bytes", "make_host_projs", "sgmv_multi_segment",
-    "sgmv_fused_segment",
+    "sgmv_fused_segment", "gemm_lora", "gemm_lora_workspace_bytes",
 ]

@@ -64,17 +64,37 @@ struct SgmvCall {
   // else with lora_segment first, using seg_hist as its workspace).
   const int32_t* ids;
   int32_t* seg_hist;
+  // The long segments were handled by another launch (the backbone GEMM with
+  // the fused expand): this call skips them and launches no tensor-tile kernel.
+  int32_t long_done;
 };
 
 lora_status launch_sgmv_cc(const SgmvCall& call, cudaStream_t stream);
 
 // ---- SGMV (tcgen05 tile path for long segments)
-// Segments of at least kLongSeg tokens whose rows are contiguous in x / y go
-// to the tensor-tile kernel when it applies (fused calls, r in {16, 32, 64});
-// the split-K kernel skips exactly those segments then.
+// Segments of at least kLongSeg tokens go to the tensor-tile kernel when it
+// applies (a batch where segments can be long; every mode and rank); the
+// split-K kernel skips exactly those segments then.
 constexpr int kLongSeg = 64;
 bool sgmv_tc_applicable(const SgmvCall& call);
 lora_status launch_sgmv_tc(const SgmvCall& call, cudaStream_t stream);
+
+// ---- backbone GEMM with the LoRA expand fused into its epilogue
+struct GemmLoraCall {
+  const uint16_t* x;
+  int64_t ldx;
+  const uint16_t* W;  // [h_in][h_out]
+  const uint16_t* A_pool;
+  const uint16_t* B_pool;
+  int32_t n_adapters, h_in, h_out, r;
+  float scale;
+  lora_segments seg;
+  uint16_t* y;
+  int64_t ldy;
+  float* v;  // workspace [n][r]
+  int32_t* err_flag;
+};
+lora_status launch_gemm_lora(const GemmLoraCall& call, cudaStream_t stream);
 
 // TMA tensor map over bf16 data: `rank` dims (innermost first), byte strides
 // of dims 1.., box extents in elements, swizzle span in bytes (0 = none).

@@ -355,6 +355,44 @@ lora_status sgmv_multi_segment(const lora_proj* projs, int32_t n_proj, int32_t n
   return launch_sgmv_cc(c, reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t gemm_lora_workspace_bytes(int32_t n_tokens, int32_t r) {
+  if (n_tokens < 0 || !rank_ok(r)) return 0;
+  return static_cast<size_t>(n_tokens) * r * sizeof(float);
+}
+
+lora_status gemm_lora(const lora_bf16* x, int64_t ldx, const lora_bf16* W, const lora_bf16* A_pool,
+                      const lora_bf16* B_pool, int32_t n_adapters, int32_t h_in, int32_t h_out, int32_t r, float scale,
+                      const lora_segments* seg, lora_bf16* y, int64_t ldy, void* workspace, size_t workspace_bytes,
+                      int32_t* err_flag, lora_stream_t stream) {
+  lora_status s = check_seg(seg, n_adapters);
+  if (s != LORA_OK) return s;
+  if (!rank_ok(r)) return LORA_ERR_UNSUPPORTED;
+  if (seg->n_tokens == 0) return LORA_OK;
+  s = check_proj(x, ldx, A_pool, B_pool, y, ldy, h_in, h_out, true, true);
+  if (s != LORA_OK) return s;
+  if (!W) return LORA_ERR_INVALID_ARG;
+  if (!al16(W)) return LORA_ERR_MISALIGNED;
+  if (!workspace || workspace_bytes < gemm_lora_workspace_bytes(seg->n_tokens, r)) return LORA_ERR_WORKSPACE;
+  if (!al16(workspace)) return LORA_ERR_MISALIGNED;
+  GemmLoraCall c{};
+  c.x = x;
+  c.ldx = ldx;
+  c.W = W;
+  c.A_pool = A_pool;
+  c.B_pool = B_pool;
+  c.n_adapters = n_adapters;
+  c.h_in = h_in;
+  c.h_out = h_out;
+  c.r = r;
+  c.scale = scale;
+  c.seg = *seg;
+  c.y = y;
+  c.ldy = ldy;
+  c.v = static_cast<float*>(workspace);
+  c.err_flag = err_flag;
+  return launch_gemm_lora(c, reinterpret_cast<cudaStream_t>(stream));
+}
+
 lora_status sgmv_fused(const lora_bf16* x, int64_t ldx, const lora_bf16* A_pool, const lora_bf16* B_pool,
                        int32_t n_adapters, int32_t h_in, int32_t h_out, int32_t r, float scale,
                        const lora_segments* seg, lora_bf16* y, int64_t ldy, int32_t* err_flag,

@@ -76,13 +76,23 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// Build-time knob: 1 = the retries of a wait carry a suspend-time hint (the
+// thread sleeps until the phase completes), 0 = plain retries.
+#ifndef LSG_WAIT_SLEEP_HINT
+#define LSG_WAIT_SLEEP_HINT 1
+#endif
+
 // Wait for the phase of parity `parity` to complete, giving up after
 // `limit_ns` nanoseconds of wall time.  Returns false on time-out.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
+#if LSG_WAIT_SLEEP_HINT
     if (mbar_try_wait_sleep(bar, parity, 1u << 16)) return true;
+#else
+    if (mbar_try_wait(bar, parity)) return true;
+#endif
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
@@ -129,6 +139,20 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int32_t
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
           smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Four rows r0..r3 of a 2-D tensor, columns [c0, c0 + w), gathered into this
+// CTA's shared memory as four consecutive rows (the tensor map's box is
+// {w, 1}; its swizzle applies as for a four-row box), completion as
+// transaction bytes on `bar`.  c0 times the element size must be a multiple
+// of 16 bytes.
+__device__ __forceinline__ void tma_gather4(void* dst, const void* tmap, int32_t c0, int32_t r0, int32_t r1,
+                                            int32_t r2, int32_t r3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -225,6 +249,12 @@ __device__ __forceinline__ void st_async_u4(uint32_t addr, uint32_t a, uint32_t 
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Arrives at named barrier `id` (counted as this warp's 32 threads) without
+// waiting for it to complete.
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ---------------------------------------------------------------- programmatic dependent launch

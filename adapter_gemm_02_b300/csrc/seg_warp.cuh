@@ -97,4 +97,80 @@ __device__ inline WarpSegOut warp_segment(const int32_t* ids, int n, int P, int3
   return o;
 }
 
+// The same result for n <= 32*E tokens (E <= 2) without shared-memory
+// scratch: lane l holds tokens l and l+32 in registers, and each token's
+// place in the stable order is the number of tokens that sort before it
+// (a smaller id, or the same id and a smaller index), counted by comparing it
+// with every token through warp shuffles.  The first token of each valid id
+// starts a segment; a segment's index is the number of segment-starting
+// tokens with a smaller id.  Ids outside [0, P) sort as P (after every valid
+// token, in token order).  perm_s[n], offs_s[S+1], adap_s[S] in shared memory.
+template <int E>
+__device__ __forceinline__ WarpSegOut warp_segment_rank(const int32_t* ids, int n, int P, int32_t* perm_s,
+                                                        int32_t* offs_s, int32_t* adap_s, int lane) {
+  constexpr int kPad = 0x7fffffff;  // lanes past n: after every token
+  int key[E];
+  bool bad = false;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = e * 32 + lane;
+    key[e] = kPad;
+    if (i < n) {
+      const int id = ids[i];
+      const bool ok = id >= 0 && id < P;
+      key[e] = ok ? id : P;
+      bad |= !ok;
+    }
+  }
+  int before[E], same_before[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) before[e] = same_before[e] = 0;
+#pragma unroll
+  for (int f = 0; f < E; ++f) {
+#pragma unroll 8
+    for (int src = 0; src < 32; ++src) {
+      const int kj = __shfl_sync(0xffffffffu, key[f], src);
+      const int j = f * 32 + src;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        before[e] += kj < key[e];
+        same_before[e] += (kj == key[e]) & (j < e * 32 + lane);
+      }
+    }
+  }
+  int S = 0, n_valid = 0;
+  unsigned lead[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    lead[e] = __ballot_sync(0xffffffffu, key[e] < P && same_before[e] == 0);
+    S += __popc(lead[e]);
+    n_valid += __popc(__ballot_sync(0xffffffffu, key[e] < P));
+  }
+  int seg[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) seg[e] = 0;
+#pragma unroll
+  for (int f = 0; f < E; ++f) {
+#pragma unroll 8
+    for (int src = 0; src < 32; ++src) {
+      const int kj = __shfl_sync(0xffffffffu, key[f], src);
+      const int lj = (lead[f] >> src) & 1;
+#pragma unroll
+      for (int e = 0; e < E; ++e) seg[e] += lj & (kj < key[e]);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = e * 32 + lane;
+    if (i < n) perm_s[before[e] + same_before[e]] = i;
+    if (key[e] < P && same_before[e] == 0) {
+      adap_s[seg[e]] = key[e];
+      offs_s[seg[e]] = before[e];
+    }
+  }
+  if (lane == 0) offs_s[S] = n_valid;
+  __syncwarp();
+  return WarpSegOut{S, n_valid, bad};
+}
+
 }  // namespace lsg

@@ -80,6 +80,9 @@ namespace lsg {
 #ifndef LSG_CC_KB_BIG
 #define LSG_CC_KB_BIG 28
 #endif
+#ifndef LSG_CC_KB_R8
+#define LSG_CC_KB_R8 LSG_CC_KB_SMALL
+#endif
 #ifndef LSG_CC_WARPS
 #define LSG_CC_WARPS 4
 #endif
@@ -147,7 +150,7 @@ struct CCTail {
   int32_t max_segments;
   int32_t n_adapters;
   int32_t csplit;     // C
-  int32_t skip_long;  // segments of >= kLongSeg contiguous tokens belong to the tensor-tile kernel
+  int32_t skip_long;  // segments of >= kLongSeg tokens belong to the tensor-tile kernel
   int32_t tc_ranks;   // slot arenas: ranks (rank_bit) whose long segments the tensor-tile kernel took
   const int32_t* slot_of;  // slot of each adapter (null: adapter a lives in slot a)
   const int32_t* rank_of;  // rank of each adapter (null: every adapter has the kernel's rank)
@@ -177,7 +180,7 @@ struct CCParams {
 template <int R, int T, int RM = R>
 struct CCCfg {
   static constexpr int kStages = RM >= 64 ? LSG_CC_STAGES_BIG : RM == 8 ? LSG_CC_STAGES_R8 : LSG_CC_STAGES_SMALL;
-  static constexpr int kStageBytes = (RM >= 64 ? LSG_CC_KB_BIG : LSG_CC_KB_SMALL) * 1024;
+  static constexpr int kStageBytes = (RM >= 64 ? LSG_CC_KB_BIG : RM == 8 ? LSG_CC_KB_R8 : LSG_CC_KB_SMALL) * 1024;
   // shrink: A rows per stage (A part + x part fit a stage), whole k-steps of
   // 16, made of NBA TMA boxes of BA rows (a box extent is at most 256)
   static constexpr int WS0 = (((kStageBytes - T * 16) / ((R + T) * 2)) / 16) * 16;
@@ -223,9 +226,15 @@ struct CCSmem {
   alignas(16) float xbuf[kXB][kMaxC][T][R];
   alignas(16) float vfull[T][R];
   alignas(16) uint16_t zero_row[8];  // fragment rows past the tile's tokens read this
+  int32_t abort;                     // a consumer warp gave up on a wait: every warp stops
 };
 
-__device__ __forceinline__ void consumer_sync() { named_bar_sync(1, kCThreads); }
+// Barrier of the consumer warps.  Returns false once a consumer warp has given
+// up on a wait (the abort flag): the caller then leaves its loop.
+__device__ __forceinline__ bool consumer_sync(const int32_t* abort) {
+  named_bar_sync(1, kCThreads);
+  return *reinterpret_cast<const volatile int32_t*>(abort) == 0;
+}
 
 __device__ __forceinline__ uint32_t ld_shared_u32(const void* p) {
   return *reinterpret_cast<const uint32_t*>(p);
@@ -266,10 +275,9 @@ struct SegCursor {
         rk = q.rank_of[ad];
       }
       if (q.skip_long && len >= kLongSeg) {
-        const int f = q.perm[o], b = q.perm[e - 1];
         // taken by the tensor-tile kernel (with slot arenas: valid slot, a rank it ran)
         const bool tc_took = q.slot_of == nullptr || (sl >= 0 && sl < q.n_slots && (rank_bit(rk) & q.tc_ranks));
-        if (f >= 0 && b < q.n_tokens && b - f == len - 1 && tc_took) len = 0;
+        if (tc_took) len = 0;
       }
     }
   }
@@ -349,6 +357,7 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
       mbar_init(&sm.empty[s], kCW);
     }
     for (int b = 0; b < kXB; ++b) mbar_init(&sm.xbar[b], 1);
+    sm.abort = 0;
     fence_mbar_init();
   }
   if (tid < 8) sm.zero_row[tid] = 0;
@@ -357,10 +366,12 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
   // arrives now and waits before its first push (or at the end).
   if (xchg) cluster_arrive_relaxed();
   // The next launch may begin its prologue; it waits for our completion before
-  // touching memory.  We wait for the launch that wrote the segmentation (and
-  // v in the expand mode) before reading anything.
+  // touching memory.  Before reading x, y, v or a segmentation record, and
+  // before writing anything, we wait for the preceding launch in the stream
+  // (which may write them).  The producer warp reads the token ids and the
+  // adapter pools first: those are never written by the launch it overlaps.
   pdl_launch_dependents();
-  pdl_wait();
+  if (warp != kCW) pdl_wait();
   // The swizzle below is computed on absolute shared addresses, which agrees
   // with the TMA's when the ring starts on a 1 KiB boundary (all CTAs alike).
   const bool ring_ok = (smem_u32(sm.ring) & 1023u) == 0;
@@ -371,6 +382,29 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
     uint32_t phase = 0;
     bool failed = !ring_ok;
     if (!ring_ok && lane == 0) set_err(q.err_flag, LORA_ERR_UNSUPPORTED);
+    // the preceding launch in the stream has completed (waited for once, just
+    // before this warp first reads x / y or a given segmentation record; then
+    // CTA 0 writes the segmentation it computed to the caller's buffers)
+    bool dep = false;
+    WarpSegOut so{0, 0, false};
+    auto wait_dep = [&]() {
+      if (dep) return;
+      pdl_wait();
+      dep = true;
+      if (q.ids != nullptr && blockIdx.x == 0) {
+        // the caller's segmentation buffers, as lora_segment fills them
+        const int n = q.n_tokens, ms = q.max_segments;
+        int32_t* perm_g = const_cast<int32_t*>(p.t.perm);
+        int32_t* offs_g = const_cast<int32_t*>(p.t.seg_offsets);
+        int32_t* adap_g = const_cast<int32_t*>(p.t.seg_adapter);
+        for (int i = lane; i < n; i += 32) perm_g[i] = q.perm[i];
+        for (int x = lane; x <= ms; x += 32) offs_g[x] = x <= so.S ? q.seg_offsets[x] : so.n_valid;
+        for (int x = lane; x < ms; x += 32) adap_g[x] = x < so.S ? q.seg_adapter[x] : -1;
+        if (lane == 0) *const_cast<int32_t*>(p.t.num_segments) = so.S;
+        if (__any_sync(0xffffffffu, so.bad) && lane == 0) set_err(q.err_flag, LORA_ERR_BAD_ADAPTER_ID);
+      }
+      __syncwarp();
+    };
     if (q.ids != nullptr) {
       const int n = q.n_tokens, P = q.n_adapters, ms = q.max_segments;
       // the sort's temporaries (ids, key cursors) in ring stage 0, which no
@@ -381,20 +415,12 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
       int32_t* offs_s = perm_s + n;
       int32_t* adap_s = offs_s + ms + 1;
       int32_t* count_s = adap_s + max(ms, 1);
-      const WarpSegOut so = warp_segment(q.ids, n, P, ids_s, cnt, perm_s, offs_s, adap_s, lane);
+      // up to 64 tokens: ranks in registers; more: counting sort in shared memory
+      so = n <= 32   ? warp_segment_rank<1>(q.ids, n, P, perm_s, offs_s, adap_s, lane)
+           : n <= 64 ? warp_segment_rank<2>(q.ids, n, P, perm_s, offs_s, adap_s, lane)
+                     : warp_segment(q.ids, n, P, ids_s, cnt, perm_s, offs_s, adap_s, lane);
       fence_proxy_async_smem();  // stage 0 is next written by the tensor copies
       if (lane == 0) *count_s = so.S;
-      if (blockIdx.x == 0) {
-        // the caller's segmentation buffers, as lora_segment fills them
-        int32_t* perm_g = const_cast<int32_t*>(q.perm);
-        int32_t* offs_g = const_cast<int32_t*>(q.seg_offsets);
-        int32_t* adap_g = const_cast<int32_t*>(q.seg_adapter);
-        for (int i = lane; i < n; i += 32) perm_g[i] = perm_s[i];
-        for (int x = lane; x <= ms; x += 32) offs_g[x] = x <= so.S ? offs_s[x] : so.n_valid;
-        for (int x = lane; x < ms; x += 32) adap_g[x] = x < so.S ? adap_s[x] : -1;
-        if (lane == 0) *const_cast<int32_t*>(q.num_segments) = so.S;
-        if (__any_sync(0xffffffffu, so.bad) && lane == 0) set_err(q.err_flag, LORA_ERR_BAD_ADAPTER_ID);
-      }
       __syncwarp();
       // the cursor reads the shared-memory copy
       if (lane == 0) {
@@ -405,19 +431,26 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
       }
       __syncwarp();
     }
+    // a given segmentation record (and a slot table) may come from the preceding launch
+    if (q.ids == nullptr) wait_dep();
     SegCursor<T> cur;
     cur.init(q, lane);
     int last_tile = -1, a = -1, sl = -1, rk = 0, t0 = 0, tlen = 0, tok = -1, ntok = 0, tk = -1;
     bool tile_ok = false, tok_ready = false;
 
+    // stages this warp has filled (bit s) and the phase parity of each one's
+    // last fill: drained before the CTA leaves after a failed wait
+    uint32_t filled = 0, fill_par = 0;
     auto acquire = [&]() -> bool {
-      bool ok = true;
-      if (lane == 0) ok = mbar_wait(&sm.empty[slot], phase ^ 1u, kWaitLimitNs);
+      bool ok = *reinterpret_cast<volatile int32_t*>(&sm.abort) == 0;
+      if (ok && lane == 0) ok = mbar_wait(&sm.empty[slot], phase ^ 1u, kWaitLimitNs);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok && lane == 0) set_err(q.err_flag, LORA_ERR_TIMEOUT);
       return ok;
     };
     auto advance = [&]() {
+      filled |= 1u << slot;
+      fill_par = (fill_par & ~(1u << slot)) | (phase << slot);
       if (++slot == kStages) {
         slot = 0;
         phase ^= 1u;
@@ -489,6 +522,7 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
             if (lane < nbx)
               tma_load_2d(st_base + lane * Cfg::BA * R * 2, &p.tmA[mi], 0, arow + r0 + lane * Cfg::BA,
                           &sm.full[slot]);
+            wait_dep();  // x rows next
             if (!tok_ready) resolve_tok();
             header(kStShrink | (st == 0 ? kStFirst : 0) | (st == nst - 1 ? kStLast : 0), pj, rl, r0, 0);
             if (lane == 0) mbar_arrive_expect_tx(&sm.full[slot], static_cast<uint32_t>(rl) * 2u * ntok);
@@ -505,6 +539,7 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
           const int sc = bw * q.map_nb[mi];  // columns per stage
           const int nst = (clen + sc - 1) / sc;
           const int brow = sl * q.rmax;  // first row of the adapter's B in the map
+          wait_dep();  // y rows next
           if (!tok_ready) resolve_tok();
           for (int st = 0; st < nst; ++st) {
             const int cc = c0 + st * sc;
@@ -528,6 +563,7 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
         }
       });
     }
+    wait_dep();  // also when this CTA had no item: CTA 0 writes the segmentation
     if (!failed && acquire()) {
       if (lane == 0) {
         sm.hdr[slot].kind = kStEnd;
@@ -539,6 +575,12 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
         sm.hdr[0].kind = kStEnd;
         mbar_arrive(&sm.full[0]);
       }
+    } else if (lane == 0) {
+      // a wait failed: no copy issued by this warp may still be landing in
+      // shared memory when the CTA leaves (bounded waits for each stage's
+      // last fill; a stage the consumers already took completes at once)
+      for (int s2 = 0; s2 < kStages; ++s2)
+        if (filled & (1u << s2)) (void)mbar_wait(&sm.full[s2], (fill_par >> s2) & 1u, kWaitLimitNs);
     }
     if (xchg) {
       cluster_wait_acquire();   // start barrier
@@ -571,14 +613,28 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
   bool quit = false;
+  int xarm = -1;  // exchange buffer armed for the current item's peer partials, until they are in
+  // This warp gives up on a wait: the error, the abort flag, and one arrival
+  // at the consumer barrier, which releases warps that wait there (or will)
+  // so that they read the flag and leave as well.
+  auto give_up = [&]() {
+    if (lane == 0) {
+      set_err(q.err_flag, LORA_ERR_TIMEOUT);
+      *reinterpret_cast<volatile int32_t*>(&sm.abort) = 1;
+    }
+    __threadfence_block();
+    __syncwarp();
+    named_bar_arrive(1, kCThreads);
+    quit = true;
+  };
 
   for (;;) {
     bool ok = true;
     if (lane == 0) ok = mbar_wait(&sm.full[slot], phase, kWaitLimitNs);
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok) {
-      if (lane == 0) set_err(q.err_flag, LORA_ERR_TIMEOUT);
-      return;
+      give_up();
+      break;
     }
     const StageHdr<T>& h = sm.hdr[slot];
     const int kind = h.kind;
@@ -603,6 +659,7 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
             for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
           if (xchg && ct == 0)
             mbar_arrive_expect_tx(&sm.xbar[b], static_cast<uint32_t>(C - 1) * T * R * 4u);
+          if (xchg) xarm = b;
         }
         // ---- v[t, :] += x[t, k-range] . A[k-range, :]  (tokens = MMA rows)
         const uint32_t a_base = smem_u32(st_base);
@@ -701,7 +758,10 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
               red[warp][g + 8][n * 8 + 2 * tig + 1] = acc[n][3];
             }
           }
-          consumer_sync();
+          if (!consumer_sync(&sm.abort)) {
+            quit = true;
+            return;
+          }
           constexpr int kV4 = T * R / 4;  // float4 elements of one partial v
           auto red_sum = [&](int i) {
             float4 vp = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -732,11 +792,15 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
             if (lane == 0) got = mbar_wait(&sm.xbar[b], (nx >> 1) & 1, kWaitLimitNs);
             got = __shfl_sync(0xffffffffu, got, 0);
             if (!got) {
-              if (lane == 0) set_err(q.err_flag, LORA_ERR_TIMEOUT);
+              give_up();
+              return;
+            }
+            xarm = -1;
+            // our own partial (plain stores) is visible to every consumer
+            if (!consumer_sync(&sm.abort)) {
               quit = true;
               return;
             }
-            consumer_sync();  // our own partial (plain stores) is visible to every consumer
             for (int i = ct; i < kV4; i += kCThreads) {
               float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
               for (int qq = 0; qq < C; ++qq) {  // fixed order: identical v in every CTA
@@ -751,7 +815,10 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
           } else {
             for (int i = ct; i < kV4; i += kCThreads) reinterpret_cast<float4*>(&vfull[0][0])[i] = red_sum(i);
           }
-          consumer_sync();
+          if (!consumer_sync(&sm.abort)) {
+            quit = true;
+            return;
+          }
           ++nx;
           if (MODE == kModeShrink && rank == 0) {
             for (int idx = ct; idx < tlen * R; idx += kCThreads) {
@@ -768,13 +835,20 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
         // ---- expand stage: y[tok, off .. off+len) += s * vfull[t] . B[:, off .. off+len)
         if (kind & kStFirst) {
           if (MODE == kModeExpand) {
-            consumer_sync();  // every warp is done with the previous item's v
+            // every warp is done with the previous item's v
+            if (!consumer_sync(&sm.abort)) {
+              quit = true;
+              return;
+            }
             for (int idx = ct; idx < T * R; idx += kCThreads) {
               const int t = idx / R, k = idx % R;
               const int tk = t < tlen ? h.tok[t] : -1;
               vfull[t][k] = tk >= 0 ? q.v_in[static_cast<int64_t>(tk) * R + k] : 0.f;
             }
-            consumer_sync();
+            if (!consumer_sync(&sm.abort)) {
+              quit = true;
+              return;
+            }
           }
           // v as bf16 hi/lo MMA A fragments (rows >= tlen are zero)
           auto split = [&](int row, int col, uint32_t& hi, uint32_t& lo) {
@@ -874,7 +948,10 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
           store(j, d0, d1);
         }
         fence_proxy_async_smem();  // our y updates, visible to the bulk stores below
-        consumer_sync();
+        if (!consumer_sync(&sm.abort)) {
+          quit = true;
+          return;
+        }
         // ---- the tile's updated y rows back to global memory, one bulk copy per token
         if (ct < tlen) {
           const int tkv = h.tok[ct];
@@ -888,7 +965,7 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
         if (lane == 0) mbar_arrive(&sm.empty[slot]);
       }
     });
-    if (quit) return;
+    if (quit) break;
     if (++slot == kStages) {
       slot = 0;
       phase ^= 1u;
@@ -896,6 +973,10 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
   }
   if (xchg) {
     if (!start_waited) cluster_wait_acquire();
+    // an exchange left before its peers' partials were in: their pushes may
+    // still arrive, and must land before this CTA may leave (bounded)
+    if (xarm >= 0 && lane == 0) (void)mbar_wait(&sm.xbar[xarm], (nx >> 1) & 1, kWaitLimitNs);
+    // no CTA leaves while a peer may still push into its shared memory
     cluster_arrive_relaxed();
     cluster_wait_acquire();
   }
@@ -927,6 +1008,8 @@ size_t seg_extra_bytes(int n, int P) {
   return static_cast<size_t>(n + (ms + 1) + std::max(ms, 1) + 1) * sizeof(int32_t);
 }
 static_assert((LSG_SEG_IN_KERNEL_MAX_TOKENS * 3 + 3) * 4 <= kSegExtraMaxBytes, "segmentation result size");
+static_assert((LSG_SEG_IN_KERNEL_MAX_TOKENS + LSG_SEG_IN_KERNEL_MAX_ADAPTERS + 1) * 4 <= LSG_CC_KB_R8 * 1024,
+              "sort temporaries in ring stage 0 (rank 8)");
 static_assert((LSG_SEG_IN_KERNEL_MAX_TOKENS + LSG_SEG_IN_KERNEL_MAX_ADAPTERS + 1) * 4 <= LSG_CC_KB_SMALL * 1024,
               "sort temporaries in ring stage 0");
 
@@ -1166,7 +1249,7 @@ lora_status launch_sgmv_cc(const SgmvCall& call, cudaStream_t stream) {
   prm.t.rank_of = call.rank_of;
   prm.t.n_slots = slots ? call.n_slots : call.n_adapters;
   prm.t.rmax = slots ? call.r_max : call.r;
-  const bool tc = sgmv_tc_applicable(call);
+  const bool tc = !call.long_done && sgmv_tc_applicable(call);
   size_t extra = 0;
   if (call.ids != nullptr) {
     // segmentation first: inside this launch when it fits, else its own kernel
@@ -1183,14 +1266,16 @@ lora_status launch_sgmv_cc(const SgmvCall& call, cudaStream_t stream) {
       if (s != LORA_OK) return s;
     }
   }
-  if (tc && !slots) {
-    // long contiguous segments on tcgen05 tiles, the rest of the batch here
+  if (call.long_done) {
+    prm.t.skip_long = 1;  // another launch took the long segments
+  } else if (tc && !slots) {
+    // long segments on tcgen05 tiles, the rest of the batch here
     const lora_status s = launch_sgmv_tc(call, stream);
     if (s != LORA_OK) return s;
     prm.t.skip_long = 1;
   } else if (tc && slots) {
-    // one tensor-tile launch per rank of the mask it serves (16, 32, 64)
-    for (int r = 16; r <= 64; r *= 2) {
+    // one tensor-tile launch per rank of the mask
+    for (int r = 8; r <= 64; r *= 2) {
       if (!(call.rank_mask & static_cast<unsigned>(rank_bit(r)) ) || r > call.r_max) continue;
       SgmvCall cr = call;
       cr.r = r;

@@ -36,9 +36,20 @@
 // item: split-K shrink, split-N expand, partial v summed through distributed
 // shared memory).  Each item recomputes its tile's shrink (x is re-read from
 // L2 by the items of the same tile), which keeps items of similar size for
-// load balance.  Only segments of at least kLongSeg tokens whose rows are
-// contiguous in x / y (true for prefill requests) are taken here; the decode
-// kernel handles the rest of the batch (it skips these segments).
+// load balance.  Every segment of at least kLongSeg tokens is taken here (the
+// decode kernel skips exactly these).  A segment whose rows are contiguous in
+// x / y (prefill requests) moves whole tiles with 2-D tensor copies; any other
+// segment (tokens of one adapter spread over the batch) gathers its rows
+// through the permutation, four rows per tile::gather4 tensor copy, and its
+// updated y rows go back to their own rows by plain 16-byte stores.
+//
+// Rank 8 runs at an MMA width of 16: the shrink's N = 16 columns read the A
+// tile's 8 columns plus 8 columns of other shared memory, whose results are
+// never used; the expand's K = 16 takes v with columns 8..15 zero and a B
+// tile whose rows 8..15 are a zero block that no copy writes.
+//
+// Modes: fused (v stays on chip), shrink (v written to device memory in fp32,
+// token order), expand (v read from device memory).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -78,7 +89,7 @@ constexpr int kMaxC = 8;  // CTAs per cluster (portable limit)
 constexpr uint64_t kTcWaitNs = 2000000000ull;
 
 struct TcProj {
-  uint16_t* y;  // for the direct stores of a tile's last rows
+  uint16_t* y;  // for the direct stores of a tile's last rows and of gathered rows
   int64_t ldy;
   int32_t h_in, h_out;
   int32_t chunk;  // columns per chunk (multiple of 128)
@@ -94,6 +105,8 @@ struct TcTail {
   const int32_t* seg_adapter;
   const int32_t* num_segments;
   int32_t* err_flag;
+  float* v_out;       // shrink mode: v [n][r] fp32, token order
+  const float* v_in;  // expand mode
   int32_t n_proj;
   int32_t ipt;  // items per tile
   int32_t n_tokens;
@@ -112,22 +125,27 @@ struct TcTail {
 
 struct TcParams {
   CUtensorMap tmX[kMaxProj];   // x [n][h_in], box {64, 128}, 128 B swizzle
+  CUtensorMap tmXg[kMaxProj];  // x, box {64, 1} (four-row gathers), 128 B swizzle
   CUtensorMap tmA[kMaxProj];   // A slabs [n_slabs][h_in][r] (slab stride h_in*rmax), box {r, 64, 1}, 2r B swizzle
   CUtensorMap tmB[kMaxProj];   // B rows [n_slabs*rmax][h_out], box {64, r}, 128 B swizzle
   CUtensorMap tmYl[kMaxProj];  // y [n][h_out], box {64, 128}, 128 B swizzle (load)
+  CUtensorMap tmYg[kMaxProj];  // y, box {64, 1} (four-row gathers), 128 B swizzle
   CUtensorMap tmYs[kMaxProj];  // y, box {64, 32}, 128 B swizzle (store)
   TcTail t;
 };
 
 template <int R>
 struct TcCfg {
-  static constexpr int kShA = 64 * R * 2;                          // A tile bytes
-  static constexpr int kShBytes = ((16384 + kShA + 1023) / 1024) * 1024;
+  static constexpr int RP = R < 16 ? 16 : R;                       // MMA width of the rank
+  static constexpr int kShA = 64 * R * 2;                          // A tile bytes the copy writes
+  static constexpr int kShARoom = 64 * RP * 2;                     // A tile bytes the shrink MMAs read
+  static constexpr int kShBytes = ((16384 + kShARoom + 1023) / 1024) * 1024;
   static constexpr int kExY = 16384 * kBH;                         // y tile bytes [128][kBN]
-  static constexpr int kExB = R * 128 * kBH;                       // B tile bytes (64-column atoms)
+  static constexpr int kExBCopy = R * 128 * kBH;                   // B tile bytes the copy writes
+  static constexpr int kExB = RP * 128 * kBH;                      // B tile bytes the expand MMAs read
   static constexpr int kExBytes = ((kExY + kExB + 1023) / 1024) * 1024;
-  static constexpr int kVop = 128 * R * 2;                         // one bf16 operand [128][r]
-  static constexpr uint32_t kSwR = R * 2;                          // swizzle span of r-wide rows
+  static constexpr int kVop = 128 * RP * 2;                        // one bf16 operand [128][RP]
+  static constexpr uint32_t kSwR = RP * 2;                         // swizzle span of RP-wide rows
   static constexpr uint32_t kSwM = kSwR / 16 - 1;
 };
 
@@ -159,28 +177,35 @@ struct TcSmem {
   int32_t abort;
 };
 
-// Cursor over the segments taken by this kernel (at least kLongSeg tokens,
-// rows contiguous), 32 at a time, locating 128-token tiles.  Executed by a
-// full warp; tile indices asked for only grow.
+// One 128-token tile of a segment taken by this kernel.
+struct TcTile {
+  int t0;    // position of its first token in the permutation
+  int tlen;  // tokens (<= 128)
+  int a;     // slab (adapter id, or slot with slot arenas)
+  int row;   // first x / y row when the segment's rows are contiguous, else -1 (rows through perm)
+};
+
+// Cursor over the segments taken by this kernel (at least kLongSeg tokens),
+// 32 at a time, locating 128-token tiles.  Executed by a full warp; tile
+// indices asked for only grow.
 struct TcCursor {
   int base = 0, tiles_before = 0, S = 0;
-  int off = 0, len = 0, ad = -1, row0 = 0;  // segment base + lane
+  int off = 0, len = 0, ad = -1, row0 = -1;  // segment base + lane
 
   __device__ void load(const TcTail& q, int lane) {
     const int s = base + lane;
     off = 0;
     len = 0;
     ad = -1;
-    row0 = 0;
+    row0 = -1;
     if (s < S) {
       const int o = q.seg_offsets[s];
       const int e = q.seg_offsets[s + 1];
       ad = q.seg_adapter[s];
       const int l = (o >= 0 && e <= q.n_tokens && e >= o) ? e - o : 0;
       if (l >= kLongSeg) {
-        const int f = q.perm[o], b = q.perm[e - 1];
-        bool take = f >= 0 && b < q.n_tokens && b - f == l - 1;
-        if (take && q.slot_of != nullptr) {
+        bool take = true;
+        if (q.slot_of != nullptr) {
           // slot arenas: the slab is the slot; other ranks and invalid entries
           // stay with the split-K kernel
           int slab = -1;
@@ -194,7 +219,10 @@ struct TcCursor {
         if (take) {
           off = o;
           len = l;
-          row0 = f;
+          // perm is ascending within a segment, so first and last rows l - 1
+          // apart mean the rows are contiguous
+          const int f = q.perm[o], b = q.perm[e - 1];
+          if (f >= 0 && b < q.n_tokens && b - f == l - 1) row0 = f;
         }
       }
     }
@@ -205,8 +233,7 @@ struct TcCursor {
     load(q, lane);
   }
 
-  // tile -> first token position t0 in perm order, length, adapter, first x/y row
-  __device__ bool find(const TcTail& q, int lane, int tile, int& tlen, int& a, int& row) {
+  __device__ bool find(const TcTail& q, int lane, int tile, TcTile& out) {
     while (base < S) {
       const int tl = (len + 127) >> 7;
       int inc = tl;
@@ -221,11 +248,13 @@ struct TcCursor {
         const int ls = __ffs(m) - 1;
         const int excl = __shfl_sync(0xffffffffu, inc - tl, ls);
         const int l = __shfl_sync(0xffffffffu, len, ls);
+        const int o = __shfl_sync(0xffffffffu, off, ls);
         const int r0 = __shfl_sync(0xffffffffu, row0, ls);
-        a = __shfl_sync(0xffffffffu, ad, ls);
+        out.a = __shfl_sync(0xffffffffu, ad, ls);
         const int k = (tile - tiles_before - excl) * 128;
-        tlen = min(128, l - k);
-        row = r0 + k;
+        out.tlen = min(128, l - k);
+        out.t0 = o + k;
+        out.row = r0 >= 0 ? r0 + k : -1;
         return true;
       }
       tiles_before += total;
@@ -235,6 +264,20 @@ struct TcCursor {
     return false;
   }
 };
+
+// Rows 4*lane .. 4*lane+3 of a gathered tile, for a four-row gather: rows past
+// the tile or outside [0, n) read a valid row of the tile instead (their
+// results are never stored).  Executed by a full warp.
+__device__ __forceinline__ void tile_rows4(const TcTail& q, const TcTile& t, int lane, int (&rr)[4]) {
+  int first = t.tlen > 0 ? q.perm[t.t0] : 0;
+  if (first < 0 || first >= q.n_tokens) first = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i = 4 * lane + j;
+    int r = i < t.tlen ? q.perm[t.t0 + i] : first;
+    rr[j] = (r >= 0 && r < q.n_tokens) ? r : first;
+  }
+}
 
 // Bounded wait by lane 0, result broadcast to the warp; a time-out sets the
 // error flag and the CTA-wide abort flag.
@@ -251,11 +294,15 @@ __device__ __forceinline__ bool warp_wait(SM& sm, uint64_t* bar, uint32_t parity
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-template <int R, bool CL>
+template <int R, bool CL, int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_constant__ TcParams p) {
   using Cfg = TcCfg<R>;
   using SM = TcSmem<R, CL>;
+  constexpr int RP = Cfg::RP;
   constexpr int kSh = SM::kSh, kEx = SM::kEx;
+  constexpr bool kHasShrink = (MODE & kModeShrink) != 0;
+  constexpr bool kHasExpand = (MODE & kModeExpand) != 0;
+  static_assert(!CL || MODE == kModeFused, "the cluster split serves the fused mode");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   auto& sm = *reinterpret_cast<SM*>(smem_raw);
   const TcTail& q = sm.t;
@@ -280,12 +327,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
   }
   if (warp == 4 && lane < kMaxProj) {
     prefetch_tmap(&p.tmX[lane]);
+    prefetch_tmap(&p.tmXg[lane]);
     prefetch_tmap(&p.tmA[lane]);
   }
   if (warp == 5 && lane < kMaxProj) {
     prefetch_tmap(&p.tmB[lane]);
     prefetch_tmap(&p.tmYl[lane]);
+    prefetch_tmap(&p.tmYg[lane]);
     prefetch_tmap(&p.tmYs[lane]);
+  }
+  if constexpr (R < RP) {
+    // rank 8: the v operand's columns 8..15 and the B tiles' rows 8..15 stay
+    // zero (no copy or store writes them)
+    for (int i = tid; i < 2 * Cfg::kVop / 16; i += kTcThreads)
+      reinterpret_cast<uint4*>(&sm.vop[0][0])[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int s = 0; s < kEx; ++s)
+      for (int i = tid; i < (Cfg::kExB - Cfg::kExBCopy) / 16; i += kTcThreads)
+        reinterpret_cast<uint4*>(sm.ex[s] + Cfg::kExY + Cfg::kExBCopy)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();  // read by the tensor cores through the async proxy
   }
   if (tid == 0) {
     for (int s = 0; s < kSh; ++s) {
@@ -321,7 +380,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
   const bool aligned = (smem_u32(sm.sh) & 1023u) == 0;
   if (!aligned && tid == 0) set_err(q.err_flag, LORA_ERR_UNSUPPORTED);
 
-  if (aligned && warp == 4) {
+  if (aligned && kHasShrink && warp == 4) {
     // ============================== shrink producer
     int slot = 0;
     uint32_t ph = 0;
@@ -329,22 +388,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
     cur.init(q, lane);
     for (int item = group;; item += ngroups) {
       const int tile = item / q.ipt, is = item - tile * q.ipt;
-      int tlen, a, row;
-      if (!cur.find(q, lane, tile, tlen, a, row)) break;
-      if (a < 0 || a >= q.n_slabs) continue;
+      TcTile t;
+      if (!cur.find(q, lane, tile, t)) break;
+      if (t.a < 0 || t.a >= q.n_slabs) continue;
       const int pj = q.item_proj[is];
       int kb0, kb1;
       split((q.proj[pj].h_in + 63) >> 6, kb0, kb1);
+      int rr[4] = {0, 0, 0, 0};
+      if (t.row < 0) tile_rows4(q, t, lane, rr);
       bool ok = true;
       for (int kb = kb0; kb < kb1 && ok; ++kb) {
         ok = warp_wait(sm, &sm.sh_empty[slot], ph ^ 1u, lane);
         if (!ok) break;
+        uint8_t* st = sm.sh[slot];
         if (lane == 0) {
-          uint8_t* st = sm.sh[slot];
           mbar_arrive_expect_tx(&sm.sh_full[slot], 16384u + Cfg::kShA);
-          tma_load_2d(st, &p.tmX[pj], kb * 64, row, &sm.sh_full[slot]);
-          tma_load_3d(st + 16384, &p.tmA[pj], 0, kb * 64, a, &sm.sh_full[slot]);
+          if (t.row >= 0) tma_load_2d(st, &p.tmX[pj], kb * 64, t.row, &sm.sh_full[slot]);
+          tma_load_3d(st + 16384, &p.tmA[pj], 0, kb * 64, t.a, &sm.sh_full[slot]);
         }
+        __syncwarp();  // the stage's byte count is registered before the gathers land
+        if (t.row < 0)
+          tma_gather4(st + lane * 512, &p.tmXg[pj], kb * 64, rr[0], rr[1], rr[2], rr[3], &sm.sh_full[slot]);
+        __syncwarp();
         if (++slot == kSh) {
           slot = 0;
           ph ^= 1u;
@@ -352,7 +417,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       }
       if (!ok || sm.abort) break;
     }
-  } else if (aligned && warp == 5) {
+  } else if (aligned && kHasExpand && warp == 5) {
     // ============================== expand producer
     int slot = 0;
     uint32_t ph = 0;
@@ -360,28 +425,38 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
     cur.init(q, lane);
     for (int item = group;; item += ngroups) {
       const int tile = item / q.ipt, is = item - tile * q.ipt;
-      int tlen, a, row;
-      if (!cur.find(q, lane, tile, tlen, a, row)) break;
-      if (a < 0 || a >= q.n_slabs) continue;
+      TcTile t;
+      if (!cur.find(q, lane, tile, t)) break;
+      if (t.a < 0 || t.a >= q.n_slabs) continue;
       const int pj = q.item_proj[is], ch = q.item_chunk[is];
       const TcProj& pr = q.proj[pj];
       const int c0 = ch * pr.chunk;
       int b0, b1;
       split((min(pr.chunk, pr.h_out - c0) + kBN - 1) / kBN, b0, b1);
+      int rr[4] = {0, 0, 0, 0};
+      if (t.row < 0) tile_rows4(q, t, lane, rr);
       bool ok = true;
       for (int b = b0; b < b1 && ok; ++b) {
         ok = warp_wait(sm, &sm.ex_empty[slot], ph ^ 1u, lane);
         if (!ok) break;
+        uint8_t* st = sm.ex[slot];
+        const int c = c0 + b * kBN;
         if (lane == 0) {
-          uint8_t* st = sm.ex[slot];
-          const int c = c0 + b * kBN;
-          mbar_arrive_expect_tx(&sm.ex_full[slot], static_cast<uint32_t>(Cfg::kExY + Cfg::kExB));
+          mbar_arrive_expect_tx(&sm.ex_full[slot], static_cast<uint32_t>(Cfg::kExY + Cfg::kExBCopy));
 #pragma unroll
           for (int h = 0; h < kBH; ++h) {
-            tma_load_2d(st + h * 16384, &p.tmYl[pj], c + h * 64, row, &sm.ex_full[slot]);
-            tma_load_2d(st + Cfg::kExY + h * R * 128, &p.tmB[pj], c + h * 64, a * q.rmax, &sm.ex_full[slot]);
+            if (t.row >= 0) tma_load_2d(st + h * 16384, &p.tmYl[pj], c + h * 64, t.row, &sm.ex_full[slot]);
+            tma_load_2d(st + Cfg::kExY + h * RP * 128, &p.tmB[pj], c + h * 64, t.a * q.rmax, &sm.ex_full[slot]);
           }
         }
+        __syncwarp();  // the stage's byte count is registered before the gathers land
+        if (t.row < 0) {
+#pragma unroll
+          for (int h = 0; h < kBH; ++h)
+            tma_gather4(st + h * 16384 + lane * 512, &p.tmYg[pj], c + h * 64, rr[0], rr[1], rr[2], rr[3],
+                        &sm.ex_full[slot]);
+        }
+        __syncwarp();
         if (++slot == kEx) {
           slot = 0;
           ph ^= 1u;
@@ -389,18 +464,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       }
       if (!ok || sm.abort) break;
     }
-  } else if (aligned && warp == 6) {
+  } else if (aligned && kHasShrink && warp == 6) {
     // ============================== shrink MMA issuer: v = x . A (this CTA's k-blocks)
-    constexpr uint32_t kIdSh = umma_idesc_bf16(128, R, 0, 1);
+    constexpr uint32_t kIdSh = umma_idesc_bf16(128, RP, 0, 1);
     int sslot = 0, it = 0;
     uint32_t sph = 0;
     TcCursor cur;
     cur.init(q, lane);
     for (int item = group;; item += ngroups) {
       const int tile = item / q.ipt, is = item - tile * q.ipt;
-      int tlen, a, row;
-      if (!cur.find(q, lane, tile, tlen, a, row)) break;
-      if (a < 0 || a >= q.n_slabs) continue;
+      TcTile t;
+      if (!cur.find(q, lane, tile, t)) break;
+      if (t.a < 0 || t.a >= q.n_slabs) continue;
       const TcProj& pr = q.proj[q.item_proj[is]];
       int kb0, kb1;
       split((pr.h_in + 63) >> 6, kb0, kb1);
@@ -417,7 +492,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint64_t ad = umma_desc(xs + k * 32, 16, 1024, 2);
-            const uint64_t bd = umma_desc(as + k * 16 * R * 2, Cfg::kShA, 8 * R * 2, umma_layout(R * 2));
+            // A tile [64][r] MN-major: r >= 16 swizzled to 2r bytes (SBO: next 8 k-rows);
+            // r = 8 without swizzle, 8x16-byte core matrices: LBO = next 8 k-rows (128 B),
+            // SBO = the 8 columns past the tile (another 1 KB of this stage; results unused)
+            const uint64_t bd = R >= 16 ? umma_desc(as + k * 16 * R * 2, Cfg::kShA, 8 * R * 2, umma_layout(R * 2))
+                                        : umma_desc(as + k * 16 * R * 2, 128, 1024, 0);
             umma_bf16(tmem + kTmemV, ad, bd, kIdSh, kb > kb0 || k > 0);
           }
           umma_commit(&sm.sh_empty[sslot]);  // the stage is free once these MMAs have read it
@@ -434,7 +513,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       if (sm.abort) break;
       ++it;
     }
-  } else if (aligned && warp == 7) {
+  } else if (aligned && kHasExpand && warp == 7) {
     // ============================== expand MMA issuer: acc = v_hi . B + v_lo . B
     constexpr uint32_t kIdEx = umma_idesc_bf16(128, kBN, 0, 1);
     int xslot = 0, ae = 0, it = 0;
@@ -443,9 +522,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
     cur.init(q, lane);
     for (int item = group;; item += ngroups) {
       const int tile = item / q.ipt, is = item - tile * q.ipt;
-      int tlen, a, row;
-      if (!cur.find(q, lane, tile, tlen, a, row)) break;
-      if (a < 0 || a >= q.n_slabs) continue;
+      TcTile t;
+      if (!cur.find(q, lane, tile, t)) break;
+      if (t.a < 0 || t.a >= q.n_slabs) continue;
       const TcProj& pr = q.proj[q.item_proj[is]];
       const int c0 = q.item_chunk[is] * pr.chunk;
       int b0, b1;
@@ -468,11 +547,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
         if (lane == 0) {
           const uint32_t bs = smem_u32(sm.ex[xslot]) + Cfg::kExY;
 #pragma unroll
-          for (int k = 0; k < R / 16; ++k) {
-            const uint64_t bd = umma_desc(bs + k * 16 * 128, R * 128, 1024, 2);
+          for (int k = 0; k < RP / 16; ++k) {
+            const uint64_t bd = umma_desc(bs + k * 16 * 128, RP * 128, 1024, 2);
 #pragma unroll
             for (int hl = 0; hl < 2; ++hl) {
-              const uint64_t ad = umma_desc(smem_u32(sm.vop[hl]) + k * 32, 16, 8 * R * 2, umma_layout(R * 2));
+              const uint64_t ad = umma_desc(smem_u32(sm.vop[hl]) + k * 32, 16, 8 * RP * 2, umma_layout(RP * 2));
               umma_bf16(tmem + kTmemAcc + buf * kBN, ad, bd, kIdEx, k > 0 || hl > 0);
             }
           }
@@ -488,7 +567,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       if (!ok || sm.abort) break;
       ++it;
     }
-  } else if (aligned && (warp < 4 || warp >= 8)) {
+  } else if (aligned && (warp < 4 || (kHasExpand && warp >= 8))) {
     // ============================== epilogue (row m = TMEM lane m): two groups
     // of four warps (0-3, 8-11); group eg turns v into the operand (group 0)
     // and updates columns [32 eg, 32 eg + 32) of every 64-column block
@@ -500,213 +579,249 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
     int pend = -1;  // (lane 0) ring slot whose y stores may still be reading it
     TcCursor cur;
     cur.init(q, lane);
+    // one 16-byte chunk (8 ranks) of a row as the hi / lo operand words
+    auto split_hl = [](const float (&f)[8], uint32_t (&hi)[4], uint32_t (&lo)[4]) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * e], f[2 * e + 1]);
+        const float2 hf = __bfloat1622float2(h);
+        const __nv_bfloat162 l = __floats2bfloat162_rn(f[2 * e] - hf.x, f[2 * e + 1] - hf.y);
+        hi[e] = *reinterpret_cast<const uint32_t*>(&h);
+        lo[e] = *reinterpret_cast<const uint32_t*>(&l);
+      }
+    };
+    // row m of the operand pair (K-major, RP-wide rows, swizzled); chunks past r keep their zeros
+    auto put_operand_row = [&](const uint32_t (&v)[RP]) {
+      const uint32_t hrow = smem_u32(sm.vop[0]) + static_cast<uint32_t>(m) * (RP * 2);
+      const uint32_t lrow = smem_u32(sm.vop[1]) + static_cast<uint32_t>(m) * (RP * 2);
+#pragma unroll
+      for (int j = 0; j < R / 8; ++j) {
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[j * 8 + e]);
+        uint32_t hi[4], lo[4];
+        split_hl(f, hi, lo);
+        const uint32_t ha = swz<Cfg::kSwM>(hrow + j * 16), la = swz<Cfg::kSwM>(lrow + j * 16);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(ha), "r"(hi[0]), "r"(hi[1]), "r"(hi[2]),
+                     "r"(hi[3])
+                     : "memory");
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(la), "r"(lo[0]), "r"(lo[1]), "r"(lo[2]),
+                     "r"(lo[3])
+                     : "memory");
+      }
+    };
     for (int item = group;; item += ngroups) {
       const int tile = item / q.ipt, is = item - tile * q.ipt;
-      int tlen, a, row;
-      if (!cur.find(q, lane, tile, tlen, a, row)) break;
-      if (a < 0 || a >= q.n_slabs) {
+      TcTile t;
+      if (!cur.find(q, lane, tile, t)) break;
+      if (t.a < 0 || t.a >= q.n_slabs) {
         if (tid == 0 && crank == 0) set_err(q.err_flag, LORA_ERR_BAD_ADAPTER_ID);
         continue;
       }
       const int pj = q.item_proj[is], ch = q.item_chunk[is];
       const TcProj& pr = q.proj[pj];
       const float scale = pr.scale;
-      int kb0, kb1;
-      split((pr.h_in + 63) >> 6, kb0, kb1);
+      // this thread's token row (-1: none, or a corrupt permutation entry: skipped and flagged)
+      int yrow = -1;
+      if (m < t.tlen) {
+        yrow = t.row >= 0 ? t.row + m : q.perm[t.t0 + m];
+        if (yrow < 0 || yrow >= q.n_tokens) {
+          if (eg == 0 && ch == 0 && crank == 0) set_err(q.err_flag, LORA_ERR_BAD_ADAPTER_ID);
+          yrow = -1;
+        }
+      }
+      int kb0 = 0, kb1 = 0;
+      if (kHasShrink) split((pr.h_in + 63) >> 6, kb0, kb1);
       bool ok = true;
       if (eg == 0) {
-      // ---- v (fp32, TMEM) -> bf16 operands hi, lo (K-major, 2r-byte swizzle)
-      ok = warp_wait(sm, &sm.v_full, it & 1, lane);
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t v[R];
-      if (kb0 < kb1) {
-        if constexpr (R == 16) {
-          tmem_ld16(tq + kTmemV, v);
-          tmem_ld_wait();
-        } else {
+        uint32_t v[RP];
+        if constexpr (kHasShrink) {
+          // ---- v (fp32, TMEM)
+          ok = warp_wait(sm, &sm.v_full, it & 1, lane);
+          if (!ok) break;
+          tc_fence_after();
+          if (kb0 < kb1) {
+            if constexpr (RP == 16) {
+              tmem_ld16(tq + kTmemV, v);
+              tmem_ld_wait();
+            } else {
 #pragma unroll
-          for (int c = 0; c < R / 32; ++c) {
-            uint32_t r32[32];
-            tmem_ld32(tq + kTmemV + c * 32, r32);
-            tmem_ld_wait();
+              for (int c = 0; c < RP / 32; ++c) {
+                uint32_t r32[32];
+                tmem_ld32(tq + kTmemV + c * 32, r32);
+                tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[c * 32 + i] = r32[i];
+                for (int i = 0; i < 32; ++i) v[c * 32 + i] = r32[i];
+              }
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < RP; ++i) v[i] = 0u;  // no k-blocks here: a zero partial
           }
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < R; ++i) v[i] = 0u;  // no k-blocks here: a zero partial
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.v_read);  // TMEM v may take the next item's shrink
-      // one 16-byte chunk (8 ranks) of a row as the hi / lo operand words
-      auto split_hl = [](const float (&f)[8], uint32_t (&hi)[4], uint32_t (&lo)[4]) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * e], f[2 * e + 1]);
-          const float2 hf = __bfloat1622float2(h);
-          const __nv_bfloat162 l = __floats2bfloat162_rn(f[2 * e] - hf.x, f[2 * e + 1] - hf.y);
-          hi[e] = *reinterpret_cast<const uint32_t*>(&h);
-          lo[e] = *reinterpret_cast<const uint32_t*>(&l);
-        }
-      };
-      if constexpr (!CL) {
-        const uint32_t hrow = smem_u32(sm.vop[0]) + static_cast<uint32_t>(m) * (R * 2);
-        const uint32_t lrow = smem_u32(sm.vop[1]) + static_cast<uint32_t>(m) * (R * 2);
-#pragma unroll
-        for (int j = 0; j < R / 8; ++j) {
-          float f[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[j * 8 + e]);
-          uint32_t hi[4], lo[4];
-          split_hl(f, hi, lo);
-          const uint32_t ha = swz<Cfg::kSwM>(hrow + j * 16), la = swz<Cfg::kSwM>(lrow + j * 16);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(ha), "r"(hi[0]), "r"(hi[1]), "r"(hi[2]),
-                       "r"(hi[3])
-                       : "memory");
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(la), "r"(lo[0]), "r"(lo[1]), "r"(lo[2]),
-                       "r"(lo[3])
-                       : "memory");
-        }
-        fence_proxy_async_smem();  // the tensor core reads the operands through the async proxy
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.vop_ready);
-      } else {
-        // ---- reduce-scatter: row m's partial to the CTA that owns the row
-        const int rpo = 128 / C;  // rows per owner
-        const int own = m / rpo, ml = m - own * rpo;
-        if (tid == 0) {
-          mbar_arrive_expect_tx(&sm.rs_full, 128u * R * 4u);    // C ranks x rpo rows x r fp32
-          mbar_arrive_expect_tx(&sm.vop_ready, 128u * R * 4u);  // 128 rows x r x (hi + lo) bf16
-        }
-        {
-          const uint32_t dst = mapa_shared(smem_u32(&sm.rbuf[(crank * rpo + ml) * R]), own);
-          const uint32_t bar = mapa_shared(smem_u32(&sm.rs_full), own);
-#pragma unroll
-          for (int j = 0; j < R / 4; ++j)
-            st_async_v4(dst + j * 16,
-                        make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                    __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])),
-                        bar);
-        }
-        ok = warp_wait(sm, &sm.rs_full, it & 1, lane);
-        if (!ok) break;
-        // ---- sum the C partials of the owned rows (fixed order: the same v in
-        // every CTA), split into hi / lo and all-gather into every CTA's operand
-        for (int w = tid; w < rpo * (R / 8); w += kTcEpiThreads) {
-          const int lr = w / (R / 8), j = w - lr * (R / 8);
-          float f[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = 0.f;
-          for (int src = 0; src < C; ++src) {
-            const float4* pp = reinterpret_cast<const float4*>(&sm.rbuf[(src * rpo + lr) * R + j * 8]);
-            const float4 u0 = pp[0], u1 = pp[1];
-            f[0] += u0.x;
-            f[1] += u0.y;
-            f[2] += u0.z;
-            f[3] += u0.w;
-            f[4] += u1.x;
-            f[5] += u1.y;
-            f[6] += u1.z;
-            f[7] += u1.w;
-          }
-          uint32_t hi[4], lo[4];
-          split_hl(f, hi, lo);
-          const uint32_t mrow = static_cast<uint32_t>(crank * rpo + lr) * (R * 2) + j * 16;
-          const uint32_t ha = swz<Cfg::kSwM>(smem_u32(sm.vop[0]) + mrow);
-          const uint32_t la = swz<Cfg::kSwM>(smem_u32(sm.vop[1]) + mrow);
-          const uint32_t bar = smem_u32(&sm.vop_ready);
-          for (int d = 0; d < C; ++d) {
-            const uint32_t rb = mapa_shared(bar, d);
-            st_async_u4(mapa_shared(ha, d), hi[0], hi[1], hi[2], hi[3], rb);
-            st_async_u4(mapa_shared(la, d), lo[0], lo[1], lo[2], lo[3], rb);
-          }
-        }
-        // the whole operand is here before the next item's expectations are
-        // registered (and the expand MMAs of this item may start)
-        ok = warp_wait(sm, &sm.vop_ready, it & 1, lane);
-        if (!ok) break;
-      }
-      }  // eg == 0
-      // ---- expand blocks: y = bf16(y + s * acc)
-      const int c0 = ch * pr.chunk;
-      int b0, b1;
-      split((min(pr.chunk, pr.h_out - c0) + kBN - 1) / kBN, b0, b1);
-      const int full_rows = (tlen >> 5) << 5;
-      for (int b = b0; b < b1 && ok; ++b) {
-        const int buf = ae & 1;
-        ok = warp_wait(sm, &sm.acc_full[buf], (ae >> 1) & 1, lane);
-        if (!ok) break;
-        tc_fence_after();
-        uint8_t* st = sm.ex[xslot];
-        const int c = c0 + b * kBN;
-        {
-          // this group's 32 columns of the block
-          uint32_t acc[32];
-          tmem_ld32(tq + kTmemAcc + buf * kBN + eg * 32, acc);
-          tmem_ld_wait();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.acc_empty[buf]);  // accumulator in registers: TMEM buffer free
-          const uint32_t rbase = smem_u32(st) + static_cast<uint32_t>(m) * 128;
+          if (lane == 0) mbar_arrive(&sm.v_read);  // TMEM v may take the next item's shrink
+        } else {
+          // ---- v from device memory (expand mode), fp32 rows in token order
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int j = eg * 4 + i;  // 16-byte chunk of the 64-column block
-            const uint32_t addr = rbase + ((static_cast<uint32_t>(j) ^ (m & 7u)) << 4);
-            uint32_t yw[4];
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(yw[0]), "=r"(yw[1]), "=r"(yw[2]), "=r"(yw[3])
-                         : "r"(addr));
+          for (int i = 0; i < RP; ++i) v[i] = 0u;
+          if (yrow >= 0) {
+            const float4* src = reinterpret_cast<const float4*>(q.v_in + static_cast<int64_t>(yrow) * R);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 yf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&yw[e]));
-              const __nv_bfloat162 o = __floats2bfloat162_rn(yf.x + scale * __uint_as_float(acc[i * 8 + 2 * e]),
-                                                             yf.y + scale * __uint_as_float(acc[i * 8 + 2 * e + 1]));
-              yw[e] = *reinterpret_cast<const uint32_t*>(&o);
+            for (int j = 0; j < R / 4; ++j) {
+              const float4 u = src[j];
+              v[4 * j] = __float_as_uint(u.x);
+              v[4 * j + 1] = __float_as_uint(u.y);
+              v[4 * j + 2] = __float_as_uint(u.z);
+              v[4 * j + 3] = __float_as_uint(u.w);
             }
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(yw[0]), "r"(yw[1]), "r"(yw[2]),
-                         "r"(yw[3])
-                         : "memory");
           }
         }
-        // rows past the last whole group of 32: written directly (16-byte stores)
-        if (m >= full_rows && m < tlen) {
-          uint16_t* yrow = pr.y + static_cast<int64_t>(row + m) * pr.ldy;
-#pragma unroll 1
-          for (int j = eg * 4; j < eg * 4 + 4; ++j) {
-            const int col = c + j * 8;
-            if (col < pr.h_out) {
-              const uint32_t addr =
-                  smem_u32(st) + static_cast<uint32_t>(m) * 128 + ((static_cast<uint32_t>(j) ^ (m & 7u)) << 4);
-              uint4 w;
+        if constexpr (!kHasExpand) {
+          // ---- shrink mode: v rows to device memory (fp32, token order)
+          if (yrow >= 0) {
+            float4* dst = reinterpret_cast<float4*>(q.v_out + static_cast<int64_t>(yrow) * R);
+#pragma unroll
+            for (int j = 0; j < R / 4; ++j)
+              dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                   __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+          }
+          ++it;
+          continue;
+        } else if constexpr (!CL) {
+          // ---- v -> bf16 operands hi, lo (K-major, 2*RP-byte swizzle)
+          put_operand_row(v);
+          fence_proxy_async_smem();  // the tensor core reads the operands through the async proxy
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.vop_ready);
+        } else {
+          // ---- reduce-scatter: row m's partial to the CTA that owns the row
+          const int rpo = 128 / C;  // rows per owner
+          const int own = m / rpo, ml = m - own * rpo;
+          if (tid == 0) {
+            mbar_arrive_expect_tx(&sm.rs_full, 128u * R * 4u);    // C ranks x rpo rows x r fp32
+            mbar_arrive_expect_tx(&sm.vop_ready, 128u * R * 4u);  // 128 rows x r x (hi + lo) bf16
+          }
+          {
+            const uint32_t dst = mapa_shared(smem_u32(&sm.rbuf[(crank * rpo + ml) * R]), own);
+            const uint32_t bar = mapa_shared(smem_u32(&sm.rs_full), own);
+#pragma unroll
+            for (int j = 0; j < R / 4; ++j)
+              st_async_v4(dst + j * 16,
+                          make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                      __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])),
+                          bar);
+          }
+          ok = warp_wait(sm, &sm.rs_full, it & 1, lane);
+          if (!ok) break;
+          // ---- sum the C partials of the owned rows (fixed order: the same v in
+          // every CTA), split into hi / lo and all-gather into every CTA's operand
+          for (int w = tid; w < rpo * (R / 8); w += kTcEpiThreads) {
+            const int lr = w / (R / 8), j = w - lr * (R / 8);
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = 0.f;
+            for (int src = 0; src < C; ++src) {
+              const float4* pp = reinterpret_cast<const float4*>(&sm.rbuf[(src * rpo + lr) * R + j * 8]);
+              const float4 u0 = pp[0], u1 = pp[1];
+              f[0] += u0.x;
+              f[1] += u0.y;
+              f[2] += u0.z;
+              f[3] += u0.w;
+              f[4] += u1.x;
+              f[5] += u1.y;
+              f[6] += u1.z;
+              f[7] += u1.w;
+            }
+            uint32_t hi[4], lo[4];
+            split_hl(f, hi, lo);
+            const uint32_t mrow = static_cast<uint32_t>(crank * rpo + lr) * (RP * 2) + j * 16;
+            const uint32_t ha = swz<Cfg::kSwM>(smem_u32(sm.vop[0]) + mrow);
+            const uint32_t la = swz<Cfg::kSwM>(smem_u32(sm.vop[1]) + mrow);
+            const uint32_t bar = smem_u32(&sm.vop_ready);
+            for (int d = 0; d < C; ++d) {
+              const uint32_t rb = mapa_shared(bar, d);
+              st_async_u4(mapa_shared(ha, d), hi[0], hi[1], hi[2], hi[3], rb);
+              st_async_u4(mapa_shared(la, d), lo[0], lo[1], lo[2], lo[3], rb);
+            }
+          }
+          // the whole operand is here before the next item's expectations are
+          // registered (and the expand MMAs of this item may start)
+          ok = warp_wait(sm, &sm.vop_ready, it & 1, lane);
+          if (!ok) break;
+        }
+      }  // eg == 0
+      if constexpr (kHasExpand) {
+        // ---- expand blocks: y = bf16(y + s * acc)
+        const int c0 = ch * pr.chunk;
+        int b0, b1;
+        split((min(pr.chunk, pr.h_out - c0) + kBN - 1) / kBN, b0, b1);
+        const bool contig = t.row >= 0;
+        const int full_rows = contig ? (t.tlen >> 5) << 5 : 0;  // rows stored by TMA boxes
+        for (int b = b0; b < b1 && ok; ++b) {
+          const int buf = ae & 1;
+          ok = warp_wait(sm, &sm.acc_full[buf], (ae >> 1) & 1, lane);
+          if (!ok) break;
+          tc_fence_after();
+          uint8_t* st = sm.ex[xslot];
+          const int c = c0 + b * kBN;
+          {
+            // this group's 32 columns of the block
+            uint32_t acc[32];
+            tmem_ld32(tq + kTmemAcc + buf * kBN + eg * 32, acc);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.acc_empty[buf]);  // accumulator in registers: TMEM buffer free
+            const uint32_t rbase = smem_u32(st) + static_cast<uint32_t>(m) * 128;
+            uint16_t* yp = yrow >= 0 ? pr.y + static_cast<int64_t>(yrow) * pr.ldy : nullptr;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int j = eg * 4 + i;  // 16-byte chunk of the 64-column block
+              const uint32_t addr = rbase + ((static_cast<uint32_t>(j) ^ (m & 7u)) << 4);
+              uint32_t yw[4];
               asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                           : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                           : "=r"(yw[0]), "=r"(yw[1]), "=r"(yw[2]), "=r"(yw[3])
                            : "r"(addr));
-              *reinterpret_cast<uint4*>(yrow + col) = w;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 yf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&yw[e]));
+                const __nv_bfloat162 o =
+                    __floats2bfloat162_rn(yf.x + scale * __uint_as_float(acc[i * 8 + 2 * e]),
+                                          yf.y + scale * __uint_as_float(acc[i * 8 + 2 * e + 1]));
+                yw[e] = *reinterpret_cast<const uint32_t*>(&o);
+              }
+              if (m < full_rows) {
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(yw[0]), "r"(yw[1]),
+                             "r"(yw[2]), "r"(yw[3])
+                             : "memory");
+              } else if (yp != nullptr && c + j * 8 < pr.h_out) {
+                // rows past the last whole group of 32, and every row of a gathered
+                // tile: written directly (16-byte stores)
+                *reinterpret_cast<uint4*>(yp + c + j * 8) = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+              }
             }
           }
-        }
-        fence_proxy_async_smem();  // our y updates, visible to the tensor stores
-        named_bar_sync(3 + wq, 64);  // the two warps of this lane quarter are done with the block
-        if (eg == 0 && lane == 0) {
-          // each lane quarter stores its own 32 rows (one 64-column box)
-          const int g = wq * 32;
-          if (g + 32 <= full_rows && c < pr.h_out) tma_store_2d(&p.tmYs[pj], c, row + g, st + g * 128);
-          bulk_commit();
-          // the previous block's stores have read their slot (this block's may
-          // still be reading): this quarter's share of that slot goes back
-          if (pend >= 0) {
-            bulk_wait_read1();
-            mbar_arrive(&sm.ex_empty[pend]);  // y rows read by the stores, B tile read by the MMAs
+          fence_proxy_async_smem();  // our y updates, visible to the tensor stores
+          named_bar_sync(3 + wq, 64);  // the two warps of this lane quarter are done with the block
+          if (eg == 0 && lane == 0) {
+            // each lane quarter stores its own 32 rows (one 64-column box)
+            const int g = wq * 32;
+            if (g + 32 <= full_rows && c < pr.h_out) tma_store_2d(&p.tmYs[pj], c, t.row + g, st + g * 128);
+            bulk_commit();
+            // the previous block's stores have read their slot (this block's may
+            // still be reading): this quarter's share of that slot goes back
+            if (pend >= 0) {
+              bulk_wait_read1();
+              mbar_arrive(&sm.ex_empty[pend]);  // y rows read by the stores, B tile read by the MMAs
+            }
+            pend = xslot;
           }
-          pend = xslot;
-        }
-        ++ae;
-        if (++xslot == kEx) {
-          xslot = 0;
-          xph ^= 1u;
+          ++ae;
+          if (++xslot == kEx) {
+            xslot = 0;
+            xph ^= 1u;
+          }
         }
       }
       if (!ok || sm.abort) break;
@@ -731,10 +846,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
 
 namespace {
 
-// Co-resident CTA groups of C CTAs (one CTA per SM) of the rank-R kernel on
+// Co-resident CTA groups of C CTAs (one CTA per SM) of a kernel instance on
 // the current device (clusters of C when CL); sets the kernel's shared-memory
 // attribute on first use.
-template <int R, bool CL>
+template <int R, bool CL, int MODE>
 lora_status tc_groups(int C, int& groups) {
   static std::mutex mu;
   static int cache[64][kMaxC + 1];
@@ -745,7 +860,7 @@ lora_status tc_groups(int C, int& groups) {
     groups = cache[dev & 63][C];
   }
   if (groups > 0) return LORA_OK;
-  auto kern = sgmv_tc_kernel<R, CL>;
+  auto kern = sgmv_tc_kernel<R, CL, MODE>;
   const size_t smem = sizeof(TcSmem<R, CL>);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
@@ -772,44 +887,45 @@ lora_status tc_groups(int C, int& groups) {
   return LORA_OK;
 }
 
-template <int R, bool CL>
+template <int R, bool CL, int MODE>
 lora_status launch_tc_rc(TcParams& prm, const SgmvCall& call, int tiles_bound, cudaStream_t stream) {
-  auto kern = sgmv_tc_kernel<R, CL>;
+  constexpr bool kHasShrink = (MODE & kModeShrink) != 0;
+  constexpr bool kHasExpand = (MODE & kModeExpand) != 0;
+  auto kern = sgmv_tc_kernel<R, CL, MODE>;
   const size_t smem = sizeof(TcSmem<R, CL>);
   const int C = prm.t.csplit;
+  const uint64_t n = static_cast<uint64_t>(call.seg.n_tokens);
   for (int i = 0; i < call.n_proj; ++i) {
     const ProjArgs& a = call.proj[i];
     lora_status s;
-    {
-      const uint64_t dims[2] = {static_cast<uint64_t>(a.h_in), static_cast<uint64_t>(call.seg.n_tokens)};
+    if (kHasShrink) {
+      const uint64_t dims[2] = {static_cast<uint64_t>(a.h_in), n};
       const uint64_t str[1] = {static_cast<uint64_t>(a.ldx) * 2};
-      const uint32_t box[2] = {64, 128};
+      const uint32_t box[2] = {64, 128}, box_g[2] = {64, 1};
       if ((s = encode_tmap_bf16(&prm.tmX[i], a.x, 2, dims, str, box, 128)) != LORA_OK) return s;
+      if ((s = encode_tmap_bf16(&prm.tmXg[i], a.x, 2, dims, str, box_g, 128)) != LORA_OK) return s;
+      const uint64_t adims[3] = {static_cast<uint64_t>(R), static_cast<uint64_t>(a.h_in),
+                                 static_cast<uint64_t>(prm.t.n_slabs)};
+      const uint64_t astr[2] = {static_cast<uint64_t>(R) * 2, static_cast<uint64_t>(a.h_in) * prm.t.rmax * 2};
+      const uint32_t abox[3] = {static_cast<uint32_t>(R), 64, 1};
+      if ((s = encode_tmap_bf16(&prm.tmA[i], a.A, 3, adims, astr, abox, R >= 16 ? R * 2 : 0)) != LORA_OK) return s;
     }
-    {
-      const uint64_t dims[3] = {static_cast<uint64_t>(R), static_cast<uint64_t>(a.h_in),
-                                static_cast<uint64_t>(prm.t.n_slabs)};
-      const uint64_t str[2] = {static_cast<uint64_t>(R) * 2, static_cast<uint64_t>(a.h_in) * prm.t.rmax * 2};
-      const uint32_t box[3] = {static_cast<uint32_t>(R), 64, 1};
-      if ((s = encode_tmap_bf16(&prm.tmA[i], a.A, 3, dims, str, box, R * 2)) != LORA_OK) return s;
-    }
-    {
-      const uint64_t dims[2] = {static_cast<uint64_t>(a.h_out), static_cast<uint64_t>(prm.t.n_slabs) * prm.t.rmax};
-      const uint64_t str[1] = {static_cast<uint64_t>(a.h_out) * 2};
-      const uint32_t box[2] = {64, static_cast<uint32_t>(R)};
-      if ((s = encode_tmap_bf16(&prm.tmB[i], a.B, 2, dims, str, box, 128)) != LORA_OK) return s;
-    }
-    {
-      const uint64_t dims[2] = {static_cast<uint64_t>(a.h_out), static_cast<uint64_t>(call.seg.n_tokens)};
+    if (kHasExpand) {
+      const uint64_t bdims[2] = {static_cast<uint64_t>(a.h_out), static_cast<uint64_t>(prm.t.n_slabs) * prm.t.rmax};
+      const uint64_t bstr[1] = {static_cast<uint64_t>(a.h_out) * 2};
+      const uint32_t bbox[2] = {64, static_cast<uint32_t>(R)};
+      if ((s = encode_tmap_bf16(&prm.tmB[i], a.B, 2, bdims, bstr, bbox, 128)) != LORA_OK) return s;
+      const uint64_t dims[2] = {static_cast<uint64_t>(a.h_out), n};
       const uint64_t str[1] = {static_cast<uint64_t>(a.ldy) * 2};
-      const uint32_t box_l[2] = {64, 128}, box_s[2] = {64, 32};
+      const uint32_t box_l[2] = {64, 128}, box_g[2] = {64, 1}, box_s[2] = {64, 32};
       if ((s = encode_tmap_bf16(&prm.tmYl[i], a.y, 2, dims, str, box_l, 128)) != LORA_OK) return s;
+      if ((s = encode_tmap_bf16(&prm.tmYg[i], a.y, 2, dims, str, box_g, 128)) != LORA_OK) return s;
       if ((s = encode_tmap_bf16(&prm.tmYs[i], a.y, 2, dims, str, box_s, 128)) != LORA_OK) return s;
     }
   }
 
   int max_groups = 0;
-  if (const lora_status st = tc_groups<R, CL>(C, max_groups); st != LORA_OK) return st;
+  if (const lora_status st = tc_groups<R, CL, MODE>(C, max_groups); st != LORA_OK) return st;
   const int64_t items = static_cast<int64_t>(tiles_bound) * prm.t.ipt;
   const int groups = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(max_groups, items)));
 
@@ -840,35 +956,46 @@ lora_status launch_tc_rc(TcParams& prm, const SgmvCall& call, int tiles_bound, c
 // for one round of items over the co-resident groups (at least one chunk of
 // about kChunkCols columns per projection; each extra chunk re-reads the
 // tile's x and the A slab for its own shrink); the plan with the fewest bytes
-// per CTA over all rounds wins (ties: the smaller C).
-template <int R>
+// per CTA over all rounds wins (ties: the smaller C).  The shrink and expand
+// modes run one CTA per item; the shrink mode has one item per tile.
+template <int R, int MODE>
 lora_status plan_and_launch(const SgmvCall& call, cudaStream_t stream) {
+  constexpr bool kHasShrink = (MODE & kModeShrink) != 0;
+  constexpr bool kHasExpand = (MODE & kModeExpand) != 0;
   TcParams prm{};
   const int n = call.seg.n_tokens;
   const int tiles_est = std::max(1, ceil_div(n, 128));
   int64_t cols = 0;
   int min_kb = 1 << 30;
   for (int i = 0; i < call.n_proj; ++i) {
-    cols += call.proj[i].h_out;
-    min_kb = std::min(min_kb, ceil_div(call.proj[i].h_in, 64));
+    cols += kHasExpand ? call.proj[i].h_out : 0;
+    if (kHasShrink) min_kb = std::min(min_kb, ceil_div(call.proj[i].h_in, 64));
   }
   struct Plan {
     int C = 0, nch[kMaxProj] = {}, ipt = 0;
     double cost = 0;
   } best;
-  for (int C = 1; C <= kMaxC && C <= min_kb; C *= 2) {
+  const int c_max = MODE == kModeFused ? kMaxC : 1;
+  for (int C = 1; C <= c_max && C <= min_kb; C *= 2) {
     int G = 0;
-    const lora_status st = C == 1 ? tc_groups<R, false>(1, G) : tc_groups<R, true>(C, G);
+    const lora_status st = C == 1 ? tc_groups<R, false, MODE>(1, G) : tc_groups<R, (MODE == kModeFused), MODE>(C, G);
     if (st != LORA_OK) return st;
     const int target = std::clamp(G / tiles_est, 1, kMaxItemsPerTile);  // items per tile
     Plan pl;
     pl.C = C;
     int base = 0;
-    for (int i = 0; i < call.n_proj; ++i) base += std::clamp(ceil_div(call.proj[i].h_out, kChunkCols), 1, 8);
+    for (int i = 0; i < call.n_proj; ++i)
+      base += kHasExpand ? std::clamp(ceil_div(call.proj[i].h_out, kChunkCols), 1, 8) : 1;
     bool ok = true;
     double bytes = 0;
     for (int i = 0; i < call.n_proj && ok; ++i) {
       const ProjArgs& a = call.proj[i];
+      if (!kHasExpand) {
+        pl.nch[i] = 1;
+        pl.ipt += 1;
+        bytes += 128.0 * a.h_in * 2 + a.h_in * R * 2;
+        continue;
+      }
       int nch = std::clamp(ceil_div(a.h_out, kChunkCols), 1, 8);
       if (base < target) {
         const int share = static_cast<int>((static_cast<int64_t>(target) * a.h_out + cols - 1) / cols);
@@ -881,7 +1008,7 @@ lora_status plan_and_launch(const SgmvCall& call, cudaStream_t stream) {
       pl.ipt += nch;
       // every CTA of a cluster needs an expand block of every item
       if (ceil_div(a.h_out - (nch - 1) * chunk, kBN) < C) ok = false;
-      bytes += static_cast<double>(nch) * (128.0 * a.h_in * 2 + a.h_in * R * 2) +
+      bytes += static_cast<double>(nch) * (kHasShrink ? 128.0 * a.h_in * 2 + a.h_in * R * 2 : 128.0 * R * 4) +
                static_cast<double>(a.h_out) * (128 * 4 + R * 2);
     }
     if (!ok) continue;
@@ -900,7 +1027,7 @@ lora_status plan_and_launch(const SgmvCall& call, cudaStream_t stream) {
     t.h_in = a.h_in;
     t.h_out = a.h_out;
     t.scale = a.scale;
-    t.chunk = round_up(ceil_div(a.h_out, best.nch[i]), 128);
+    t.chunk = kHasExpand ? round_up(ceil_div(a.h_out, best.nch[i]), 128) : 0;
     for (int c = 0; c < best.nch[i]; ++c) {
       prm.t.item_proj[ipt] = static_cast<int8_t>(i);
       prm.t.item_chunk[ipt] = static_cast<int8_t>(c);
@@ -918,6 +1045,8 @@ lora_status plan_and_launch(const SgmvCall& call, cudaStream_t stream) {
   prm.t.seg_adapter = call.seg.seg_adapter;
   prm.t.num_segments = call.seg.num_segments;
   prm.t.err_flag = call.err_flag;
+  prm.t.v_out = call.v_out;
+  prm.t.v_in = call.v_in;
   prm.t.n_proj = call.n_proj;
   prm.t.ipt = ipt;
   prm.t.n_tokens = n;
@@ -925,8 +1054,19 @@ lora_status plan_and_launch(const SgmvCall& call, cudaStream_t stream) {
   prm.t.n_adapters = call.n_adapters;
   // upper bound of the tiles of segments of at least kLongSeg tokens
   const int tiles_bound = ceil_div(n, 128) + n / kLongSeg;
-  if (best.C > 1) return launch_tc_rc<R, true>(prm, call, tiles_bound, stream);
-  return launch_tc_rc<R, false>(prm, call, tiles_bound, stream);
+  if constexpr (MODE == kModeFused) {
+    if (best.C > 1) return launch_tc_rc<R, true, MODE>(prm, call, tiles_bound, stream);
+  }
+  return launch_tc_rc<R, false, MODE>(prm, call, tiles_bound, stream);
+}
+
+template <int R>
+lora_status launch_mode(const SgmvCall& call, cudaStream_t stream) {
+  switch (call.mode) {
+    case kModeShrink: return plan_and_launch<R, kModeShrink>(call, stream);
+    case kModeExpand: return plan_and_launch<R, kModeExpand>(call, stream);
+    default: return plan_and_launch<R, kModeFused>(call, stream);
+  }
 }
 
 }  // namespace
@@ -940,15 +1080,16 @@ constexpr int kTcMinTokens = 512;
 bool sgmv_tc_applicable(const SgmvCall& call) {
   const int n = call.seg.n_tokens;
   const int max_seg = std::max(1, std::min(n, call.n_adapters));
-  return call.mode == kModeFused && (call.r == 16 || call.r == 32 || call.r == 64) && n >= kLongSeg &&
+  return (call.r == 8 || call.r == 16 || call.r == 32 || call.r == 64) && n >= kLongSeg &&
          (n / max_seg >= kLongSeg || n >= kTcMinTokens);
 }
 
 lora_status launch_sgmv_tc(const SgmvCall& call, cudaStream_t stream) {
   switch (call.r) {
-    case 16: return plan_and_launch<16>(call, stream);
-    case 32: return plan_and_launch<32>(call, stream);
-    case 64: return plan_and_launch<64>(call, stream);
+    case 8: return launch_mode<8>(call, stream);
+    case 16: return launch_mode<16>(call, stream);
+    case 32: return launch_mode<32>(call, stream);
+    case 64: return launch_mode<64>(call, stream);
     default: return LORA_ERR_UNSUPPORTED;
   }
 }

@@ -28,7 +28,7 @@ STATUS = {
 SYMBOLS = ("lora_status_str", "lora_abi_version", "lora_segment_workspace_bytes", "lora_segment",
            "lora_segment_noalloc", "sgmv_shrink", "sgmv_expand", "sgmv_fused", "sgmv_multi", "sgmv_multi_slots",
            "lora_slot_copy", "lora_slot_assign", "sgmv_multi_host_workspace_bytes", "sgmv_multi_host",
-           "sgmv_multi_segment")
+           "sgmv_multi_segment", "gemm_lora_workspace_bytes", "gemm_lora")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -90,6 +90,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sgmv_multi_host.argtypes = [ctypes.POINTER(LoraProj), i32, i32, i32, p, i32, p, sz, p, p]
     lib.sgmv_multi_segment.restype = ctypes.c_int
     lib.sgmv_multi_segment.argtypes = [ctypes.POINTER(LoraProj), i32, i32, i32, p, i32, p, p, p, p, p, sz, p, p]
+    lib.gemm_lora_workspace_bytes.restype = sz
+    lib.gemm_lora_workspace_bytes.argtypes = [i32, i32]
+    lib.gemm_lora.restype = ctypes.c_int
+    lib.gemm_lora.argtypes = [p, i64, p, p, p, i32, i32, i32, i32, ctypes.c_float, ctypes.POINTER(LoraSegments), p,
+                              i64, p, sz, p, p]
     lib.lora_slot_copy.restype = ctypes.c_int
     lib.lora_slot_copy.argtypes = [ctypes.POINTER(LoraSlotSrc), i32, i32, i32, i32, i32, p]
     lib.lora_slot_assign.restype = ctypes.c_int
@@ -479,3 +484,32 @@ def sgmv_fused_segment(x: torch.Tensor, A_pool: torch.Tensor, B_pool: torch.Tens
     """One projection of sgmv_multi_segment (y updated in place)."""
     return sgmv_multi_segment([(x, A_pool, B_pool, y, scale)], ids, A_pool.shape[0], out=out, err_flag=err_flag,
                               stream=stream)
+
+
+def gemm_lora_workspace_bytes(n_tokens: int, r: int) -> int:
+    return int(load_library().gemm_lora_workspace_bytes(int(n_tokens), int(r)))
+
+
+def gemm_lora(x: torch.Tensor, W: torch.Tensor, A_pool: torch.Tensor, B_pool: torch.Tensor, seg: Segments,
+              y: torch.Tensor, scale: float, *, workspace: Optional[torch.Tensor] = None,
+              err_flag: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """y = x . W + scale * (x . A[a_i]) . B[a_i] with the expand fused into the
+    backbone GEMM (y written, not accumulated).  W: [h_in, h_out] bf16."""
+    lib = load_library()
+    _req(x, "x", torch.bfloat16, 2)
+    _req(y, "y", torch.bfloat16, 2)
+    _req(W, "W", torch.bfloat16, 2)
+    _pool(A_pool, "A_pool")
+    _pool(B_pool, "B_pool")
+    P, h_in, r = A_pool.shape
+    if tuple(W.shape) != (h_in, y.shape[1]) or not W.is_contiguous():
+        raise ValueError("W must be a contiguous [h_in, h_out] tensor")
+    if x.shape[1] != h_in or B_pool.shape != (P, r, y.shape[1]):
+        raise ValueError("shape mismatch")
+    need = gemm_lora_workspace_bytes(x.shape[0], r)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    _check(lib.gemm_lora(_ptr(x), _rows(x, "x"), _ptr(W), _ptr(A_pool), _ptr(B_pool), P, h_in, y.shape[1], r,
+                         float(scale), ctypes.byref(seg.c_struct), _ptr(y), _rows(y, "y"), _ptr(workspace),
+                         workspace.numel() * workspace.element_size(), _ptr(err_flag), _stream(stream)), "gemm_lora")
+    return y

@@ -108,6 +108,18 @@ def n_copies(step_bytes: int, max_copies: int) -> int:
     return max(2, min(max_copies, int(np.ceil(2.2 * L2_BYTES / step_bytes))))
 
 
+def bf16_peaks():
+    """(sustained, burst) dense bf16 TFLOP/s from MEASURED_PEAKS.json, else the
+    fallback figures (1400, 1800)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops_sustained"]), float(d["bf16_tflops"])
+    except Exception:
+        return 1400.0, 1800.0
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -485,6 +497,8 @@ def run_ours(args) -> None:
         out["per_config"] = per_config(K, Wm, dev, lsg, args.max_copies, peak)
     if not args.no_batch_curve and world == 1:
         out["batch_curve_us"] = batch_curve(K, Wm, dev, lsg, args.max_copies)
+    if not args.no_backbone and world == 1:
+        out["backbone_fused"] = backbone_fused(Wm, dev, lsg, bf16_peaks())
     if not args.no_slots and world == 1:
         out["slot_pool_us"] = slots_measure(K, Wm, dev, lsg, args.max_copies, peak)
         out["pool_loader"] = pool_loader_measure(g_step, K, dev, lsg)
@@ -726,7 +740,8 @@ def pool_loader_measure(g_step, K, dev, lsg, n_layers=32, reps=5):
                    "table entry; CUDA events on the loader and compute streams"}
 
 
-PER_CONFIG = ("7b_layer", "13b_prefill", "70b_decode_r8", "70b_decode_r16", "70b_decode_r32", "70b_decode_r64")
+PER_CONFIG = ("7b_layer", "13b_prefill", "13b_prefill_interleaved", "70b_decode_r8", "70b_decode_r16",
+              "70b_decode_r32", "70b_decode_r64")
 
 
 def per_config(K, Wm, dev, lsg, max_copies, peak):
@@ -794,6 +809,73 @@ def per_config(K, Wm, dev, lsg, max_copies, peak):
     return out
 
 
+def backbone_fused(Wm, dev, lsg, bf16_peaks):
+    """The Llama2-13B prefill layer (7 projections, 6224 tokens, r=64) with
+    synthetic backbone weights W: the backbone projection with its LoRA delta
+    as gemm_lora (the expand fused into the GEMM's accumulator, y written
+    once; one call per projection), against cuBLAS x @ W per projection
+    followed by one sgmv_multi for the layer.  Segmentation given (computed
+    once).  TFLOP/s count 2*n*h_in*h_out per projection plus the LoRA flops."""
+    import torch
+    from workloads import make_backbone_weights
+
+    wl = WORKLOADS["13b_prefill"]
+    ids = wl.ids()
+    inp = make_inputs(wl, dev)
+    Ws = make_backbone_weights(wl, dev)
+    seg = lsg.lora_segment(inp.ids, wl.P)
+    n = wl.n
+    ys = [torch.empty(n, p.h_out, dtype=torch.bfloat16, device=dev) for p in wl.projs]
+    ws = torch.empty(lsg.gemm_lora_workspace_bytes(n, wl.r), dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    projs = [(inp.x[p.x_key], inp.A[i], inp.B[i], ys[i], wl.scale) for i, p in enumerate(wl.projs)]
+    cproj = lsg.make_projs(projs)
+
+    def fused():
+        for i, p in enumerate(wl.projs):
+            lsg.gemm_lora(inp.x[p.x_key], Ws[i], inp.A[i], inp.B[i], seg, ys[i], wl.scale, workspace=ws,
+                          err_flag=err)
+
+    def unfused():
+        for i, p in enumerate(wl.projs):
+            torch.matmul(inp.x[p.x_key], Ws[i], out=ys[i])
+        lsg.sgmv_multi(projs, seg, err_flag=err, c_projs=cproj)
+
+    def gemm_only():
+        for i, p in enumerate(wl.projs):
+            torch.matmul(inp.x[p.x_key], Ws[i], out=ys[i])
+
+    side = torch.cuda.Stream(dev)
+    out = {"workload": wl.description + "; synthetic W ~ N(0, 1/h_in) per projection",
+           "how": "CUDA graph of 3 layer passes, median of 5 replays (events on the replay stream)"}
+    gemm_flops = sum(2 * n * p.h_in * p.h_out for p in wl.projs)
+    lora_flops = flops(wl, ids)
+    reps = 3
+    for name, fn in (("fused_gemm_lora", fused), ("cublas_gemm_then_sgmv_multi", unfused),
+                     ("cublas_gemm_alone", gemm_only)):
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(max(1, Wm // 2)):
+                fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for _ in range(reps):
+                fn()
+        ms = _time_graph_median(g, side, reps=5, settle_s=0.3)[0] / reps
+        del g
+        f = gemm_flops + (0 if name == "cublas_gemm_alone" else lora_flops)
+        tf = f / (ms * 1e-3) / 1e12
+        out[name] = {"us": round(ms * 1e3, 1), "tflops": round(tf, 1),
+                     "frac_of_bf16_sustained": round(tf / bf16_peaks[0], 4) if bf16_peaks[0] else None,
+                     "frac_of_bf16_burst": round(tf / bf16_peaks[1], 4) if bf16_peaks[1] else None}
+    assert int(err.item()) == 0, f"device error flag {int(err.item())}"
+    out["fused_over_unfused"] = round(out["fused_gemm_lora"]["us"] / out["cublas_gemm_then_sgmv_multi"]["us"], 4)
+    del inp, Ws, ys, ws
+    torch.cuda.empty_cache()
+    return out
+
+
 def batch_curve(K, Wm, dev, lsg, max_copies):
     """Step latency against batch size, identical vs mixed adapters, for a
     decode projection (Llama2-7B 4096->4096, r=16) and a prefill projection
@@ -845,6 +927,8 @@ def main(argv=None):
                     help="time cap of the reference arm's timed calls")
     ap.add_argument("--no-batch-curve", action="store_true",
                     help="skip step latency against batch size (decode and prefill, identical vs mixed adapters)")
+    ap.add_argument("--no-backbone", action="store_true",
+                    help="skip the backbone GEMM with the fused LoRA expand against cuBLAS + SGMV")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the per-workload kernel times of the 7B layer, 13B prefill and 70B decode batches")
     args = ap.parse_args(argv)

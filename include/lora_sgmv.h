@@ -229,6 +229,12 @@ LORA_API lora_status sgmv_multi(const lora_proj* projs, int32_t n_proj, int32_t 
  * lora_segment's kernel first (with `workspace`, sized as
  * lora_segment_workspace_bytes says) and then the SGMV kernels.  Errors: as
  * lora_segment and sgmv_multi.
+ * Ordering: a one-launch step reads `ids` and the adapter pools while the
+ * preceding kernel in the stream may still be running (programmatic dependent
+ * launch); it reads x and y, and writes anything, only after that kernel has
+ * completed.  So ids and pools must not be written by a preceding kernel that
+ * lets its dependents start early (griddepcontrol.launch_dependents) before
+ * it writes them; copies and ordinary kernels are waited for in full.
  */
 LORA_API lora_status sgmv_multi_segment(const lora_proj* projs, int32_t n_proj, int32_t n_adapters, int32_t r,
                                         const int32_t* ids, int32_t n_tokens, int32_t* perm, int32_t* seg_offsets,
@@ -255,6 +261,38 @@ LORA_API size_t sgmv_multi_host_workspace_bytes(const lora_proj* projs, int32_t 
 LORA_API lora_status sgmv_multi_host(const lora_proj* projs, int32_t n_proj, int32_t n_adapters, int32_t r,
                                      const int32_t* ids_host, int32_t n_tokens, void* workspace,
                                      size_t workspace_bytes, int32_t* err_flag, lora_stream_t stream);
+
+/*
+ * The backbone projection with the LoRA delta, y written once:
+ *
+ *     y[i,:] = x[i,:] . W + s * ((x[i,:] . A[a_i]) . B[a_i])
+ *
+ * Punica: Multi-Tenant LoRA Serving (research.elamur.ai summary), "Summary":
+ * the backbone runs as one ordinary GEMM over the batch and the per-adapter
+ * low-rank additions are computed together; "Interesting ideas" I1: the
+ * shared and the per-tenant computation are split.  Here the expand of every
+ * segment of at least 64 tokens joins the GEMM's accumulator (tensor cores,
+ * fp32), so it adds no y read or write: a shrink launch writes v = x . A of
+ * those tokens to the workspace, the GEMM launch computes x . W + s * v . B
+ * for them and x . W for every other token and writes y, and the split-K
+ * SGMV launch then adds the delta of the shorter segments to y in place.
+ *   x [n][ldx], y [n][ldy] (written, not accumulated): as sgmv_fused.
+ *   W [h_in][h_out] row-major bf16 (device), shared by every token,
+ *     16-byte aligned.
+ *   A_pool, B_pool, seg, r: as sgmv_fused.
+ *   workspace: device memory of gemm_lora_workspace_bytes(n, r) bytes (v,
+ *     fp32 [n][r]), 16-byte aligned; contents on exit unspecified.
+ * A token whose adapter id is invalid (outside every segment) gets
+ * y = x . W; err_flag as for lora_segment.  Errors: as sgmv_fused, plus W
+ * NULL (LORA_ERR_INVALID_ARG) or misaligned, workspace missing or too small
+ * (LORA_ERR_WORKSPACE).  The product x . W is accumulated in fp32 in tile
+ * order (not the oracle's order); y is rounded to bf16 once.
+ */
+LORA_API size_t gemm_lora_workspace_bytes(int32_t n_tokens, int32_t r);
+LORA_API lora_status gemm_lora(const lora_bf16* x, int64_t ldx, const lora_bf16* W, const lora_bf16* A_pool,
+                               const lora_bf16* B_pool, int32_t n_adapters, int32_t h_in, int32_t h_out, int32_t r,
+                               float scale, const lora_segments* seg, lora_bf16* y, int64_t ldy, void* workspace,
+                               size_t workspace_bytes, int32_t* err_flag, lora_stream_t stream);
 
 /*
  * Slot tables: adapter pools stored as arenas of fixed-size slots, so that

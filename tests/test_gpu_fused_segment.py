@@ -43,6 +43,14 @@ CASES = {
     "prefill_long_segments": (np.repeat(np.array([1, 0], np.int32), [300, 200]), 2, 512, 640, 32),
     "all_invalid": (np.array([3, 3, -1, 7, 3], np.int32), 3, 256, 256, 16),
     "one_adapter_pool": (np.zeros(37, np.int32), 1, 512, 256, 32),
+    # up to 64 tokens the kernel ranks ids in registers: duplicates, invalid
+    # ids and both sizes of that path
+    "rank_sort_32_dups": (np.random.default_rng(5).integers(-1, 6, 32).astype(np.int32), 5, 256, 256, 16),
+    "rank_sort_33": (np.random.default_rng(6).integers(0, 9, 33).astype(np.int32), 9, 256, 256, 16),
+    "rank_sort_64_dups_invalid": (np.where(np.random.default_rng(7).random(64) < 0.1, 40,
+                                           np.random.default_rng(8).integers(0, 12, 64)).astype(np.int32),
+                                  12, 256, 512, 32),
+    "rank_sort_64_distinct": (np.random.default_rng(9).permutation(200)[:64].astype(np.int32), 200, 256, 256, 8),
 }
 
 

@@ -61,11 +61,13 @@ def test_7b_layer_all_projections():
         assert_within_tol(r.y(i), r.ref(i), p.name)
 
 
-def test_13b_prefill_every_row():
+@pytest.mark.parametrize("name", ["13b_prefill", "13b_prefill_interleaved"])
+def test_13b_prefill_every_row(name):
     """All 6224 rows of all seven projections against the oracle (the
     oracle's threaded entry point), plus an extra cross-check of every row
-    against fp32 torch.matmul."""
-    wl = WORKLOADS["13b_prefill"]
+    against fp32 torch.matmul; the requests sorted (contiguous rows) and
+    interleaved (every segment's rows gathered)."""
+    wl = WORKLOADS[name]
     r = Run(wl)
     check_segments(r.seg, r.ids, wl.P)
     assert int(r.err.cpu()[0]) == 0

@@ -1,8 +1,10 @@
-"""Long-segment (prefill) batches through sgmv_fused / sgmv_multi against the
-oracle.  Segments of at least 64 tokens whose rows are contiguous take the
-tensor-tile kernel; interleaved long segments and short ones take the
-split-K kernel in the same call, so these batches exercise the split of one
-batch between the two and the edges of the 128-token tiles."""
+"""Long-segment (prefill) batches through sgmv_fused / sgmv_multi /
+sgmv_shrink / sgmv_expand against the oracle.  Segments of at least 64 tokens
+take the tensor-tile kernel: contiguous ones by whole-tile tensor copies,
+interleaved ones (tokens of one adapter spread over the batch) by four-row
+gathers through the permutation; short segments take the split-K kernel in
+the same call, so these batches exercise the split of one batch between the
+two and the edges of the 128-token tiles."""
 
 import numpy as np
 import pytest
@@ -31,7 +33,7 @@ def _mixed_ids(rng):
     return np.concatenate(ids).astype(np.int32)
 
 
-@pytest.mark.parametrize("r", [16, 32, 64])
+@pytest.mark.parametrize("r", [8, 16, 32, 64])
 @pytest.mark.parametrize("h_in,h_out", [(520, 1000), (1024, 384), (136, 2056)])
 def test_mixed_long_short_interleaved(r, h_in, h_out):
     rng = np.random.default_rng(r * 1000 + h_in + h_out)
@@ -180,3 +182,89 @@ def test_many_items_take_one_cta_per_item():
     assert int(err.item()) == 0
     for i, ((A, B, y0), p) in enumerate(zip(refs, projs)):
         assert_within_tol(p[3], oracle_rows(x, A, B, ids, p[4], y0), f"projection {i}")
+
+
+def _interleaved_requests(rng, lens, adapters):
+    """Requests of the given lengths and adapters whose tokens are dealt out
+    round robin over the batch (no segment's rows are contiguous)."""
+    queues = [list(np.full(l, a, np.int32)) for l, a in zip(lens, adapters)]
+    ids = []
+    while any(queues):
+        for qu in queues:
+            if qu:
+                ids.append(qu.pop())
+    return np.asarray(ids, np.int32)
+
+
+@pytest.mark.parametrize("r", [8, 16, 64])
+def test_interleaved_prefill_requests_every_row(r):
+    """A prefill batch of 1,664 tokens whose eight requests' tokens are
+    interleaved: every segment is long and gathered; every row checked."""
+    rng = np.random.default_rng(70 + r)
+    lens = [300, 128, 257, 190, 64, 333, 200, 192]
+    ids = _interleaved_requests(rng, lens, [5, 0, 7, 2, 6, 1, 3, 4])
+    n, P, h_in, h_out = ids.size, 8, 1024, 1536
+    x = _bf16(rng.standard_normal((n, h_in)))
+    A = _bf16(rng.standard_normal((P, h_in, r)) / np.sqrt(h_in))
+    B = _bf16(rng.standard_normal((P, r, h_out)) / np.sqrt(r))
+    y = _bf16(rng.standard_normal((n, h_out)))
+    y0 = y.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    seg = lsg.lora_segment(torch.from_numpy(ids).cuda(), P, err_flag=err)
+    check_segments(seg, ids, P)
+    lsg.sgmv_fused(x, A, B, seg, y, 0.5, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_within_tol(y, oracle_rows(x, A, B, ids, 0.5, y0))
+
+
+def test_exact_arithmetic_gathered_prefill_is_bit_exact():
+    """Small-integer inputs on interleaved long segments: exact sums, so the
+    gathered tensor-tile path equals the oracle bit for bit."""
+    rng = np.random.default_rng(71)
+    ids = _interleaved_requests(rng, [260, 200, 130], [1, 0, 2])
+    n, P, h_in, h_out, r = ids.size, 3, 1024, 640, 64
+    x = rng.choice([-1.0, 0.0, 1.0], (n, h_in), p=[0.25, 0.5, 0.25])
+    A = rng.choice([-1.0, 0.0, 1.0], (P, h_in, r), p=[0.02, 0.96, 0.02])
+    B = rng.choice([-1.0, 0.0, 1.0], (P, r, h_out), p=[0.1, 0.8, 0.1])
+    y0 = rng.integers(-8, 9, (n, h_out)).astype(np.float64)
+    xt, At, Bt, yt = _bf16(x), _bf16(A), _bf16(B), _bf16(y0)
+    import oracle
+
+    y_ref = oracle.sgmv_ref(xt.cpu(), At.cpu(), Bt.cpu(), ids, 2.0, yt.cpu())
+    assert np.all(np.abs(y_ref) <= 256) and np.all(y_ref == np.round(y_ref))
+    seg = lsg.lora_segment(torch.from_numpy(ids).cuda(), P)
+    lsg.sgmv_fused(xt, At, Bt, seg, yt, 2.0)
+    assert np.array_equal(yt.float().cpu().numpy(), y_ref)
+
+
+@pytest.mark.parametrize("r", [8, 16, 64])
+@pytest.mark.parametrize("gathered", [False, True], ids=["contiguous", "gathered"])
+def test_shrink_then_expand_long_segments(r, gathered):
+    """Standalone shrink (v to device memory) and expand (v from device
+    memory) on prefill segments: v within the fp32 summation bound of the
+    oracle's v, y within the parity tolerance."""
+    import oracle
+
+    rng = np.random.default_rng(80 + r + gathered)
+    lens, ads = [400, 128, 77, 300], [2, 0, 3, 1]
+    ids = _interleaved_requests(rng, lens, ads) if gathered else \
+        np.concatenate([np.full(l, a, np.int32) for l, a in zip(lens, ads)])
+    n, P, h_in, h_out = ids.size, 4, 2048, 1024
+    x = _bf16(rng.standard_normal((n, h_in)))
+    A = _bf16(rng.standard_normal((P, h_in, r)) / np.sqrt(h_in))
+    B = _bf16(rng.standard_normal((P, r, h_out)) / np.sqrt(r))
+    y = _bf16(rng.standard_normal((n, h_out)))
+    y0 = y.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    seg = lsg.lora_segment(torch.from_numpy(ids).cuda(), P, err_flag=err)
+    v = lsg.sgmv_shrink(x, A, seg, err_flag=err)
+    lsg.sgmv_expand(v, B, seg, y, 1.5, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    y_ref, v_ref = oracle.sgmv_ref(x.cpu(), A.cpu(), B.cpu(), ids, 1.5, y0.cpu(), want_v=True)
+    xa = (x.float().abs() @ A.float().abs().permute(1, 0, 2).reshape(h_in, -1)).cpu().numpy()
+    xa = xa.reshape(n, P, r)[np.arange(n), ids]
+    vb = 2 * (h_in + 2) * 2.0 ** -24 * xa + 1e-30
+    assert np.all(np.abs(v.cpu().numpy() - v_ref) <= vb)
+    assert_within_tol(y, y_ref)

@@ -16,6 +16,7 @@ from .gen import (  # noqa: F401
     distinct_ids,
     f32_from_bf16_bits,
     llama_projs,
+    make_backbone_weights,
     make_inputs,
     make_slot_inputs,
     normal_bf16,

@@ -97,15 +97,26 @@ def zipf_ids(n: int, P: int, alpha: float, seed: int = 0) -> np.ndarray:
 
 
 def prefill_ids(n_requests: int = 8, P: int = 32, lo: int = 128, hi: int = 2048,
-                seed: int = 0) -> np.ndarray:
+                seed: int = 0, interleave: bool = False) -> np.ndarray:
     """Prefill batch: request i has a prompt of L_i ~ U{lo..hi} tokens and its
     own adapter (distinct, drawn from the pool); requests are laid out in
-    ascending adapter order, so the batch is already sorted by adapter."""
+    ascending adapter order, so the batch is already sorted by adapter.  With
+    interleave, the requests' tokens are dealt out round robin instead (same
+    ids, no request's rows contiguous)."""
     rng = np.random.default_rng(seed)
     lengths = rng.integers(lo, hi + 1, n_requests)
     adapters = rng.choice(P, n_requests, replace=False)
     order = np.argsort(adapters, kind="stable")
-    return np.concatenate([np.full(lengths[i], adapters[i], dtype=np.int32) for i in order])
+    if not interleave:
+        return np.concatenate([np.full(lengths[i], adapters[i], dtype=np.int32) for i in order])
+    left = [int(lengths[i]) for i in order]
+    out = []
+    while any(left):
+        for k, i in enumerate(order):
+            if left[k]:
+                out.append(adapters[i])
+                left[k] -= 1
+    return np.asarray(out, dtype=np.int32)
 
 
 # ---------------------------------------------------------------- workloads
@@ -136,6 +147,11 @@ def _build_workloads() -> Dict[str, Workload]:
                            prefill_ids,
                            "Llama2-13B prefill, 7 projections, r=64, 8 requests of U[128,2048] tokens, "
                            "8 adapters of pool 32, sorted by adapter")
+    w["13b_prefill_interleaved"] = _mk("13b_prefill_interleaved", llama_projs("13b"), 64, 32, int(ids13.size), 1.0,
+                                       lambda: prefill_ids(interleave=True),
+                                       "Llama2-13B prefill, 7 projections, r=64, the 8 requests of the prefill batch "
+                                       "with their tokens interleaved round robin (rows gathered per segment)",
+                                       "13b_prefill")
     ids13s = prefill_ids(n_requests=2)
     w["13b_prefill_small"] = _mk("13b_prefill_small", llama_projs("13b"), 64, 32, int(ids13s.size),
                                  1.0, lambda: prefill_ids(n_requests=2),
@@ -250,3 +266,10 @@ def make_slot_inputs(h_in: int, h_out: int, ids: np.ndarray, rank_of: np.ndarray
                       normal_bf16((n, h_in), 1.0, seed_for(name, "x", copy), device), A_ar, B_ar,
                       normal_bf16((n, h_out), 1.0, seed_for(name, "y0", copy), device),
                       torch.from_numpy(slots).to(device), torch.from_numpy(np.asarray(rank_of, np.int32)).to(device))
+
+
+def make_backbone_weights(wl: Workload, device="cpu", copy: int = 0) -> List[torch.Tensor]:
+    """Synthetic backbone weights W [h_in][h_out] per projection, N(0, 1/h_in)
+    (so x . W ~ N(0, 1) for x ~ N(0, 1)), rounded to bf16."""
+    return [normal_bf16((p.h_in, p.h_out), 1.0 / p.h_in, seed_for(wl.seed_name, "W", p.name, copy), device)
+            for p in wl.projs]
