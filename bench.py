@@ -927,6 +927,8 @@ def main(argv=None):
                     help="time cap of the reference arm's timed calls")
     ap.add_argument("--no-batch-curve", action="store_true",
                     help="skip step latency against batch size (decode and prefill, identical vs mixed adapters)")
+    ap.add_argument("--backbone-only", action="store_true",
+                    help="only the backbone GEMM + LoRA comparison (a diagnostic line, not the benchmark contract)")
     ap.add_argument("--no-backbone", action="store_true",
                     help="skip the backbone GEMM with the fused LoRA expand against cuBLAS + SGMV")
     ap.add_argument("--no-per-config", action="store_true",
@@ -936,6 +938,13 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.backbone_only:
+        import torch
+
+        import adapter_gemm_02_b300 as lsg
+
+        print(json.dumps({"backbone_fused": backbone_fused(args.warmup, torch.device("cuda", 0), lsg, bf16_peaks())}),
+              flush=True)
     else:
         run_ours(args)
 
