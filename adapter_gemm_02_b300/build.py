@@ -34,10 +34,10 @@ def headers():
                   + [os.path.join(ROOT, "include", "lora_sgmv.h")])
 
 
-def stale() -> bool:
-    if not os.path.exists(LIB):
+def stale(path: str = LIB) -> bool:
+    if not os.path.exists(path):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(path)
     return any(os.path.getmtime(f) > t for f in sources() + headers())
 
 
@@ -62,6 +62,16 @@ def build(verbose: bool = False, extra=(), out: str = LIB) -> str:
     subprocess.run([_nvcc(), *ARCH, "--shared", "-Xcompiler", "-fPIC", *objs, "-o", out + ".tmp"], check=True)
     os.replace(out + ".tmp", out)
     return out
+
+
+TEST_HOOKS_LIB = os.path.join(PKG, "liblora_sgmv_testhooks.so")
+
+
+def build_test_hooks(verbose: bool = False) -> str:
+    """The library as tests build it to exercise bounded waits that run out:
+    20 ms per wait, and hooks (lora_test_withhold) that make a kernel
+    withhold one signal.  Never loaded by the product path."""
+    return build(verbose, extra=("-DLSG_WAIT_LIMIT_NS=20000000ull", "-DLSG_TEST_HOOKS=1"), out=TEST_HOOKS_LIB)
 
 
 if __name__ == "__main__":

@@ -32,9 +32,9 @@
 //              boxes, MN-major, 128 B swizzle), B tiles [r][256]
 //   warp 5     TMEM allocation; one thread issues the MMAs (M = 128, N = 256)
 // The two 256-column accumulators alternate, so the epilogue of one tile
-// overlaps the main loop of the next.  Each CTA takes a contiguous range of
-// (token tile, column tile) units, column tiles inner, so consecutive units
-// reuse the x rows from L2 and the v operand of a tile's only segment.
+// overlaps the main loop of the next.  Units (token tile, column tile),
+// column tiles inner, are dealt round robin over the CTAs, so the units in
+// flight together cover a few token tiles and all of W: both stay in L2.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -50,7 +50,7 @@ constexpr int kGlThreads = 192;
 constexpr int kGlStages = 4;
 constexpr int kGlBN = 256;     // output columns per tile (MMA N)
 constexpr int kGlMaxRuns = 3;  // long segments (>= 64 tokens) a 128-token window can overlap
-constexpr uint64_t kGlWaitNs = 2000000000ull;
+constexpr uint64_t kGlWaitNs = LSG_WAIT_LIMIT_NS;
 
 struct GlTail {
   const int32_t* perm;
@@ -98,6 +98,7 @@ struct GlSmem {
   uint64_t acc_empty[2];
   uint64_t op_full;   // the operand of the next long segment is in shared memory
   uint64_t op_empty;  // the expand MMAs of the last one completed
+  uint64_t drain;     // the MMA issuer, at exit: its MMAs have completed
   uint32_t tmem_base;
   int32_t abort;
 };
@@ -198,6 +199,7 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
     }
     mbar_init(&sm.op_full, 4);
     mbar_init(&sm.op_empty, 1);
+    mbar_init(&sm.drain, 1);
     sm.abort = 0;
     fence_mbar_init();
   }
@@ -211,10 +213,11 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
   const bool aligned = (smem_u32(sm.st) & 1023u) == 0;
   if (!aligned && tid == 0) set_err(q.err_flag, LORA_ERR_UNSUPPORTED);
 
-  // this CTA's units: a contiguous range of (token tile, column tile), column tiles inner
+  // units (token tile, column tile), column tiles inner, dealt round robin: the
+  // units in flight together cover a few token tiles and all of W, which stay
+  // in L2 (a contiguous range per CTA would put all of x and W in flight)
   const int units = q.m_tiles * q.n_tiles;
-  const int u0 = static_cast<int>((static_cast<int64_t>(units) * blockIdx.x) / gridDim.x);
-  const int u1 = static_cast<int>((static_cast<int64_t>(units) * (blockIdx.x + 1)) / gridDim.x);
+  const int u0 = static_cast<int>(blockIdx.x), ustep = static_cast<int>(gridDim.x);
   const int S = min(max(*q.num_segments, 0), q.max_segments);
 
   if (aligned && warp == 4) {
@@ -233,7 +236,7 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
       }
     };
     bool ok = true;
-    for (int u = u0; u < u1 && ok; ++u) {
+    for (int u = u0; u < units && ok; u += ustep) {
       const int mt = u / q.n_tiles, nt = u - mt * q.n_tiles;
       if (mt != cur_m) {
         gl_tile(q, S, mt, lane, t);
@@ -295,7 +298,7 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
     uint32_t ph = 0;
     GlTile t{};
     bool ok = true;
-    for (int u = u0; u < u1 && ok; ++u, ++ui) {
+    for (int u = u0; u < units && ok; u += ustep, ++ui) {
       const int mt = u / q.n_tiles;
       if (mt != cur_m) {
         gl_tile(q, S, mt, lane, t);
@@ -358,6 +361,12 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
       if (lane == 0) umma_commit(&sm.acc_full[buf]);
       __syncwarp();
     }
+    // every MMA issued here has completed before TMEM is released
+    if (lane == 0) {
+      umma_commit(&sm.drain);
+      (void)mbar_wait(&sm.drain, 0, kGlWaitNs);
+    }
+    __syncwarp();
   } else if (aligned && warp < 4) {
     // ============================== epilogue: thread = tile row m
     const int m = warp * 32 + lane;
@@ -366,7 +375,7 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
     GlTile t{};
     bool ok = true;
     const float s = q.scale;
-    for (int u = u0; u < u1 && ok; ++u, ++ui) {
+    for (int u = u0; u < units && ok; u += ustep, ++ui) {
       const int mt = u / q.n_tiles, nt = u - mt * q.n_tiles;
       if (mt != cur_m) {
         gl_tile(q, S, mt, lane, t);

@@ -11,6 +11,11 @@
 
 namespace lsg {
 
+// Bound of every wait inside a kernel (build-time knob; a test build shortens it).
+#ifndef LSG_WAIT_LIMIT_NS
+#define LSG_WAIT_LIMIT_NS 2000000000ull
+#endif
+
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 inline int round_up(int a, int b) { return ceil_div(a, b) * b; }
 
@@ -103,5 +108,14 @@ lora_status encode_tmap_bf16(CUtensorMap* out, const void* base, int rank, const
 
 // Records a CUDA error from a runtime call; returns LORA_ERR_CUDA on failure.
 lora_status cuda_status(cudaError_t e);
+
+#ifdef LSG_TEST_HOOKS
+// Test builds only: the kernels withhold one signal (1: the decode kernel's
+// end-of-work marker, 2: the partial v that CTA 1 of each decode cluster
+// pushes, 3: the tensor-tile kernel's first expand accumulator), so a bounded
+// wait runs out; 0: none.
+lora_status test_withhold_cc(int what);
+lora_status test_withhold_tc(int what);
+#endif
 
 }  // namespace lsg

@@ -70,6 +70,15 @@ const char* lora_status_str(int s) {
 
 int lora_abi_version(void) { return LORA_SGMV_ABI_VERSION; }
 
+#ifdef LSG_TEST_HOOKS
+// Test builds only (not declared in the public header): which signal the
+// kernels withhold, so that a bounded wait runs out (see internal.h).
+LORA_API lora_status lora_test_withhold(int what) {
+  const lora_status s = test_withhold_cc(what);
+  return s != LORA_OK ? s : test_withhold_tc(what);
+}
+#endif
+
 size_t lora_segment_workspace_bytes(int32_t n_tokens, int32_t n_adapters) {
   if (n_tokens < 0 || n_adapters < 1) return 0;
   return seg_plan(n_tokens, n_adapters).ws_bytes;

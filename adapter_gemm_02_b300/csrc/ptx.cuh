@@ -156,6 +156,18 @@ __device__ __forceinline__ void tma_gather4(void* dst, const void* tmap, int32_t
       : "memory");
 }
 
+// Four consecutive rows of this CTA's shared memory (as a four-row gather
+// lays them out) -> rows r0..r3, columns [c0, c0 + w) of a 2-D tensor (box
+// {w, 1}), tracked as a bulk async-group of the executing thread.
+__device__ __forceinline__ void tma_scatter4(const void* tmap, int32_t c0, int32_t r0, int32_t r1, int32_t r2,
+                                             int32_t r3, const void* src) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile::scatter4.bulk_group [%0, {%1, %2, %3, %4, %5}], [%6];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(src))
+      : "memory");
+}
+
 // This CTA's shared memory -> global, tracked as a bulk async-group of the
 // executing thread.  dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {

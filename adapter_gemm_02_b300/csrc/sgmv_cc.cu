@@ -81,7 +81,7 @@ namespace lsg {
 #define LSG_CC_KB_BIG 28
 #endif
 #ifndef LSG_CC_KB_R8
-#define LSG_CC_KB_R8 LSG_CC_KB_SMALL
+#define LSG_CC_KB_R8 16
 #endif
 #ifndef LSG_CC_WARPS
 #define LSG_CC_WARPS 4
@@ -94,7 +94,15 @@ constexpr int kCThreads = kCW * 32;    // consumer threads
 constexpr int kThreads = kCThreads + 32;
 constexpr int kMaxC = 8;               // CTAs per cluster (portable limit)
 constexpr int kXB = 2;                 // partial-v exchange buffers
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+constexpr uint64_t kWaitLimitNs = LSG_WAIT_LIMIT_NS;  // per wait (2 s)
+
+#ifdef LSG_TEST_HOOKS
+__device__ int g_test_withhold;
+__device__ __forceinline__ bool withhold(int what) { return *(volatile int*)&g_test_withhold == what; }
+lora_status test_withhold_cc(int what) { return cuda_status(cudaMemcpyToSymbol(g_test_withhold, &what, sizeof(int))); }
+#else
+__device__ __forceinline__ bool withhold(int) { return false; }
+#endif
 
 enum : int { kStShrink = 1, kStExpand = 2, kStFirst = 4, kStLast = 8, kStEnd = 16 };
 
@@ -565,7 +573,7 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
     }
     wait_dep();  // also when this CTA had no item: CTA 0 writes the segmentation
     if (!failed && acquire()) {
-      if (lane == 0) {
+      if (lane == 0 && !withhold(1)) {
         sm.hdr[slot].kind = kStEnd;
         mbar_arrive(&sm.full[slot]);
       }
@@ -786,7 +794,8 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
               reinterpret_cast<float4*>(&xbuf[b][rank][0][0])[i] = vp;
               const uint32_t src = smem_u32(&xbuf[b][rank][0][0]) + i * 16;
               for (int qq = 0; qq < C; ++qq)
-                if (qq != rank) st_async_v4(mapa_shared(src, qq), vp, mapa_shared(bar, qq));
+                if (qq != rank && !(rank == 1 && withhold(2)))
+                  st_async_v4(mapa_shared(src, qq), vp, mapa_shared(bar, qq));
             }
             bool got = true;
             if (lane == 0) got = mbar_wait(&sm.xbar[b], (nx >> 1) & 1, kWaitLimitNs);

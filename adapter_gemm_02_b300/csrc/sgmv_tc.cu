@@ -41,7 +41,8 @@
 // x / y (prefill requests) moves whole tiles with 2-D tensor copies; any other
 // segment (tokens of one adapter spread over the batch) gathers its rows
 // through the permutation, four rows per tile::gather4 tensor copy, and its
-// updated y rows go back to their own rows by plain 16-byte stores.
+// updated y rows go back by tile::scatter4 tensor stores (rows of an
+// incomplete group of four by 16-byte stores).
 //
 // Rank 8 runs at an MMA width of 16: the shrink's N = 16 columns read the A
 // tile's 8 columns plus 8 columns of other shared memory, whose results are
@@ -86,7 +87,15 @@ constexpr uint32_t kTmemAcc = 128;  // expand accumulators: [128, 256), [256, 38
 constexpr int kChunkCols = LSG_TC_CHUNK;  // expand columns per item, about
 constexpr int kMaxItemsPerTile = 64;
 constexpr int kMaxC = 8;  // CTAs per cluster (portable limit)
-constexpr uint64_t kTcWaitNs = 2000000000ull;
+constexpr uint64_t kTcWaitNs = LSG_WAIT_LIMIT_NS;
+
+#ifdef LSG_TEST_HOOKS
+__device__ int g_test_withhold;
+__device__ __forceinline__ bool withhold(int what) { return *(volatile int*)&g_test_withhold == what; }
+lora_status test_withhold_tc(int what) { return cuda_status(cudaMemcpyToSymbol(g_test_withhold, &what, sizeof(int))); }
+#else
+__device__ __forceinline__ bool withhold(int) { return false; }
+#endif
 
 struct TcProj {
   uint16_t* y;  // for the direct stores of a tile's last rows and of gathered rows
@@ -173,6 +182,7 @@ struct TcSmem {
   uint64_t rs_full;    // (cluster) every rank's partial of the rows this CTA owns has arrived
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
+  uint64_t drain[2];  // each MMA issuer, at exit: its MMAs have completed
   uint32_t tmem_base;
   int32_t abort;
 };
@@ -362,6 +372,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.acc_full[b], 1);
       mbar_init(&sm.acc_empty[b], 8);  // both epilogue groups' warps
+      mbar_init(&sm.drain[b], 1);
     }
     sm.abort = 0;
     fence_mbar_init();
@@ -383,7 +394,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
   if (aligned && kHasShrink && warp == 4) {
     // ============================== shrink producer
     int slot = 0;
-    uint32_t ph = 0;
+    uint32_t ph = 0, filled = 0, fill_par = 0;
     TcCursor cur;
     cur.init(q, lane);
     for (int item = group;; item += ngroups) {
@@ -410,6 +421,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
         if (t.row < 0)
           tma_gather4(st + lane * 512, &p.tmXg[pj], kb * 64, rr[0], rr[1], rr[2], rr[3], &sm.sh_full[slot]);
         __syncwarp();
+        filled |= 1u << slot;
+        fill_par = (fill_par & ~(1u << slot)) | (ph << slot);
         if (++slot == kSh) {
           slot = 0;
           ph ^= 1u;
@@ -417,10 +430,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       }
       if (!ok || sm.abort) break;
     }
+    if (lane == 0 && sm.abort)  // no copy issued here may still be landing when the CTA leaves
+      for (int s2 = 0; s2 < kSh; ++s2)
+        if (filled & (1u << s2)) (void)mbar_wait(&sm.sh_full[s2], (fill_par >> s2) & 1u, kTcWaitNs);
   } else if (aligned && kHasExpand && warp == 5) {
     // ============================== expand producer
     int slot = 0;
-    uint32_t ph = 0;
+    uint32_t ph = 0, filled = 0, fill_par = 0;
     TcCursor cur;
     cur.init(q, lane);
     for (int item = group;; item += ngroups) {
@@ -457,6 +473,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
                         &sm.ex_full[slot]);
         }
         __syncwarp();
+        filled |= 1u << slot;
+        fill_par = (fill_par & ~(1u << slot)) | (ph << slot);
         if (++slot == kEx) {
           slot = 0;
           ph ^= 1u;
@@ -464,6 +482,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       }
       if (!ok || sm.abort) break;
     }
+    if (lane == 0 && sm.abort)  // no copy issued here may still be landing when the CTA leaves
+      for (int s2 = 0; s2 < kEx; ++s2)
+        if (filled & (1u << s2)) (void)mbar_wait(&sm.ex_full[s2], (fill_par >> s2) & 1u, kTcWaitNs);
   } else if (aligned && kHasShrink && warp == 6) {
     // ============================== shrink MMA issuer: v = x . A (this CTA's k-blocks)
     constexpr uint32_t kIdSh = umma_idesc_bf16(128, RP, 0, 1);
@@ -513,6 +534,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       if (sm.abort) break;
       ++it;
     }
+    // every MMA issued here has completed before TMEM is released
+    if (lane == 0) {
+      umma_commit(&sm.drain[0]);
+      (void)mbar_wait(&sm.drain[0], 0, kTcWaitNs);
+    }
+    __syncwarp();
   } else if (aligned && kHasExpand && warp == 7) {
     // ============================== expand MMA issuer: acc = v_hi . B + v_lo . B
     constexpr uint32_t kIdEx = umma_idesc_bf16(128, kBN, 0, 1);
@@ -555,7 +582,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
               umma_bf16(tmem + kTmemAcc + buf * kBN, ad, bd, kIdEx, k > 0 || hl > 0);
             }
           }
-          umma_commit(&sm.acc_full[buf]);
+          if (!(withhold(3) && ae == 0)) umma_commit(&sm.acc_full[buf]);
         }
         __syncwarp();
         ++ae;
@@ -567,6 +594,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       if (!ok || sm.abort) break;
       ++it;
     }
+    // every MMA issued here has completed before TMEM is released
+    if (lane == 0) {
+      umma_commit(&sm.drain[1]);
+      (void)mbar_wait(&sm.drain[1], 0, kTcWaitNs);
+    }
+    __syncwarp();
   } else if (aligned && (warp < 4 || (kHasExpand && warp >= 8))) {
     // ============================== epilogue (row m = TMEM lane m): two groups
     // of four warps (0-3, 8-11); group eg turns v into the operand (group 0)
@@ -576,7 +609,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
     const uint32_t tq = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     int xslot = 0, ae = 0, it = 0;
     uint32_t xph = 0;
-    int pend = -1;  // (lane 0) ring slot whose y stores may still be reading it
+    int pend = -1;  // ring slot whose y stores may still be reading it
     TcCursor cur;
     cur.init(q, lane);
     // one 16-byte chunk (8 ranks) of a row as the hi / lo operand words
@@ -758,6 +791,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
         split((min(pr.chunk, pr.h_out - c0) + kBN - 1) / kBN, b0, b1);
         const bool contig = t.row >= 0;
         const int full_rows = contig ? (t.tlen >> 5) << 5 : 0;  // rows stored by TMA boxes
+        // gathered tile: rows in a group of four valid rows go out by one
+        // four-row scatter (lane j of the quarter's warp: rows 4j .. 4j+3)
+        const unsigned vmask = __ballot_sync(0xffffffffu, yrow >= 0);
+        const bool by_tensor_store = contig ? m < full_rows : ((vmask >> (lane & ~3)) & 0xFu) == 0xFu;
+        int yr4[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) yr4[k] = __shfl_sync(0xffffffffu, yrow, (4 * lane + k) & 31);
+        const bool scatter_lane = !contig && lane < 8 && ((vmask >> (4 * lane)) & 0xFu) == 0xFu;
         for (int b = b0; b < b1 && ok; ++b) {
           const int buf = ae & 1;
           ok = warp_wait(sm, &sm.acc_full[buf], (ae >> 1) & 1, lane);
@@ -791,29 +832,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
                                           yf.y + scale * __uint_as_float(acc[i * 8 + 2 * e + 1]));
                 yw[e] = *reinterpret_cast<const uint32_t*>(&o);
               }
-              if (m < full_rows) {
+              if (by_tensor_store) {
                 asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(yw[0]), "r"(yw[1]),
                              "r"(yw[2]), "r"(yw[3])
                              : "memory");
               } else if (yp != nullptr && c + j * 8 < pr.h_out) {
-                // rows past the last whole group of 32, and every row of a gathered
-                // tile: written directly (16-byte stores)
+                // rows past the last whole group of 32 (contiguous tile) or of
+                // four (gathered tile): written directly (16-byte stores)
                 *reinterpret_cast<uint4*>(yp + c + j * 8) = make_uint4(yw[0], yw[1], yw[2], yw[3]);
               }
             }
           }
           fence_proxy_async_smem();  // our y updates, visible to the tensor stores
           named_bar_sync(3 + wq, 64);  // the two warps of this lane quarter are done with the block
-          if (eg == 0 && lane == 0) {
-            // each lane quarter stores its own 32 rows (one 64-column box)
+          if (eg == 0) {
+            // each lane quarter stores its own 32 rows: one 64-column box, or
+            // four-row scatters of a gathered tile
             const int g = wq * 32;
-            if (g + 32 <= full_rows && c < pr.h_out) tma_store_2d(&p.tmYs[pj], c, t.row + g, st + g * 128);
+            if (lane == 0 && g + 32 <= full_rows && c < pr.h_out) tma_store_2d(&p.tmYs[pj], c, t.row + g, st + g * 128);
+            if (scatter_lane && c < pr.h_out)
+              tma_scatter4(&p.tmYg[pj], c, yr4[0], yr4[1], yr4[2], yr4[3], st + (g + 4 * lane) * 128);
             bulk_commit();
             // the previous block's stores have read their slot (this block's may
             // still be reading): this quarter's share of that slot goes back
             if (pend >= 0) {
               bulk_wait_read1();
-              mbar_arrive(&sm.ex_empty[pend]);  // y rows read by the stores, B tile read by the MMAs
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&sm.ex_empty[pend]);  // y rows read by the stores, B tile read by the MMAs
             }
             pend = xslot;
           }
@@ -828,7 +873,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       ++it;
     }
   }
-  if (aligned && warp < 4 && lane == 0) bulk_wait_read0();  // the last y stores have read shared memory
+  if (aligned && warp < 4) bulk_wait_read0();  // the last y stores have read shared memory
   tc_fence_before();
   __syncthreads();
   if (CL) {
