@@ -24,7 +24,12 @@
 //  3. the split-K SGMV kernel adds the delta of the short segments to y in
 //     place (a step that finds no short segment does nothing).
 //
-// gemm_lora_kernel: one CTA per SM, persistent, six warps:
+// gemm_lora_kernel: one CTA per SM, persistent, in clusters of CM CTAs that
+// take CM consecutive token tiles of the same column tile together: CTA k of
+// a cluster loads its own x rows and the k-th part of the W tile, which it
+// multicasts to every CTA of the cluster (each W tile is read from L2 once per
+// cluster instead of once per CTA); a ring slot is refilled only after every
+// CTA of the cluster has consumed it.  Six warps:
 //   warps 0-3  epilogue (warp w: TMEM lane quarter w; thread = tile row): the
 //              v operand of each long segment, then y from the accumulator
 //   warp 4     producer: TMA x tiles [128][64] (2-D box, or four-row gathers
@@ -32,9 +37,12 @@
 //              boxes, MN-major, 128 B swizzle), B tiles [r][256]
 //   warp 5     TMEM allocation; one thread issues the MMAs (M = 128, N = 256)
 // The two 256-column accumulators alternate, so the epilogue of one tile
-// overlaps the main loop of the next.  Units (token tile, column tile),
-// column tiles inner, are dealt round robin over the CTAs, so the units in
-// flight together cover a few token tiles and all of W: both stay in L2.
+// overlaps the main loop of the next.  Units (group of CM token tiles, column
+// tile), column tiles inner, are dealt round robin over the clusters, so the
+// units in flight together cover a few token tiles and all of W: both stay in
+// L2.  The long segments' expand slots of a unit are as many in every CTA of
+// the cluster (the most any of its token tiles has; a CTA with fewer fills
+// the rest with empty slots), so the rings stay in step.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -50,6 +58,20 @@ constexpr int kGlThreads = 192;
 constexpr int kGlStages = 4;
 constexpr int kGlBN = 256;     // output columns per tile (MMA N)
 constexpr int kGlMaxRuns = 3;  // long segments (>= 64 tokens) a 128-token window can overlap
+// Build-time knobs, set by measurement: clusters of 4 that share W tiles by
+// multicast halved the L2 reads but ran slower (132 SMs hold whole clusters,
+// and the four rings wait for each other), so CTAs run alone (CM = 1); the
+// producer prefetches the x and W boxes of the k-block LSG_GL_PREFETCH stages
+// ahead into L2, so the ring's refills find them there.
+#ifndef LSG_GL_CM
+#define LSG_GL_CM 1
+#endif
+#ifndef LSG_GL_PREFETCH
+#define LSG_GL_PREFETCH 0
+#endif
+constexpr int kGlCM = LSG_GL_CM;  // CTAs per cluster sharing the W tiles (1, 2 or 4)
+constexpr int kGlPrefetch = LSG_GL_PREFETCH;
+static_assert(kGlCM == 1 || kGlCM == 2 || kGlCM == 4, "cluster size");
 constexpr uint64_t kGlWaitNs = LSG_WAIT_LIMIT_NS;
 
 struct GlTail {
@@ -116,6 +138,11 @@ __device__ __forceinline__ void gl_tile(const GlTail& q, int S, int mt, int lane
   const int n = q.n_tokens;
   t.t0 = mt * 128;
   t.tlen = min(128, n - t.t0);
+  if (t.tlen <= 0) {  // a cluster's token tile past the batch: no rows, no segments
+    t.row = -1;
+    t.nrun = 0;
+    return;
+  }
   const int f = q.perm[t.t0];
   bool c = f >= 0 && f + t.tlen <= n;
 #pragma unroll
@@ -166,11 +193,12 @@ __device__ __forceinline__ bool gl_wait(SM& sm, uint64_t* bar, uint32_t parity, 
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-template <int R>
+template <int R, int CM>
 __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_constant__ GlParams p) {
   using Cfg = GlCfg<R>;
   using SM = GlSmem<R>;
   constexpr int RP = Cfg::RP;
+  constexpr uint16_t kMask = static_cast<uint16_t>((1u << CM) - 1u);  // every CTA of the cluster
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   auto& sm = *reinterpret_cast<SM*>(smem_raw);
   const GlTail& q = sm.t;
@@ -191,7 +219,7 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
   if (tid == 0) {
     for (int s = 0; s < kGlStages; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 1);
+      mbar_init(&sm.empty[s], CM);  // every CTA of the cluster has consumed the slot
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.acc_full[b], 1);
@@ -207,24 +235,41 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (CM > 1) {  // every CTA's barriers exist before a peer copies or commits into them
+    cluster_arrive_relaxed();
+    cluster_wait_acquire();
+  }
   const uint32_t tmem = sm.tmem_base;
   pdl_launch_dependents();
   pdl_wait();  // v (and the segmentation) come from the launches before
   const bool aligned = (smem_u32(sm.st) & 1023u) == 0;
   if (!aligned && tid == 0) set_err(q.err_flag, LORA_ERR_UNSUPPORTED);
 
-  // units (token tile, column tile), column tiles inner, dealt round robin: the
-  // units in flight together cover a few token tiles and all of W, which stay
-  // in L2 (a contiguous range per CTA would put all of x and W in flight)
-  const int units = q.m_tiles * q.n_tiles;
-  const int u0 = static_cast<int>(blockIdx.x), ustep = static_cast<int>(gridDim.x);
+  // units (group of CM token tiles, column tile), column tiles inner, dealt
+  // round robin over the clusters: the units in flight together cover a few
+  // token tiles and all of W, which stay in L2 (a contiguous range per
+  // cluster would put all of x and W in flight)
+  const int crank = static_cast<int>(blockIdx.x) % CM;
+  const int units = ((q.m_tiles + CM - 1) / CM) * q.n_tiles;
+  const int u0 = static_cast<int>(blockIdx.x) / CM, ustep = static_cast<int>(gridDim.x) / CM;
   const int S = min(max(*q.num_segments, 0), q.max_segments);
+  // expand slots of a unit: the most long segments any token tile of the group overlaps
+  auto group_runs = [&](int g) {
+    int mx = 0;
+#pragma unroll
+    for (int k = 0; k < CM; ++k) {
+      GlTile tk;
+      gl_tile(q, S, g * CM + k, lane, tk);
+      mx = max(mx, tk.nrun);
+    }
+    return mx;
+  };
 
   if (aligned && warp == 4) {
     // ============================== producer
     int slot = 0;
     uint32_t ph = 0, filled = 0, fill_par = 0;
-    int cur_m = -1;
+    int cur_m = -1, nslots_x = 0;
     GlTile t{};
     int rr[4] = {0, 0, 0, 0};
     auto advance = [&]() {
@@ -237,11 +282,13 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
     };
     bool ok = true;
     for (int u = u0; u < units && ok; u += ustep) {
-      const int mt = u / q.n_tiles, nt = u - mt * q.n_tiles;
+      const int g = u / q.n_tiles, nt = u - g * q.n_tiles;
+      const int mt = g * CM + crank;
       if (mt != cur_m) {
         gl_tile(q, S, mt, lane, t);
+        nslots_x = CM > 1 ? group_runs(g) : t.nrun;
         cur_m = mt;
-        if (t.row < 0) {
+        if (t.tlen > 0 && t.row < 0) {
           // four rows per lane for the gathers; rows past the tile or with a
           // corrupt permutation entry read a valid row (never stored)
           int first = q.perm[t.t0];
@@ -259,28 +306,46 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
         ok = gl_wait(sm, &sm.empty[slot], ph ^ 1u, lane);
         if (!ok) break;
         uint8_t* st = sm.st[slot];
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&sm.full[slot], static_cast<uint32_t>(Cfg::kStage));
-          if (t.row >= 0) tma_load_2d(st, &p.tmX, kb * 64, t.row, &sm.full[slot]);
+        if (kGlPrefetch > 0 && lane == 0 && kb + kGlPrefetch < q.k_blocks) {
+          // the boxes this CTA will load kGlPrefetch stages later, into L2 now
+          const int kp = kb + kGlPrefetch;
+          if (t.tlen > 0 && t.row >= 0) tma_prefetch_2d(&p.tmX, kp * 64, t.row);
 #pragma unroll
-          for (int h = 0; h < 4; ++h) tma_load_2d(st + Cfg::kX + h * 8192, &p.tmW, c0 + h * 64, kb * 64, &sm.full[slot]);
+          for (int h = crank * (4 / CM); h < (crank + 1) * (4 / CM); ++h) tma_prefetch_2d(&p.tmW, c0 + h * 64, kp * 64);
+        }
+        if (lane == 0) {
+          // own x rows (none past the batch) and the whole W tile (every CTA's part)
+          mbar_arrive_expect_tx(&sm.full[slot], static_cast<uint32_t>((t.tlen > 0 ? Cfg::kX : 0) + Cfg::kW));
+          if (t.tlen > 0 && t.row >= 0) tma_load_2d(st, &p.tmX, kb * 64, t.row, &sm.full[slot]);
+#pragma unroll
+          for (int h = crank * (4 / CM); h < (crank + 1) * (4 / CM); ++h) {
+            if constexpr (CM > 1)
+              tma_load_2d_mc(st + Cfg::kX + h * 8192, &p.tmW, c0 + h * 64, kb * 64, &sm.full[slot], kMask);
+            else
+              tma_load_2d(st + Cfg::kX + h * 8192, &p.tmW, c0 + h * 64, kb * 64, &sm.full[slot]);
+          }
         }
         __syncwarp();  // the stage's byte count is registered before the gathers land
-        if (t.row < 0) tma_gather4(st + lane * 512, &p.tmXg, kb * 64, rr[0], rr[1], rr[2], rr[3], &sm.full[slot]);
+        if (t.tlen > 0 && t.row < 0)
+          tma_gather4(st + lane * 512, &p.tmXg, kb * 64, rr[0], rr[1], rr[2], rr[3], &sm.full[slot]);
         __syncwarp();
         advance();
       }
 #pragma unroll
       for (int j = 0; j < kGlMaxRuns; ++j) {
-        if (j >= t.nrun || !ok) break;
+        if (j >= nslots_x || !ok) break;
         ok = gl_wait(sm, &sm.empty[slot], ph ^ 1u, lane);
         if (!ok) break;
         uint8_t* st = sm.st[slot];
         if (lane == 0) {
-          mbar_arrive_expect_tx(&sm.full[slot], static_cast<uint32_t>(Cfg::kB));
+          if (j < t.nrun) {
+            mbar_arrive_expect_tx(&sm.full[slot], static_cast<uint32_t>(Cfg::kB));
 #pragma unroll
-          for (int h = 0; h < 4; ++h)
-            tma_load_3d(st + Cfg::kX + h * RP * 128, &p.tmB, c0 + h * 64, 0, t.a[j], &sm.full[slot]);
+            for (int h = 0; h < 4; ++h)
+              tma_load_3d(st + Cfg::kX + h * RP * 128, &p.tmB, c0 + h * 64, 0, t.a[j], &sm.full[slot]);
+          } else {
+            mbar_arrive(&sm.full[slot]);  // an empty slot: keeps the cluster's rings in step
+          }
         }
         __syncwarp();
         advance();
@@ -294,35 +359,47 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
   } else if (aligned && warp == 5) {
     // ============================== MMA issuer
     constexpr uint32_t kId = umma_idesc_bf16(128, kGlBN, 0, 1);
-    int slot = 0, ui = 0, nop = 0, cur_m = -1;
+    int slot = 0, ui = 0, nop = 0, cur_m = -1, nslots_x = 0;
     uint32_t ph = 0;
     GlTile t{};
     bool ok = true;
-    for (int u = u0; u < units && ok; u += ustep, ++ui) {
-      const int mt = u / q.n_tiles;
+    // a consumed slot goes back to the producers of every CTA of the cluster
+    auto release = [&](int sl) {
+      if constexpr (CM > 1) umma_commit_mc(&sm.empty[sl], kMask);
+      else umma_commit(&sm.empty[sl]);
+    };
+    for (int u = u0; u < units && ok; u += ustep) {
+      const int g = u / q.n_tiles;
+      const int mt = g * CM + crank;
       if (mt != cur_m) {
         gl_tile(q, S, mt, lane, t);
+        nslots_x = CM > 1 ? group_runs(g) : t.nrun;
         cur_m = mt;
       }
+      const bool mine = t.tlen > 0;  // a token tile past the batch: slots consumed, no MMAs
       const int buf = ui & 1;
       const uint32_t acc = tmem + static_cast<uint32_t>(buf * kGlBN);
-      ok = gl_wait(sm, &sm.acc_empty[buf], ((ui >> 1) & 1) ^ 1u, lane);
-      if (!ok) break;
-      tc_fence_after();
+      if (mine) {
+        ok = gl_wait(sm, &sm.acc_empty[buf], ((ui >> 1) & 1) ^ 1u, lane);
+        if (!ok) break;
+        tc_fence_after();
+      }
       for (int kb = 0; kb < q.k_blocks && ok; ++kb) {
         ok = gl_wait(sm, &sm.full[slot], ph, lane);
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t xs = smem_u32(sm.st[slot]), ws = xs + Cfg::kX;
+          if (mine) {
+            const uint32_t xs = smem_u32(sm.st[slot]), ws = xs + Cfg::kX;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            // x: K-major, 128 B swizzle; W: MN-major, 128 B swizzle, 64-column atoms 8 KB apart
-            const uint64_t ad = umma_desc(xs + k * 32, 16, 1024, 2);
-            const uint64_t bd = umma_desc(ws + k * 16 * 128, 8192, 1024, 2);
-            umma_bf16(acc, ad, bd, kId, kb > 0 || k > 0);
+            for (int k = 0; k < 4; ++k) {
+              // x: K-major, 128 B swizzle; W: MN-major, 128 B swizzle, 64-column atoms 8 KB apart
+              const uint64_t ad = umma_desc(xs + k * 32, 16, 1024, 2);
+              const uint64_t bd = umma_desc(ws + k * 16 * 128, 8192, 1024, 2);
+              umma_bf16(acc, ad, bd, kId, kb > 0 || k > 0);
+            }
           }
-          umma_commit(&sm.empty[slot]);
+          release(slot);
         }
         __syncwarp();
         if (++slot == kGlStages) {
@@ -332,34 +409,41 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
       }
 #pragma unroll
       for (int j = 0; j < kGlMaxRuns; ++j) {
-        if (j >= t.nrun || !ok) break;
-        ok = gl_wait(sm, &sm.op_full, nop & 1, lane) && gl_wait(sm, &sm.full[slot], ph, lane);
+        if (j >= nslots_x || !ok) break;
+        const bool run = j < t.nrun;
+        ok = (!run || gl_wait(sm, &sm.op_full, nop & 1, lane)) && gl_wait(sm, &sm.full[slot], ph, lane);
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t bs = smem_u32(sm.st[slot]) + Cfg::kX;
+          if (run) {
+            const uint32_t bs = smem_u32(sm.st[slot]) + Cfg::kX;
 #pragma unroll
-          for (int k = 0; k < RP / 16; ++k) {
-            const uint64_t bd = umma_desc(bs + k * 16 * 128, RP * 128, 1024, 2);
+            for (int k = 0; k < RP / 16; ++k) {
+              const uint64_t bd = umma_desc(bs + k * 16 * 128, RP * 128, 1024, 2);
 #pragma unroll
-            for (int hl = 0; hl < 2; ++hl) {
-              const uint64_t ad = umma_desc(smem_u32(sm.vop[hl]) + k * 32, 16, 8 * RP * 2, umma_layout(RP * 2));
-              umma_bf16(acc, ad, bd, kId, true);
+              for (int hl = 0; hl < 2; ++hl) {
+                const uint64_t ad =
+                    umma_desc(smem_u32(sm.vop[hl]) + k * 32, 16, 8 * RP * 2, umma_layout(RP * 2));
+                umma_bf16(acc, ad, bd, kId, true);
+              }
             }
           }
-          umma_commit(&sm.empty[slot]);
-          umma_commit(&sm.op_empty);
+          release(slot);
+          if (run) umma_commit(&sm.op_empty);
         }
         __syncwarp();
-        ++nop;
+        if (run) ++nop;
         if (++slot == kGlStages) {
           slot = 0;
           ph ^= 1u;
         }
       }
       if (!ok) break;
-      if (lane == 0) umma_commit(&sm.acc_full[buf]);
-      __syncwarp();
+      if (mine) {
+        if (lane == 0) umma_commit(&sm.acc_full[buf]);
+        __syncwarp();
+        ++ui;
+      }
     }
     // every MMA issued here has completed before TMEM is released
     if (lane == 0) {
@@ -375,8 +459,9 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
     GlTile t{};
     bool ok = true;
     const float s = q.scale;
-    for (int u = u0; u < units && ok; u += ustep, ++ui) {
-      const int mt = u / q.n_tiles, nt = u - mt * q.n_tiles;
+    for (int u = u0; u < units && ok; u += ustep) {
+      const int g = u / q.n_tiles, nt = u - g * q.n_tiles;
+      const int mt = g * CM + crank;
       if (mt != cur_m) {
         gl_tile(q, S, mt, lane, t);
         cur_m = mt;
@@ -389,6 +474,7 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
           }
         }
       }
+      if (t.tlen <= 0) continue;  // a token tile past the batch: nothing to store
       const int buf = ui & 1;
       // ---- operand (s * v, bf16 hi + lo, K-major, 2*RP-byte swizzle) of each long segment
 #pragma unroll
@@ -478,10 +564,15 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.acc_empty[buf]);
+      ++ui;
     }
   }
   tc_fence_before();
   __syncthreads();
+  if (CM > 1) {  // no CTA leaves while a peer may still copy or commit into it
+    cluster_arrive_relaxed();
+    cluster_wait_acquire();
+  }
   if (warp == 5) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -516,36 +607,57 @@ lora_status launch_gemm_lora_r(GlParams& prm, const void* x, int64_t ldx, const 
     const uint32_t box[3] = {64, static_cast<uint32_t>(GlCfg<R>::RP), 1};
     if ((s = encode_tmap_bf16(&prm.tmB, B_pool, 3, dims, str, box, 128)) != LORA_OK) return s;
   }
-  auto kern = gemm_lora_kernel<R>;
+  auto kern = gemm_lora_kernel<R, kGlCM>;
   const size_t smem = sizeof(GlSmem<R>);
   static std::mutex mu;
-  static int nsm_cache[64];
+  static int groups_cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
-  int nsm = 0;
+  int clusters = 0;
   {
     std::lock_guard<std::mutex> lk(mu);
-    nsm = nsm_cache[dev & 63];
+    clusters = groups_cache[dev & 63];
   }
-  if (nsm == 0) {
+  cudaLaunchAttribute at[2];
+  auto cluster_attr = [&](cudaLaunchAttribute& a) {
+    a.id = cudaLaunchAttributeClusterDimension;
+    a.val.clusterDim.x = kGlCM;
+    a.val.clusterDim.y = 1;
+    a.val.clusterDim.z = 1;
+  };
+  if (clusters == 0) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess)
       return LORA_ERR_CUDA;
-    if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return LORA_ERR_CUDA;
+    if (kGlCM > 1) {
+      cudaLaunchConfig_t occ{};
+      occ.gridDim = dim3(kGlCM * 64);
+      occ.blockDim = dim3(kGlThreads);
+      occ.dynamicSmemBytes = smem;
+      cluster_attr(at[0]);
+      occ.attrs = at;
+      occ.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&clusters, kern, &occ) != cudaSuccess) return LORA_ERR_CUDA;
+    } else if (cudaDeviceGetAttribute(&clusters, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      return LORA_ERR_CUDA;
+    }
+    clusters = std::max(1, clusters);
     std::lock_guard<std::mutex> lk(mu);
-    nsm_cache[dev & 63] = nsm;
+    groups_cache[dev & 63] = clusters;
   }
-  const int units = t.m_tiles * t.n_tiles;
+  const int units = ceil_div(t.m_tiles, kGlCM) * t.n_tiles;
   cudaLaunchConfig_t cfg{};
-  cudaLaunchAttribute at[1];
-  cfg.gridDim = dim3(std::max(1, std::min(nsm, units)));
+  int na = 0;
+  cfg.gridDim = dim3(std::max(1, std::min(clusters, units)) * kGlCM);
   cfg.blockDim = dim3(kGlThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
+  if (kGlCM > 1) cluster_attr(at[na++]);
+  at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = na;
   return cuda_status(cudaLaunchKernelEx(&cfg, kern, prm));
 }
 

@@ -5,7 +5,8 @@
 // requests sit next to each other and form dense segments; "Summary":
 // requests of the same adapter are grouped.
 //
-// One CTA runs a stable counting sort.  Warp w owns the w-th contiguous chunk
+// One CTA runs a stable counting sort (batches of more than 256 tokens; smaller
+// ones take the rank sort below, which needs no histogram over the pool).  Warp w owns the w-th contiguous chunk
 // of tokens and one histogram row H[w][0..P] (bucket P collects invalid ids,
 // so they land after every valid token).  Steps: per-warp counts (warp-match
 // aggregated, no atomics: the row is private to the warp), per-key exclusive
@@ -27,8 +28,17 @@ namespace lsg {
 constexpr size_t kSegSmemBudget = 200 * 1024;
 constexpr int kSegScratchInts = 128;  // block-scan partials, in shared memory
 
+constexpr int kSegRankTokens = 256;  // batches up to this size take the rank sort (no histogram)
+
 SegPlan seg_plan(int n, int P) {
   SegPlan pl{};
+  if (n >= 1 && n <= kSegRankTokens) {  // the rank sort's batches (an empty batch takes the counting sort)
+    pl.nw = 1;
+    pl.gmem = false;
+    pl.ws_bytes = 0;
+    pl.smem_bytes = 0;
+    return pl;
+  }
   const int want = std::clamp(std::max(ceil_div(std::max(n, 1), 64), ceil_div(P + 1, 256)), 1, 32);
   const size_t row = static_cast<size_t>(P + 1) * sizeof(int32_t);
   const size_t scratch = kSegScratchInts * sizeof(int32_t);
@@ -183,9 +193,74 @@ __global__ void __launch_bounds__(1024)
   }
 }
 
+// The same segmentation for a small batch (n <= kSegRankMaxTokens), one thread
+// per token and no histogram over the pool: token i's place in the stable
+// order is the number of tokens that sort before it (a smaller id, or the
+// same id and a smaller index), counted over all ids in shared memory; the
+// first token of each valid id starts a segment, whose index is the number of
+// such first tokens with a smaller id.  Ids outside [0, P) sort as P.
+constexpr int kSegRankMaxTokens = kSegRankTokens;
+
+__global__ void __launch_bounds__(kSegRankMaxTokens)
+    lora_segment_rank_kernel(const int32_t* __restrict__ ids, int n, int P, int max_segments,
+                             int32_t* __restrict__ perm, int32_t* __restrict__ seg_offsets,
+                             int32_t* __restrict__ seg_adapter, int32_t* __restrict__ num_segments,
+                             int32_t* err_flag) {
+  __shared__ int32_t keys[kSegRankMaxTokens];
+  __shared__ int32_t lead_keys[kSegRankMaxTokens];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int i = threadIdx.x;
+  constexpr int kPad = 0x7fffffff;  // threads past n: after every token
+  int key = kPad;
+  bool bad = false;
+  if (i < n) {
+    const int id = ids[i];
+    bad = id < 0 || id >= P;
+    key = bad ? P : id;
+  }
+  keys[i] = key;
+  __syncthreads();
+  int before = 0, same_before = 0;
+  for (int j = 0; j < n; ++j) {
+    const int kj = keys[j];
+    before += kj < key;
+    same_before += (kj == key) & (j < i);
+  }
+  const bool lead = i < n && key < P && same_before == 0;
+  lead_keys[i] = lead ? key : kPad;
+  const int S = __syncthreads_count(lead);
+  const int n_valid = __syncthreads_count(i < n && key < P);
+  if (bad) set_err(err_flag, LORA_ERR_BAD_ADAPTER_ID);
+  if (i < n) perm[before + same_before] = i;
+  if (lead) {
+    int seg = 0;
+    for (int j = 0; j < n; ++j) seg += lead_keys[j] < key;
+    seg_adapter[seg] = key;
+    seg_offsets[seg] = before;
+  }
+  for (int x = S + i; x <= max_segments; x += blockDim.x) seg_offsets[x] = n_valid;
+  for (int x = S + i; x < max_segments; x += blockDim.x) seg_adapter[x] = -1;
+  if (i == 0) *num_segments = S;
+}
+
 lora_status launch_segment(const int32_t* ids, int n, int P, int32_t* perm, int32_t* seg_offsets,
                            int32_t* seg_adapter, int32_t* num_segments, int32_t* hist, int32_t* err_flag,
                            cudaStream_t stream) {
+  if (n >= 1 && n <= kSegRankMaxTokens) {
+    // small batch: the rank sort (needs no workspace whatever the pool)
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute at[1];
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(static_cast<unsigned>(round_up(n, 32)));
+    cfg.stream = stream;
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, lora_segment_rank_kernel, ids, n, P, std::min(n, P), perm,
+                                          seg_offsets, seg_adapter, num_segments, err_flag));
+  }
   static std::once_flag once[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
@@ -196,6 +271,11 @@ lora_status launch_segment(const int32_t* ids, int n, int P, int32_t* perm, int3
   });
   if (attr_err != cudaSuccess) return LORA_ERR_CUDA;
   const SegPlan pl = seg_plan(n, P);
+  // the counting sort's rows (nw + 1 of P + 1 ints) and scan scratch must fit the
+  // shared memory it is given (rows in the workspace: the scratch alone)
+  const size_t rows_bytes = static_cast<size_t>(pl.nw + 1) * (static_cast<size_t>(P) + 1) * sizeof(int32_t);
+  const size_t need = (pl.gmem ? 0 : rows_bytes) + kSegScratchInts * sizeof(int32_t);
+  if (pl.smem_bytes < need || (pl.gmem && hist == nullptr)) return LORA_ERR_UNSUPPORTED;
   const int max_segments = std::min(n, P);
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute at[1];

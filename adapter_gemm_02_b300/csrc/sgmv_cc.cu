@@ -83,6 +83,17 @@ namespace lsg {
 #ifndef LSG_CC_KB_R8
 #define LSG_CC_KB_R8 16
 #endif
+#ifndef LSG_CC_STAGES_R32
+#define LSG_CC_STAGES_R32 LSG_CC_STAGES_SMALL
+#endif
+#ifndef LSG_CC_KB_R32
+#define LSG_CC_KB_R32 LSG_CC_KB_SMALL
+#endif
+// Tiles of 4 tokens when segments hold at most this many tokens on average
+// (the tokens per possible segment), else of 16.
+#ifndef LSG_CC_T4_MAX_AVG
+#define LSG_CC_T4_MAX_AVG 3.0
+#endif
 #ifndef LSG_CC_WARPS
 #define LSG_CC_WARPS 4
 #endif
@@ -187,8 +198,12 @@ struct CCParams {
 // Rank R's stage contents in a ring shaped for rank RM >= R.
 template <int R, int T, int RM = R>
 struct CCCfg {
-  static constexpr int kStages = RM >= 64 ? LSG_CC_STAGES_BIG : RM == 8 ? LSG_CC_STAGES_R8 : LSG_CC_STAGES_SMALL;
-  static constexpr int kStageBytes = (RM >= 64 ? LSG_CC_KB_BIG : RM == 8 ? LSG_CC_KB_R8 : LSG_CC_KB_SMALL) * 1024;
+  static constexpr int kStages = RM >= 64   ? LSG_CC_STAGES_BIG
+                                : RM == 8  ? LSG_CC_STAGES_R8
+                                : RM == 32 ? LSG_CC_STAGES_R32
+                                           : LSG_CC_STAGES_SMALL;
+  static constexpr int kStageBytes =
+      (RM >= 64 ? LSG_CC_KB_BIG : RM == 8 ? LSG_CC_KB_R8 : RM == 32 ? LSG_CC_KB_R32 : LSG_CC_KB_SMALL) * 1024;
   // shrink: A rows per stage (A part + x part fit a stage), whole k-steps of
   // 16, made of NBA TMA boxes of BA rows (a box extent is at most 256)
   static constexpr int WS0 = (((kStageBytes - T * 16) / ((R + T) * 2)) / 16) * 16;
@@ -1222,7 +1237,7 @@ lora_status launch_sgmv_cc(const SgmvCall& call, cudaStream_t stream) {
   const int C = std::clamp(ceil_div(hmax, LSG_CC_ROWS_PER_CTA), 1, kMaxC);
   // tokens per tile (MMA rows): small tiles when segments are short on average
   const double avg = static_cast<double>(n) / std::max(1, std::min(n, call.n_adapters));
-  const int T = avg <= 3.0 ? 4 : 16;
+  const int T = avg <= LSG_CC_T4_MAX_AVG ? 4 : 16;
 
   CCParams prm{};
   for (int i = 0; i < call.n_proj; ++i) {

@@ -40,9 +40,11 @@
 // decode kernel skips exactly these).  A segment whose rows are contiguous in
 // x / y (prefill requests) moves whole tiles with 2-D tensor copies; any other
 // segment (tokens of one adapter spread over the batch) gathers its rows
-// through the permutation, four rows per tile::gather4 tensor copy, and its
-// updated y rows go back by tile::scatter4 tensor stores (rows of an
-// incomplete group of four by 16-byte stores).
+// through the permutation: the producer warp copies them into the swizzled
+// tile with 16-byte cp.async copies (a four-row tensor gather per lane ran at
+// half the sorted batch's rate), and the updated y rows go back by
+// tile::scatter4 tensor stores (rows of an incomplete group of four by
+// 16-byte stores).
 //
 // Rank 8 runs at an MMA width of 16: the shrink's N = 16 columns read the A
 // tile's 8 columns plus 8 columns of other shared memory, whose results are
@@ -81,6 +83,12 @@ static_assert(kBN == 64, "expand block: two epilogue groups of 32 columns");
 #define LSG_TC_EX_STAGES 4
 #endif
 constexpr int kExStages = LSG_TC_EX_STAGES;
+// Gathered tiles: 1 = eight lanes copy one 128-byte row (four whole rows per
+// warp instruction, for loads and for the y stores), 0 = one lane per row
+// (four-row tensor scatters for the y stores).
+#ifndef LSG_TC_GATHER_COAL
+#define LSG_TC_GATHER_COAL 0
+#endif
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemV = 0;      // v accumulator: columns [0, r)
 constexpr uint32_t kTmemAcc = 128;  // expand accumulators: [128, 256), [256, 384)
@@ -98,7 +106,9 @@ __device__ __forceinline__ bool withhold(int) { return false; }
 #endif
 
 struct TcProj {
-  uint16_t* y;  // for the direct stores of a tile's last rows and of gathered rows
+  const uint16_t* x;  // gathered tiles' x rows (copied by the producer)
+  int64_t ldx;
+  uint16_t* y;  // gathered tiles' y rows, and the direct stores of a tile's last rows
   int64_t ldy;
   int32_t h_in, h_out;
   int32_t chunk;  // columns per chunk (multiple of 128)
@@ -134,11 +144,10 @@ struct TcTail {
 
 struct TcParams {
   CUtensorMap tmX[kMaxProj];   // x [n][h_in], box {64, 128}, 128 B swizzle
-  CUtensorMap tmXg[kMaxProj];  // x, box {64, 1} (four-row gathers), 128 B swizzle
   CUtensorMap tmA[kMaxProj];   // A slabs [n_slabs][h_in][r] (slab stride h_in*rmax), box {r, 64, 1}, 2r B swizzle
   CUtensorMap tmB[kMaxProj];   // B rows [n_slabs*rmax][h_out], box {64, r}, 128 B swizzle
   CUtensorMap tmYl[kMaxProj];  // y [n][h_out], box {64, 128}, 128 B swizzle (load)
-  CUtensorMap tmYg[kMaxProj];  // y, box {64, 1} (four-row gathers), 128 B swizzle
+  CUtensorMap tmYg[kMaxProj];  // y, box {64, 1} (four-row scatters), 128 B swizzle
   CUtensorMap tmYs[kMaxProj];  // y, box {64, 32}, 128 B swizzle (store)
   TcTail t;
 };
@@ -172,6 +181,7 @@ struct TcSmem {
   alignas(1024) uint8_t vop[2][TcCfg<R>::kVop];  // hi, lo
   alignas(16) float rbuf[CL ? 128 * R : 4];      // partial v rows this CTA owns: [source rank][row][r]
   alignas(16) TcTail t;
+  int32_t grow[2][128];  // gathered tile's rows (-1: none): [0] shrink producer, [1] expand producer
   alignas(8) uint64_t sh_full[kSh];
   uint64_t sh_empty[kSh];
   uint64_t ex_full[kEx];
@@ -275,18 +285,57 @@ struct TcCursor {
   }
 };
 
-// Rows 4*lane .. 4*lane+3 of a gathered tile, for a four-row gather: rows past
-// the tile or outside [0, n) read a valid row of the tile instead (their
-// results are never stored).  Executed by a full warp.
+// x / y rows of tile rows 4*lane .. 4*lane+3 of a gathered tile; -1 for rows
+// past the tile or with a permutation entry outside [0, n) (zero-filled,
+// never stored).
 __device__ __forceinline__ void tile_rows4(const TcTail& q, const TcTile& t, int lane, int (&rr)[4]) {
-  int first = t.tlen > 0 ? q.perm[t.t0] : 0;
-  if (first < 0 || first >= q.n_tokens) first = 0;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int i = 4 * lane + j;
-    int r = i < t.tlen ? q.perm[t.t0 + i] : first;
-    rr[j] = (r >= 0 && r < q.n_tokens) ? r : first;
+    const int r = i < t.tlen ? q.perm[t.t0 + i] : -1;
+    rr[j] = (r >= 0 && r < q.n_tokens) ? r : -1;
   }
+}
+
+// Gathered rows 4*lane .. 4*lane+3 of a [128][64] bf16 tile (128 B rows, 128 B
+// swizzle: 16-byte chunk c of row m at chunk c ^ (m & 7)): columns [c0, c0+64)
+// of the given rows of a [n][ld] matrix of `width` columns, by 16-byte
+// cp.async copies; chunks past `width` and rows of -1 are zero-filled.  Then
+// this lane's arrival on `bar` once its copies have landed.
+__device__ __forceinline__ void gather_rows_cp_async(uint8_t* tile, const uint16_t* base, int64_t ld, int width,
+                                                     int c0, const int (&rr)[4], int lane, uint64_t* bar) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int m = 4 * lane + j;
+    const uint32_t drow = smem_u32(tile) + static_cast<uint32_t>(m) * 128;
+    const uint16_t* srow = base + static_cast<int64_t>(rr[j] >= 0 ? rr[j] : 0) * ld + c0;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const bool ok = rr[j] >= 0 && c0 + c * 8 < width;
+      cp_async16(drow + ((static_cast<uint32_t>(c) ^ (static_cast<uint32_t>(m) & 7u)) << 4), ok ? srow + c * 8 : base,
+                 ok ? 16u : 0u);
+    }
+  }
+  cp_async_mbar_arrive(bar);
+}
+
+// The same copy with eight lanes per row: lane l copies 16-byte chunk l & 7
+// of tile rows 4i + (l >> 3), i = 0..31, whose source rows `rows` lists
+// (-1: zero-filled).  Each warp instruction moves four whole 128-byte rows.
+__device__ __forceinline__ void gather_rows_coal(uint8_t* tile, const uint16_t* base, int64_t ld, int width, int c0,
+                                                 const int32_t* rows, int lane, uint64_t* bar) {
+  const uint32_t c = static_cast<uint32_t>(lane & 7);
+  const bool col_ok = c0 + static_cast<int>(c) * 8 < width;
+  const uint32_t t0 = smem_u32(tile);
+#pragma unroll 8
+  for (int i = 0; i < 32; ++i) {
+    const int m = 4 * i + (lane >> 3);
+    const int r = rows[m];
+    const bool ok = col_ok && r >= 0;
+    cp_async16(t0 + static_cast<uint32_t>(m) * 128 + ((c ^ (static_cast<uint32_t>(m) & 7u)) << 4),
+               ok ? base + static_cast<int64_t>(r) * ld + c0 + c * 8 : base, ok ? 16u : 0u);
+  }
+  cp_async_mbar_arrive(bar);
 }
 
 // Bounded wait by lane 0, result broadcast to the warp; a time-out sets the
@@ -337,7 +386,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
   }
   if (warp == 4 && lane < kMaxProj) {
     prefetch_tmap(&p.tmX[lane]);
-    prefetch_tmap(&p.tmXg[lane]);
     prefetch_tmap(&p.tmA[lane]);
   }
   if (warp == 5 && lane < kMaxProj) {
@@ -406,20 +454,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       int kb0, kb1;
       split((q.proj[pj].h_in + 63) >> 6, kb0, kb1);
       int rr[4] = {0, 0, 0, 0};
-      if (t.row < 0) tile_rows4(q, t, lane, rr);
+      if (t.row < 0) {
+        tile_rows4(q, t, lane, rr);
+        if (LSG_TC_GATHER_COAL) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) sm.grow[0][4 * lane + j] = rr[j];
+          __syncwarp();
+        }
+      }
       bool ok = true;
       for (int kb = kb0; kb < kb1 && ok; ++kb) {
         ok = warp_wait(sm, &sm.sh_empty[slot], ph ^ 1u, lane);
         if (!ok) break;
         uint8_t* st = sm.sh[slot];
+        // gathered rows: every lane copies its four rows and arrives (before
+        // the producer's own arrival, so the phase waits for them)
+        if (t.row < 0) {
+          if (LSG_TC_GATHER_COAL)
+            gather_rows_coal(st, q.proj[pj].x, q.proj[pj].ldx, q.proj[pj].h_in, kb * 64, sm.grow[0], lane,
+                             &sm.sh_full[slot]);
+          else
+            gather_rows_cp_async(st, q.proj[pj].x, q.proj[pj].ldx, q.proj[pj].h_in, kb * 64, rr, lane,
+                                 &sm.sh_full[slot]);
+        }
+        __syncwarp();
         if (lane == 0) {
-          mbar_arrive_expect_tx(&sm.sh_full[slot], 16384u + Cfg::kShA);
+          mbar_arrive_expect_tx(&sm.sh_full[slot], (t.row >= 0 ? 16384u : 0u) + Cfg::kShA);
           if (t.row >= 0) tma_load_2d(st, &p.tmX[pj], kb * 64, t.row, &sm.sh_full[slot]);
           tma_load_3d(st + 16384, &p.tmA[pj], 0, kb * 64, t.a, &sm.sh_full[slot]);
         }
-        __syncwarp();  // the stage's byte count is registered before the gathers land
-        if (t.row < 0)
-          tma_gather4(st + lane * 512, &p.tmXg[pj], kb * 64, rr[0], rr[1], rr[2], rr[3], &sm.sh_full[slot]);
         __syncwarp();
         filled |= 1u << slot;
         fill_par = (fill_par & ~(1u << slot)) | (ph << slot);
@@ -450,27 +513,37 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       int b0, b1;
       split((min(pr.chunk, pr.h_out - c0) + kBN - 1) / kBN, b0, b1);
       int rr[4] = {0, 0, 0, 0};
-      if (t.row < 0) tile_rows4(q, t, lane, rr);
+      if (t.row < 0) {
+        tile_rows4(q, t, lane, rr);
+        if (LSG_TC_GATHER_COAL) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) sm.grow[1][4 * lane + j] = rr[j];
+          __syncwarp();
+        }
+      }
       bool ok = true;
       for (int b = b0; b < b1 && ok; ++b) {
         ok = warp_wait(sm, &sm.ex_empty[slot], ph ^ 1u, lane);
         if (!ok) break;
         uint8_t* st = sm.ex[slot];
         const int c = c0 + b * kBN;
+        if (t.row < 0) {
+          // gathered rows by every lane (arrivals before the producer's own)
+          static_assert(kBH == 1, "one 64-column half per block");
+          if (LSG_TC_GATHER_COAL)
+            gather_rows_coal(st, pr.y, pr.ldy, pr.h_out, c, sm.grow[1], lane, &sm.ex_full[slot]);
+          else
+            gather_rows_cp_async(st, pr.y, pr.ldy, pr.h_out, c, rr, lane, &sm.ex_full[slot]);
+        }
+        __syncwarp();
         if (lane == 0) {
-          mbar_arrive_expect_tx(&sm.ex_full[slot], static_cast<uint32_t>(Cfg::kExY + Cfg::kExBCopy));
+          mbar_arrive_expect_tx(&sm.ex_full[slot],
+                                static_cast<uint32_t>((t.row >= 0 ? Cfg::kExY : 0) + Cfg::kExBCopy));
 #pragma unroll
           for (int h = 0; h < kBH; ++h) {
             if (t.row >= 0) tma_load_2d(st + h * 16384, &p.tmYl[pj], c + h * 64, t.row, &sm.ex_full[slot]);
             tma_load_2d(st + Cfg::kExY + h * RP * 128, &p.tmB[pj], c + h * 64, t.a * q.rmax, &sm.ex_full[slot]);
           }
-        }
-        __syncwarp();  // the stage's byte count is registered before the gathers land
-        if (t.row < 0) {
-#pragma unroll
-          for (int h = 0; h < kBH; ++h)
-            tma_gather4(st + h * 16384 + lane * 512, &p.tmYg[pj], c + h * 64, rr[0], rr[1], rr[2], rr[3],
-                        &sm.ex_full[slot]);
         }
         __syncwarp();
         filled |= 1u << slot;
@@ -507,6 +580,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       for (int kb = kb0; kb < kb1 && ok; ++kb) {
         ok = warp_wait(sm, &sm.sh_full[sslot], sph, lane);
         if (!ok) break;
+        if (t.row < 0) fence_proxy_async_smem();  // gathered x rows were written by cp.async (generic proxy)
         tc_fence_after();
         if (lane == 0) {
           const uint32_t xs = smem_u32(sm.sh[sslot]), as = xs + 16384;
@@ -794,11 +868,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
         // gathered tile: rows in a group of four valid rows go out by one
         // four-row scatter (lane j of the quarter's warp: rows 4j .. 4j+3)
         const unsigned vmask = __ballot_sync(0xffffffffu, yrow >= 0);
-        const bool by_tensor_store = contig ? m < full_rows : ((vmask >> (lane & ~3)) & 0xFu) == 0xFu;
+        const bool by_tensor_store =
+            contig ? m < full_rows : (LSG_TC_GATHER_COAL || ((vmask >> (lane & ~3)) & 0xFu) == 0xFu);
         int yr4[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) yr4[k] = __shfl_sync(0xffffffffu, yrow, (4 * lane + k) & 31);
-        const bool scatter_lane = !contig && lane < 8 && ((vmask >> (4 * lane)) & 0xFu) == 0xFu;
+        const bool scatter_lane =
+            !LSG_TC_GATHER_COAL && !contig && lane < 8 && ((vmask >> (4 * lane)) & 0xFu) == 0xFu;
         for (int b = b0; b < b1 && ok; ++b) {
           const int buf = ae & 1;
           ok = warp_wait(sm, &sm.acc_full[buf], (ae >> 1) & 1, lane);
@@ -845,6 +921,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
           }
           fence_proxy_async_smem();  // our y updates, visible to the tensor stores
           named_bar_sync(3 + wq, 64);  // the two warps of this lane quarter are done with the block
+          if (LSG_TC_GATHER_COAL && !contig) {
+            // gathered tile: each warp of the quarter stores 16 of its rows,
+            // eight lanes per row (16-byte stores of the updated slot rows)
+            const uint32_t cc = static_cast<uint32_t>(lane & 7);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int src = eg * 16 + 4 * i + (lane >> 3);
+              const int r = __shfl_sync(0xffffffffu, yrow, src);
+              const uint32_t mm = static_cast<uint32_t>(wq * 32 + src);
+              if (r >= 0 && c + static_cast<int>(cc) * 8 < pr.h_out) {
+                uint32_t w[4];
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                             : "r"(smem_u32(st) + mm * 128 + ((cc ^ (mm & 7u)) << 4)));
+                *reinterpret_cast<uint4*>(pr.y + static_cast<int64_t>(r) * pr.ldy + c + cc * 8) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
+              }
+            }
+          }
           if (eg == 0) {
             // each lane quarter stores its own 32 rows: one 64-column box, or
             // four-row scatters of a gathered tile
@@ -946,9 +1041,8 @@ lora_status launch_tc_rc(TcParams& prm, const SgmvCall& call, int tiles_bound, c
     if (kHasShrink) {
       const uint64_t dims[2] = {static_cast<uint64_t>(a.h_in), n};
       const uint64_t str[1] = {static_cast<uint64_t>(a.ldx) * 2};
-      const uint32_t box[2] = {64, 128}, box_g[2] = {64, 1};
+      const uint32_t box[2] = {64, 128};
       if ((s = encode_tmap_bf16(&prm.tmX[i], a.x, 2, dims, str, box, 128)) != LORA_OK) return s;
-      if ((s = encode_tmap_bf16(&prm.tmXg[i], a.x, 2, dims, str, box_g, 128)) != LORA_OK) return s;
       const uint64_t adims[3] = {static_cast<uint64_t>(R), static_cast<uint64_t>(a.h_in),
                                  static_cast<uint64_t>(prm.t.n_slabs)};
       const uint64_t astr[2] = {static_cast<uint64_t>(R) * 2, static_cast<uint64_t>(a.h_in) * prm.t.rmax * 2};
@@ -1067,6 +1161,8 @@ lora_status plan_and_launch(const SgmvCall& call, cudaStream_t stream) {
   for (int i = 0; i < call.n_proj; ++i) {
     const ProjArgs& a = call.proj[i];
     TcProj& t = prm.t.proj[i];
+    t.x = a.x;
+    t.ldx = a.ldx;
     t.y = a.y;
     t.ldy = a.ldy;
     t.h_in = a.h_in;

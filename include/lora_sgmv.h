@@ -105,8 +105,9 @@ typedef struct {
 
 /*
  * Bytes of device workspace lora_segment needs for (n_tokens, n_adapters).
- * 0 when the per-warp histograms fit in shared memory (pools of up to ~25k
- * adapters); otherwise the histograms live in the workspace.
+ * 0 for batches of at most 256 tokens (ranked without a histogram over the
+ * pool) and when the per-warp histograms fit in shared memory (pools of up to
+ * ~25k adapters); otherwise the histograms live in the workspace.
  */
 LORA_API size_t lora_segment_workspace_bytes(int32_t n_tokens, int32_t n_adapters);
 
@@ -115,7 +116,9 @@ LORA_API size_t lora_segment_workspace_bytes(int32_t n_tokens, int32_t n_adapter
  * ideas" I2 (sort the batch by adapter) and "Summary" (requests of the same
  * adapter grouped).  A stable counting sort: histogram of ids over
  * [0, n_adapters), exclusive scan into segment offsets, compaction of the
- * non-empty adapters (ascending id), stable scatter of token indices.
+ * non-empty adapters (ascending id), stable scatter of token indices; a batch
+ * of at most 256 tokens is ranked directly (one thread per token counts the
+ * tokens that sort before it), with the same result.
  *   ids[n_tokens]      device int32 adapter ids.
  *   perm, seg_offsets, seg_adapter, num_segments: outputs as described for
  *                      lora_segments, sized with max_segments =
@@ -146,8 +149,9 @@ LORA_API lora_status lora_segment(const int32_t* ids, int32_t n_tokens, int32_t 
  * LORA_SEGMENT_NOALLOC_SCRATCH_BYTES (8 MiB) that every GPU which loads the
  * library holds until the process exits (under CUDA's lazy module loading the
  * array is reserved when the first call in a context loads the module that
- * holds it).  Pools needing more scratch than that
- * (more than about 63,500 adapters) return LORA_ERR_WORKSPACE without a launch.
+ * holds it).  Batches of more than 256 tokens over pools needing more scratch
+ * than that (more than about 63,500 adapters) return LORA_ERR_WORKSPACE
+ * without a launch.
  * The call allocates nothing.
  *  - The first call in each CUDA context (with its device current) looks up
  *    the array's device address and caches it for that context; make that

@@ -50,7 +50,8 @@ def test_segment_workspace_sizes(lib):
     # histograms fit shared memory for pools up to ~25k adapters
     assert lsg.lora_segment_workspace_bytes(256, 1000) == 0
     assert lsg.lora_segment_workspace_bytes(6224, 32) == 0
-    big = lsg.lora_segment_workspace_bytes(100, 60000)
+    assert lsg.lora_segment_workspace_bytes(100, 60000) == 0  # up to 256 tokens: ranked, no histogram
+    big = lsg.lora_segment_workspace_bytes(300, 60000)
     assert big >= 2 * 60001 * 4 and big % 4 == 0
     assert lsg.lora_segment_workspace_bytes(-1, 10) == 0
 
@@ -69,7 +70,7 @@ def test_host_validation_without_gpu(lib):
     assert lib.lora_segment(P(16), 4, 0, P(16), P(16), P(16), P(16), None, 0, None, None) == -1
     assert lib.lora_segment(P(16), 4, 4, P(16), None, P(16), P(16), None, 0, None, None) == -1
     # huge pool: workspace required
-    assert lib.lora_segment(P(16), 4, 60000, P(16), P(16), P(16), P(16), None, 0, None, None) == -5
+    assert lib.lora_segment(P(16), 300, 60000, P(16), P(16), P(16), P(16), None, 0, None, None) == -5
     # sgmv_*: null segmentation, unsupported rank, bad widths, misalignment, ld < width
     assert lib.sgmv_fused(P(256), 64, P(256), P(256), 4, 64, 64, 16, 1.0, None, P(256), 64, None, None) == -1
     assert lib.sgmv_fused(P(256), 64, P(256), P(256), 4, 64, 64, 12, 1.0, ctypes.byref(s), P(256), 64, None,
@@ -188,7 +189,8 @@ def test_one_call_step_validation_without_gpu(lib):
     assert f(arr, 1, 0, 16, *ok) == -1                                                        # no adapters
     assert f(arr, 1, 8, 16, None, 32, P(256), P(256), P(256), P(256), None, 0, None, None) == -1  # no ids
     assert f(arr, 1, 8, 16, P(258), 32, P(256), P(256), P(256), P(256), None, 0, None, None) == -2
-    assert f(arr, 1, 60000, 16, *ok) == -5                                                    # workspace
+    big = (P(256), 300, P(256), P(256), P(256), P(256), None, 0, None, None)  # > 256 tokens: histograms
+    assert f(arr, 1, 60000, 16, *big) == -5                                                   # workspace
     bad = (lsg.lora_sgmv.LoraProj * 1)()
     bad[0] = lsg.lora_sgmv.LoraProj(258, 256, 256, 256, 64, 64, 64, 64, 1.0)                 # x misaligned
     assert f(bad, 1, 8, 16, *ok) == -2
