@@ -61,10 +61,11 @@
 namespace lsg {
 
 // Ring shape per rank (build-time knobs, chosen by measurement on B300):
-// ranks 8-32 use two 24 KiB stages, so that one CTA's share of a decode item
-// (A rows + B columns + x/y pieces) is in flight at once and three to four
-// CTAs share an SM; r = 64, whose CTAs registers hold to two per SM, keeps
-// three 28 KiB stages in flight.
+// two stages, 16 KiB at r = 8, 24 KiB at r = 16 and 28 KiB at r = 32, so that
+// one CTA's share of a decode item (A rows + B columns + x/y pieces) is in
+// flight at once and three to four CTAs share an SM (larger r = 8 / 16 stages
+// and 32 or 40 KiB at r = 32 measured slower); r = 64, whose CTAs registers
+// hold to two per SM, keeps three 28 KiB stages in flight.
 #ifndef LSG_CC_STAGES_SMALL
 #define LSG_CC_STAGES_SMALL 2
 #endif
@@ -87,7 +88,7 @@ namespace lsg {
 #define LSG_CC_STAGES_R32 LSG_CC_STAGES_SMALL
 #endif
 #ifndef LSG_CC_KB_R32
-#define LSG_CC_KB_R32 LSG_CC_KB_SMALL
+#define LSG_CC_KB_R32 28
 #endif
 // Tiles of 4 tokens when segments hold at most this many tokens on average
 // (the tokens per possible segment), else of 16.

@@ -37,14 +37,15 @@
 // shared memory).  Each item recomputes its tile's shrink (x is re-read from
 // L2 by the items of the same tile), which keeps items of similar size for
 // load balance.  Every segment of at least kLongSeg tokens is taken here (the
-// decode kernel skips exactly these).  A segment whose rows are contiguous in
-// x / y (prefill requests) moves whole tiles with 2-D tensor copies; any other
-// segment (tokens of one adapter spread over the batch) gathers its rows
-// through the permutation: the producer warp copies them into the swizzled
-// tile with 16-byte cp.async copies (a four-row tensor gather per lane ran at
-// half the sorted batch's rate), and the updated y rows go back by
-// tile::scatter4 tensor stores (rows of an incomplete group of four by
-// 16-byte stores).
+// decode kernel skips exactly these).  A tile whose rows are contiguous in
+// x / y (a prefill request, or a run of one inside a segment of several
+// requests) moves with 2-D tensor copies; any other tile (tokens of one
+// adapter spread over the batch) gathers its rows through the permutation:
+// each producer lane loads four rows per stage by a tile::gather4 tensor copy
+// into the swizzled tile, and the updated y rows go back by tile::scatter4
+// tensor stores (rows of an incomplete group of four by 16-byte stores).
+// Gathered tiles run at about half the rate of contiguous ones: every 128-byte
+// row piece is its own request, against one 16 KB box.
 //
 // Rank 8 runs at an MMA width of 16: the shrink's N = 16 columns read the A
 // tile's 8 columns plus 8 columns of other shared memory, whose results are
@@ -83,12 +84,25 @@ static_assert(kBN == 64, "expand block: two epilogue groups of 32 columns");
 #define LSG_TC_EX_STAGES 4
 #endif
 constexpr int kExStages = LSG_TC_EX_STAGES;
-// Gathered tiles: 1 = eight lanes copy one 128-byte row (four whole rows per
-// warp instruction, for loads and for the y stores), 0 = one lane per row
-// (four-row tensor scatters for the y stores).
-#ifndef LSG_TC_GATHER_COAL
-#define LSG_TC_GATHER_COAL 0
+// the cluster variant's rings (its partial-v receive buffer takes their room)
+#ifndef LSG_TC_SH_STAGES_CL
+#define LSG_TC_SH_STAGES_CL 3
 #endif
+#ifndef LSG_TC_EX_STAGES_CL
+#define LSG_TC_EX_STAGES_CL 3
+#endif
+// Gathered tiles' x and y rows: 1 = four-row tensor gathers (one per lane and
+// stage), 0 = 16-byte cp.async copies by the producer's lanes (the full 13B
+// prefill layer with interleaved requests: 795 against 849 us).
+#ifndef LSG_TC_GATHER4
+#define LSG_TC_GATHER4 1
+#endif
+// 1: an expand slot goes back as soon as this block's y stores have read it;
+// 0: one block later (after the next block's stores are issued).
+#ifndef LSG_TC_RELEASE_EARLY
+#define LSG_TC_RELEASE_EARLY 1
+#endif
+
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemV = 0;      // v accumulator: columns [0, r)
 constexpr uint32_t kTmemAcc = 128;  // expand accumulators: [128, 256), [256, 384)
@@ -144,6 +158,7 @@ struct TcTail {
 
 struct TcParams {
   CUtensorMap tmX[kMaxProj];   // x [n][h_in], box {64, 128}, 128 B swizzle
+  CUtensorMap tmXg[kMaxProj];  // x, box {64, 1} (four-row gathers), 128 B swizzle
   CUtensorMap tmA[kMaxProj];   // A slabs [n_slabs][h_in][r] (slab stride h_in*rmax), box {r, 64, 1}, 2r B swizzle
   CUtensorMap tmB[kMaxProj];   // B rows [n_slabs*rmax][h_out], box {64, r}, 128 B swizzle
   CUtensorMap tmYl[kMaxProj];  // y [n][h_out], box {64, 128}, 128 B swizzle (load)
@@ -171,8 +186,8 @@ struct TcCfg {
 // buffer and takes one stage from each ring to make room for it.
 template <int R, bool CL>
 struct TcSmem {
-  static constexpr int kSh = CL ? kShStages - 1 : kShStages;
-  static constexpr int kEx = CL ? kExStages - 1 : kExStages;
+  static constexpr int kSh = CL ? LSG_TC_SH_STAGES_CL : kShStages;
+  static constexpr int kEx = CL ? LSG_TC_EX_STAGES_CL : kExStages;
   // the epilogue hands a slot back one block late, so each ring needs two
   // stages (an expand block of 128 columns leaves the cluster variant one)
   static_assert(kSh >= 2 && kEx >= 2, "ring depth");
@@ -181,7 +196,6 @@ struct TcSmem {
   alignas(1024) uint8_t vop[2][TcCfg<R>::kVop];  // hi, lo
   alignas(16) float rbuf[CL ? 128 * R : 4];      // partial v rows this CTA owns: [source rank][row][r]
   alignas(16) TcTail t;
-  int32_t grow[2][128];  // gathered tile's rows (-1: none): [0] shrink producer, [1] expand producer
   alignas(8) uint64_t sh_full[kSh];
   uint64_t sh_empty[kSh];
   uint64_t ex_full[kEx];
@@ -202,7 +216,7 @@ struct TcTile {
   int t0;    // position of its first token in the permutation
   int tlen;  // tokens (<= 128)
   int a;     // slab (adapter id, or slot with slot arenas)
-  int row;   // first x / y row when the segment's rows are contiguous, else -1 (rows through perm)
+  int row;   // first x / y row when the tile's rows are contiguous, else -1 (rows through perm)
 };
 
 // Cursor over the segments taken by this kernel (at least kLongSeg tokens),
@@ -275,6 +289,18 @@ struct TcCursor {
         out.tlen = min(128, l - k);
         out.t0 = o + k;
         out.row = r0 >= 0 ? r0 + k : -1;
+        if (r0 < 0) {
+          // a segment of several runs of rows (requests of one adapter apart
+          // in the batch): a tile inside one run still moves by 2-D tiles
+          int f = -1, b = -1;
+          if (lane == 0) {
+            f = q.perm[out.t0];
+            b = q.perm[out.t0 + out.tlen - 1];
+          }
+          f = __shfl_sync(0xffffffffu, f, 0);
+          b = __shfl_sync(0xffffffffu, b, 0);
+          if (f >= 0 && b < q.n_tokens && b - f == out.tlen - 1) out.row = f;
+        }
         return true;
       }
       tiles_before += total;
@@ -315,25 +341,6 @@ __device__ __forceinline__ void gather_rows_cp_async(uint8_t* tile, const uint16
       cp_async16(drow + ((static_cast<uint32_t>(c) ^ (static_cast<uint32_t>(m) & 7u)) << 4), ok ? srow + c * 8 : base,
                  ok ? 16u : 0u);
     }
-  }
-  cp_async_mbar_arrive(bar);
-}
-
-// The same copy with eight lanes per row: lane l copies 16-byte chunk l & 7
-// of tile rows 4i + (l >> 3), i = 0..31, whose source rows `rows` lists
-// (-1: zero-filled).  Each warp instruction moves four whole 128-byte rows.
-__device__ __forceinline__ void gather_rows_coal(uint8_t* tile, const uint16_t* base, int64_t ld, int width, int c0,
-                                                 const int32_t* rows, int lane, uint64_t* bar) {
-  const uint32_t c = static_cast<uint32_t>(lane & 7);
-  const bool col_ok = c0 + static_cast<int>(c) * 8 < width;
-  const uint32_t t0 = smem_u32(tile);
-#pragma unroll 8
-  for (int i = 0; i < 32; ++i) {
-    const int m = 4 * i + (lane >> 3);
-    const int r = rows[m];
-    const bool ok = col_ok && r >= 0;
-    cp_async16(t0 + static_cast<uint32_t>(m) * 128 + ((c ^ (static_cast<uint32_t>(m) & 7u)) << 4),
-               ok ? base + static_cast<int64_t>(r) * ld + c0 + c * 8 : base, ok ? 16u : 0u);
   }
   cp_async_mbar_arrive(bar);
 }
@@ -386,6 +393,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
   }
   if (warp == 4 && lane < kMaxProj) {
     prefetch_tmap(&p.tmX[lane]);
+    if (LSG_TC_GATHER4) prefetch_tmap(&p.tmXg[lane]);
     prefetch_tmap(&p.tmA[lane]);
   }
   if (warp == 5 && lane < kMaxProj) {
@@ -454,14 +462,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       int kb0, kb1;
       split((q.proj[pj].h_in + 63) >> 6, kb0, kb1);
       int rr[4] = {0, 0, 0, 0};
-      if (t.row < 0) {
-        tile_rows4(q, t, lane, rr);
-        if (LSG_TC_GATHER_COAL) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) sm.grow[0][4 * lane + j] = rr[j];
-          __syncwarp();
-        }
-      }
+      if (t.row < 0) tile_rows4(q, t, lane, rr);
       bool ok = true;
       for (int kb = kb0; kb < kb1 && ok; ++kb) {
         ok = warp_wait(sm, &sm.sh_empty[slot], ph ^ 1u, lane);
@@ -469,16 +470,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
         uint8_t* st = sm.sh[slot];
         // gathered rows: every lane copies its four rows and arrives (before
         // the producer's own arrival, so the phase waits for them)
-        if (t.row < 0) {
-          if (LSG_TC_GATHER_COAL)
-            gather_rows_coal(st, q.proj[pj].x, q.proj[pj].ldx, q.proj[pj].h_in, kb * 64, sm.grow[0], lane,
-                             &sm.sh_full[slot]);
-          else
-            gather_rows_cp_async(st, q.proj[pj].x, q.proj[pj].ldx, q.proj[pj].h_in, kb * 64, rr, lane,
-                                 &sm.sh_full[slot]);
-        }
+        if (t.row < 0 && !LSG_TC_GATHER4)
+          gather_rows_cp_async(st, q.proj[pj].x, q.proj[pj].ldx, q.proj[pj].h_in, kb * 64, rr, lane, &sm.sh_full[slot]);
         __syncwarp();
-        if (lane == 0) {
+        if (LSG_TC_GATHER4 && t.row < 0) {
+          // every byte of the stage arrives by tensor copies (rows past the
+          // tile read as zeros): expected before any is issued
+          if (lane == 0) mbar_arrive_expect_tx(&sm.sh_full[slot], 16384u + Cfg::kShA);
+          __syncwarp();
+          // rows of -1 (none) read past the tensor's last row: zeros
+          const int nr = q.n_tokens;
+          tma_gather4(st + lane * 512, &p.tmXg[pj], kb * 64, rr[0] < 0 ? nr : rr[0], rr[1] < 0 ? nr : rr[1],
+                      rr[2] < 0 ? nr : rr[2], rr[3] < 0 ? nr : rr[3], &sm.sh_full[slot]);
+          if (lane == 0) tma_load_3d(st + 16384, &p.tmA[pj], 0, kb * 64, t.a, &sm.sh_full[slot]);
+        } else if (lane == 0) {
           mbar_arrive_expect_tx(&sm.sh_full[slot], (t.row >= 0 ? 16384u : 0u) + Cfg::kShA);
           if (t.row >= 0) tma_load_2d(st, &p.tmX[pj], kb * 64, t.row, &sm.sh_full[slot]);
           tma_load_3d(st + 16384, &p.tmA[pj], 0, kb * 64, t.a, &sm.sh_full[slot]);
@@ -513,30 +518,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       int b0, b1;
       split((min(pr.chunk, pr.h_out - c0) + kBN - 1) / kBN, b0, b1);
       int rr[4] = {0, 0, 0, 0};
-      if (t.row < 0) {
-        tile_rows4(q, t, lane, rr);
-        if (LSG_TC_GATHER_COAL) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) sm.grow[1][4 * lane + j] = rr[j];
-          __syncwarp();
-        }
-      }
+      if (t.row < 0) tile_rows4(q, t, lane, rr);
       bool ok = true;
       for (int b = b0; b < b1 && ok; ++b) {
         ok = warp_wait(sm, &sm.ex_empty[slot], ph ^ 1u, lane);
         if (!ok) break;
         uint8_t* st = sm.ex[slot];
         const int c = c0 + b * kBN;
-        if (t.row < 0) {
+        if (t.row < 0 && !LSG_TC_GATHER4) {
           // gathered rows by every lane (arrivals before the producer's own)
           static_assert(kBH == 1, "one 64-column half per block");
-          if (LSG_TC_GATHER_COAL)
-            gather_rows_coal(st, pr.y, pr.ldy, pr.h_out, c, sm.grow[1], lane, &sm.ex_full[slot]);
-          else
-            gather_rows_cp_async(st, pr.y, pr.ldy, pr.h_out, c, rr, lane, &sm.ex_full[slot]);
+          gather_rows_cp_async(st, pr.y, pr.ldy, pr.h_out, c, rr, lane, &sm.ex_full[slot]);
         }
         __syncwarp();
-        if (lane == 0) {
+        if (LSG_TC_GATHER4 && t.row < 0) {
+          if (lane == 0) mbar_arrive_expect_tx(&sm.ex_full[slot], static_cast<uint32_t>(Cfg::kExY + Cfg::kExBCopy));
+          __syncwarp();
+          const int nr = q.n_tokens;
+          tma_gather4(st + lane * 512, &p.tmYg[pj], c, rr[0] < 0 ? nr : rr[0], rr[1] < 0 ? nr : rr[1],
+                      rr[2] < 0 ? nr : rr[2], rr[3] < 0 ? nr : rr[3], &sm.ex_full[slot]);
+          if (lane == 0) tma_load_2d(st + Cfg::kExY, &p.tmB[pj], c, t.a * q.rmax, &sm.ex_full[slot]);
+        } else if (lane == 0) {
           mbar_arrive_expect_tx(&sm.ex_full[slot],
                                 static_cast<uint32_t>((t.row >= 0 ? Cfg::kExY : 0) + Cfg::kExBCopy));
 #pragma unroll
@@ -868,13 +870,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
         // gathered tile: rows in a group of four valid rows go out by one
         // four-row scatter (lane j of the quarter's warp: rows 4j .. 4j+3)
         const unsigned vmask = __ballot_sync(0xffffffffu, yrow >= 0);
-        const bool by_tensor_store =
-            contig ? m < full_rows : (LSG_TC_GATHER_COAL || ((vmask >> (lane & ~3)) & 0xFu) == 0xFu);
+        const bool by_tensor_store = contig ? m < full_rows : ((vmask >> (lane & ~3)) & 0xFu) == 0xFu;
         int yr4[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) yr4[k] = __shfl_sync(0xffffffffu, yrow, (4 * lane + k) & 31);
-        const bool scatter_lane =
-            !LSG_TC_GATHER_COAL && !contig && lane < 8 && ((vmask >> (4 * lane)) & 0xFu) == 0xFu;
+        const bool scatter_lane = !contig && lane < 8 && ((vmask >> (4 * lane)) & 0xFu) == 0xFu;
         for (int b = b0; b < b1 && ok; ++b) {
           const int buf = ae & 1;
           ok = warp_wait(sm, &sm.acc_full[buf], (ae >> 1) & 1, lane);
@@ -921,25 +921,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
           }
           fence_proxy_async_smem();  // our y updates, visible to the tensor stores
           named_bar_sync(3 + wq, 64);  // the two warps of this lane quarter are done with the block
-          if (LSG_TC_GATHER_COAL && !contig) {
-            // gathered tile: each warp of the quarter stores 16 of its rows,
-            // eight lanes per row (16-byte stores of the updated slot rows)
-            const uint32_t cc = static_cast<uint32_t>(lane & 7);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int src = eg * 16 + 4 * i + (lane >> 3);
-              const int r = __shfl_sync(0xffffffffu, yrow, src);
-              const uint32_t mm = static_cast<uint32_t>(wq * 32 + src);
-              if (r >= 0 && c + static_cast<int>(cc) * 8 < pr.h_out) {
-                uint32_t w[4];
-                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                             : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-                             : "r"(smem_u32(st) + mm * 128 + ((cc ^ (mm & 7u)) << 4)));
-                *reinterpret_cast<uint4*>(pr.y + static_cast<int64_t>(r) * pr.ldy + c + cc * 8) =
-                    make_uint4(w[0], w[1], w[2], w[3]);
-              }
-            }
-          }
           if (eg == 0) {
             // each lane quarter stores its own 32 rows: one 64-column box, or
             // four-row scatters of a gathered tile
@@ -948,9 +929,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
             if (scatter_lane && c < pr.h_out)
               tma_scatter4(&p.tmYg[pj], c, yr4[0], yr4[1], yr4[2], yr4[3], st + (g + 4 * lane) * 128);
             bulk_commit();
-            // the previous block's stores have read their slot (this block's may
-            // still be reading): this quarter's share of that slot goes back
-            if (pend >= 0) {
+            if (LSG_TC_RELEASE_EARLY) {
+              bulk_wait_read0();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&sm.ex_empty[xslot]);  // y rows read by the stores, B tile by the MMAs
+            } else if (pend >= 0) {
+              // the previous block's stores have read their slot (this block's may
+              // still be reading): this quarter's share of that slot goes back
               bulk_wait_read1();
               __syncwarp();
               if (lane == 0) mbar_arrive(&sm.ex_empty[pend]);  // y rows read by the stores, B tile read by the MMAs
@@ -1043,6 +1028,10 @@ lora_status launch_tc_rc(TcParams& prm, const SgmvCall& call, int tiles_bound, c
       const uint64_t str[1] = {static_cast<uint64_t>(a.ldx) * 2};
       const uint32_t box[2] = {64, 128};
       if ((s = encode_tmap_bf16(&prm.tmX[i], a.x, 2, dims, str, box, 128)) != LORA_OK) return s;
+      if (LSG_TC_GATHER4) {
+        const uint32_t box_g[2] = {64, 1};
+        if ((s = encode_tmap_bf16(&prm.tmXg[i], a.x, 2, dims, str, box_g, 128)) != LORA_OK) return s;
+      }
       const uint64_t adims[3] = {static_cast<uint64_t>(R), static_cast<uint64_t>(a.h_in),
                                  static_cast<uint64_t>(prm.t.n_slabs)};
       const uint64_t astr[2] = {static_cast<uint64_t>(R) * 2, static_cast<uint64_t>(a.h_in) * prm.t.rmax * 2};

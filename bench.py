@@ -749,7 +749,8 @@ def per_config(K, Wm, dev, lsg, max_copies, peak):
     Llama2-7B decode layer, the Llama2-13B prefill batch, the Llama2-70B
     decode batches at ranks 8-64), each with its own L2 rotation.
     step_us: one sgmv_multi_segment call (segmentation + SGMV); sgmv_us: the
-    SGMV launches alone (segmentation given); kernel_us: the step when it is
+    SGMV launches alone (segmentation given); segment_us: lora_segment alone
+    (n ids, P adapters); kernel_us: the step when it is
     one launch, else the SGMV launches.  Each is the median of 7 replays of a
     K-call graph, timed with CUDA events on the replay stream."""
     import torch
@@ -779,13 +780,17 @@ def per_config(K, Wm, dev, lsg, max_copies, peak):
             inp, seg, projs, cp = copies[k % NB]
             lsg.sgmv_multi(projs, seg, err_flag=err, c_projs=cp)
 
+        def segment(k):
+            inp, seg, projs, cp = copies[k % NB]
+            lsg.lora_segment(inp.ids, wl.P, out=seg, workspace=ws, err_flag=err)
+
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
             for k in range(max(Wm, NB)):
                 step(k)
         torch.cuda.synchronize()
         graphs = []
-        for fn in (step, sgmv):
+        for fn in (step, sgmv, segment):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=side):
                 for k in range(K):
@@ -793,11 +798,13 @@ def per_config(K, Wm, dev, lsg, max_copies, peak):
             graphs.append(g)
         step_ms = _time_graph_median(graphs[0], side, settle_s=0.2)[0] / K
         sgmv_ms = _time_graph_median(graphs[1], side)[0] / K
+        seg_ms = _time_graph_median(graphs[2], side)[0] / K
         assert int(err.item()) == 0, f"{name}: device error flag {int(err.item())}"
         kern_ms = step_ms if one_launch(wl) else sgmv_ms
         kname = dominant_kernel(wl)
         gbs = ab / (kern_ms * 1e-3) / 1e9
         out[name] = {"step_us": round(step_ms * 1e3, 3), "sgmv_us": round(sgmv_ms * 1e3, 3),
+                     "segment_us": round(seg_ms * 1e3, 3),
                      "kernel_us": round(kern_ms * 1e3, 3), "kernel": kname,
                      "launches_per_step": launches_per_step(wl), "algorithmic_bytes": int(ab), "flops": int(nf),
                      "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),

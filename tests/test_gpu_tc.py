@@ -1,7 +1,7 @@
 """Long-segment (prefill) batches through sgmv_fused / sgmv_multi /
 sgmv_shrink / sgmv_expand against the oracle.  Segments of at least 64 tokens
-take the tensor-tile kernel: contiguous ones by whole-tile tensor copies,
-interleaved ones (tokens of one adapter spread over the batch) by four-row
+take the tensor-tile kernel: tiles of contiguous rows by whole-tile tensor
+copies, others (tokens of one adapter spread over the batch) by four-row
 gathers through the permutation; short segments take the split-K kernel in
 the same call, so these batches exercise the split of one batch between the
 two and the edges of the 128-token tiles."""
@@ -204,6 +204,43 @@ def test_interleaved_prefill_requests_every_row(r):
     lens = [300, 128, 257, 190, 64, 333, 200, 192]
     ids = _interleaved_requests(rng, lens, [5, 0, 7, 2, 6, 1, 3, 4])
     n, P, h_in, h_out = ids.size, 8, 1024, 1536
+    x = _bf16(rng.standard_normal((n, h_in)))
+    A = _bf16(rng.standard_normal((P, h_in, r)) / np.sqrt(h_in))
+    B = _bf16(rng.standard_normal((P, r, h_out)) / np.sqrt(r))
+    y = _bf16(rng.standard_normal((n, h_out)))
+    y0 = y.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    seg = lsg.lora_segment(torch.from_numpy(ids).cuda(), P, err_flag=err)
+    check_segments(seg, ids, P)
+    lsg.sgmv_fused(x, A, B, seg, y, 0.5, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_within_tol(y, oracle_rows(x, A, B, ids, 0.5, y0))
+
+
+def _chunked_requests(lens, adapters, g):
+    """Requests dealt out round robin in chunks of g tokens: each segment is a
+    sequence of runs of contiguous rows."""
+    left = list(lens)
+    ids = []
+    while any(left):
+        for k, a in enumerate(adapters):
+            t = min(g, left[k])
+            ids.extend([a] * t)
+            left[k] -= t
+    return np.asarray(ids, np.int32)
+
+
+@pytest.mark.parametrize("r", [16, 64])
+@pytest.mark.parametrize("g", [96, 128, 160])
+def test_requests_in_runs_every_row(r, g):
+    """Requests in runs of g tokens: tiles inside one run move by whole-tile
+    copies, tiles that straddle two runs gather their rows; every row is
+    compared with the oracle, and the last run ends at the batch's last row."""
+    rng = np.random.default_rng(90 + r + g)
+    lens = [400, 256, 333, 129]
+    ids = _chunked_requests(lens, [3, 0, 2, 1], g)
+    n, P, h_in, h_out = ids.size, 4, 704, 1088
     x = _bf16(rng.standard_normal((n, h_in)))
     A = _bf16(rng.standard_normal((P, h_in, r)) / np.sqrt(h_in))
     B = _bf16(rng.standard_normal((P, r, h_out)) / np.sqrt(r))
