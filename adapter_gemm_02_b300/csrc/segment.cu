@@ -194,11 +194,14 @@ __global__ void __launch_bounds__(1024)
 }
 
 // The same segmentation for a small batch (n <= kSegRankMaxTokens), one thread
-// per token and no histogram over the pool: token i's place in the stable
-// order is the number of tokens that sort before it (a smaller id, or the
-// same id and a smaller index), counted over all ids in shared memory; the
-// first token of each valid id starts a segment, whose index is the number of
-// such first tokens with a smaller id.  Ids outside [0, P) sort as P.
+// per token and no histogram over the pool.  Token i's place in the stable
+// order is the number of tokens that sort before it: a smaller id, or the
+// same id at a smaller index (tokens j < i count when id_j <= id_i, tokens
+// j > i when id_j < id_i), counted over all ids in shared memory.  The sorted
+// ids then mark the segments: sorted position t starts one when its id is
+// valid and differs from position t - 1's, and its segment index is the
+// number of such starts before it (a block-wide prefix count).  Ids outside
+// [0, P) sort as P, after every valid id, in no segment.
 constexpr int kSegRankMaxTokens = kSegRankTokens;
 
 __global__ void __launch_bounds__(kSegRankMaxTokens)
@@ -206,11 +209,12 @@ __global__ void __launch_bounds__(kSegRankMaxTokens)
                              int32_t* __restrict__ perm, int32_t* __restrict__ seg_offsets,
                              int32_t* __restrict__ seg_adapter, int32_t* __restrict__ num_segments,
                              int32_t* err_flag) {
-  __shared__ int32_t keys[kSegRankMaxTokens];
-  __shared__ int32_t lead_keys[kSegRankMaxTokens];
+  __shared__ __align__(16) int32_t keys[kSegRankMaxTokens];
+  __shared__ int32_t skeys[kSegRankMaxTokens];
+  __shared__ int32_t warp_starts[kSegRankMaxTokens / 32];
   pdl_launch_dependents();
   pdl_wait();
-  const int i = threadIdx.x;
+  const int i = threadIdx.x, lane = i & 31, warp = i >> 5, nw = blockDim.x >> 5;
   constexpr int kPad = 0x7fffffff;  // threads past n: after every token
   int key = kPad;
   bool bad = false;
@@ -221,23 +225,47 @@ __global__ void __launch_bounds__(kSegRankMaxTokens)
   }
   keys[i] = key;
   __syncthreads();
-  int before = 0, same_before = 0;
-  for (int j = 0; j < n; ++j) {
-    const int kj = keys[j];
-    before += kj < key;
-    same_before += (kj == key) & (j < i);
+  // place in the stable order (blockDim is a multiple of 32: whole int4 groups)
+  const int4* k4 = reinterpret_cast<const int4*>(keys);
+  const int i4 = i >> 2, n4 = blockDim.x >> 2;
+  int pos = 0;
+  for (int j4 = 0; j4 < i4; ++j4) {
+    const int4 v = k4[j4];
+    pos += (v.x <= key) + (v.y <= key) + (v.z <= key) + (v.w <= key);
   }
-  const bool lead = i < n && key < P && same_before == 0;
-  lead_keys[i] = lead ? key : kPad;
-  const int S = __syncthreads_count(lead);
-  const int n_valid = __syncthreads_count(i < n && key < P);
+  {
+    const int4 v = k4[i4];
+    const int e = i & 3;  // the group holding token i: j < i counts <=, j > i counts <
+    pos += (e > 0 ? v.x <= key : v.x < key) + (e > 1 ? v.y <= key : (e < 1 && v.y < key)) +
+           (e > 2 ? v.z <= key : (e < 2 && v.z < key)) + (e < 3 && v.w < key);
+  }
+  for (int j4 = i4 + 1; j4 < n4; ++j4) {
+    const int4 v = k4[j4];
+    pos += (v.x < key) + (v.y < key) + (v.z < key) + (v.w < key);
+  }
+  if (i < n) {
+    perm[pos] = i;
+    skeys[pos] = key;
+  }
   if (bad) set_err(err_flag, LORA_ERR_BAD_ADAPTER_ID);
-  if (i < n) perm[before + same_before] = i;
-  if (lead) {
-    int seg = 0;
-    for (int j = 0; j < n; ++j) seg += lead_keys[j] < key;
-    seg_adapter[seg] = key;
-    seg_offsets[seg] = before;
+  __syncthreads();
+  // sorted position t = i: a segment starts here when the id is valid and new
+  const int sk = i < n ? skeys[i] : kPad;
+  const bool valid = sk < P;
+  const bool start = valid && (i == 0 || skeys[i - 1] != sk);
+  const unsigned sb = __ballot_sync(0xffffffffu, start);
+  if (lane == 0) warp_starts[warp] = __popc(sb);
+  const int n_valid = __syncthreads_count(valid);
+  int seg = __popc(sb & ((1u << lane) - 1u));
+  int S = 0;
+  for (int w = 0; w < nw; ++w) {
+    const int c = warp_starts[w];
+    seg += w < warp ? c : 0;
+    S += c;
+  }
+  if (start) {
+    seg_adapter[seg] = sk;
+    seg_offsets[seg] = i;
   }
   for (int x = S + i; x <= max_segments; x += blockDim.x) seg_offsets[x] = n_valid;
   for (int x = S + i; x < max_segments; x += blockDim.x) seg_adapter[x] = -1;

@@ -198,7 +198,8 @@ struct TcSmem {
   alignas(16) TcTail t;
   alignas(8) uint64_t sh_full[kSh];
   uint64_t sh_empty[kSh];
-  uint64_t ex_full[kEx];
+  uint64_t ex_full[kEx];  // B tile landed (the expand MMAs wait for it)
+  uint64_t ey_full[kEx];  // y tile landed (the epilogue waits for it)
   uint64_t ex_empty[kEx];
   uint64_t v_full;     // shrink MMAs of the item done (v in TMEM)
   uint64_t v_read;     // the epilogue has read v out of TMEM
@@ -419,6 +420,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
     }
     for (int s = 0; s < kEx; ++s) {
       mbar_init(&sm.ex_full[s], 1);
+      mbar_init(&sm.ey_full[s], 1);
       mbar_init(&sm.ex_empty[s], 4);  // each epilogue warp, once its y stores have read the slot
     }
     mbar_init(&sm.v_full, 1);
@@ -525,27 +527,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
         if (!ok) break;
         uint8_t* st = sm.ex[slot];
         const int c = c0 + b * kBN;
-        if (t.row < 0 && !LSG_TC_GATHER4) {
-          // gathered rows by every lane (arrivals before the producer's own)
-          static_assert(kBH == 1, "one 64-column half per block");
-          gather_rows_cp_async(st, pr.y, pr.ldy, pr.h_out, c, rr, lane, &sm.ex_full[slot]);
+        static_assert(kBH == 1, "one 64-column half per block");
+        // B first, on its own barrier: the MMAs need only B, and the epilogue
+        // waits for the y tile (ey_full) while they run
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&sm.ex_full[slot], static_cast<uint32_t>(Cfg::kExBCopy));
+          tma_load_2d(st + Cfg::kExY, &p.tmB[pj], c, t.a * q.rmax, &sm.ex_full[slot]);
         }
-        __syncwarp();
-        if (LSG_TC_GATHER4 && t.row < 0) {
-          if (lane == 0) mbar_arrive_expect_tx(&sm.ex_full[slot], static_cast<uint32_t>(Cfg::kExY + Cfg::kExBCopy));
+        if (t.row >= 0) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&sm.ey_full[slot], static_cast<uint32_t>(Cfg::kExY));
+            tma_load_2d(st, &p.tmYl[pj], c, t.row, &sm.ey_full[slot]);
+          }
+        } else if (LSG_TC_GATHER4) {
+          // every y byte arrives by tensor gathers (rows of -1 read past the
+          // tensor's last row: zeros), expected before any is issued
+          if (lane == 0) mbar_arrive_expect_tx(&sm.ey_full[slot], static_cast<uint32_t>(Cfg::kExY));
           __syncwarp();
           const int nr = q.n_tokens;
           tma_gather4(st + lane * 512, &p.tmYg[pj], c, rr[0] < 0 ? nr : rr[0], rr[1] < 0 ? nr : rr[1],
-                      rr[2] < 0 ? nr : rr[2], rr[3] < 0 ? nr : rr[3], &sm.ex_full[slot]);
-          if (lane == 0) tma_load_2d(st + Cfg::kExY, &p.tmB[pj], c, t.a * q.rmax, &sm.ex_full[slot]);
-        } else if (lane == 0) {
-          mbar_arrive_expect_tx(&sm.ex_full[slot],
-                                static_cast<uint32_t>((t.row >= 0 ? Cfg::kExY : 0) + Cfg::kExBCopy));
-#pragma unroll
-          for (int h = 0; h < kBH; ++h) {
-            if (t.row >= 0) tma_load_2d(st + h * 16384, &p.tmYl[pj], c + h * 64, t.row, &sm.ex_full[slot]);
-            tma_load_2d(st + Cfg::kExY + h * RP * 128, &p.tmB[pj], c + h * 64, t.a * q.rmax, &sm.ex_full[slot]);
-          }
+                      rr[2] < 0 ? nr : rr[2], rr[3] < 0 ? nr : rr[3], &sm.ey_full[slot]);
+        } else {
+          // gathered rows by every lane (their arrivals), then the producer's own
+          gather_rows_cp_async(st, pr.y, pr.ldy, pr.h_out, c, rr, lane, &sm.ey_full[slot]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.ey_full[slot]);
         }
         __syncwarp();
         filled |= 1u << slot;
@@ -559,7 +565,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
     }
     if (lane == 0 && sm.abort)  // no copy issued here may still be landing when the CTA leaves
       for (int s2 = 0; s2 < kEx; ++s2)
-        if (filled & (1u << s2)) (void)mbar_wait(&sm.ex_full[s2], (fill_par >> s2) & 1u, kTcWaitNs);
+        if (filled & (1u << s2)) {
+          (void)mbar_wait(&sm.ex_full[s2], (fill_par >> s2) & 1u, kTcWaitNs);
+          (void)mbar_wait(&sm.ey_full[s2], (fill_par >> s2) & 1u, kTcWaitNs);
+        }
   } else if (aligned && kHasShrink && warp == 6) {
     // ============================== shrink MMA issuer: v = x . A (this CTA's k-blocks)
     constexpr uint32_t kIdSh = umma_idesc_bf16(128, RP, 0, 1);
@@ -877,7 +886,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
         const bool scatter_lane = !contig && lane < 8 && ((vmask >> (4 * lane)) & 0xFu) == 0xFu;
         for (int b = b0; b < b1 && ok; ++b) {
           const int buf = ae & 1;
-          ok = warp_wait(sm, &sm.acc_full[buf], (ae >> 1) & 1, lane);
+          ok = warp_wait(sm, &sm.acc_full[buf], (ae >> 1) & 1, lane) && warp_wait(sm, &sm.ey_full[xslot], xph, lane);
           if (!ok) break;
           tc_fence_after();
           uint8_t* st = sm.ex[xslot];

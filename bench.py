@@ -130,11 +130,11 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-KERNEL_SOURCES = {"sgmv_cc_kernel": ("sgmv_cc.cu", "ptx.cuh"), "sgmv_tc_kernel": ("sgmv_tc.cu", "ptx.cuh")}
+KERNEL_SOURCES = {"sgmv_cc_kernel": ("sgmv_cc.cu", "seg_warp.cuh", "ptx.cuh"), "sgmv_tc_kernel": ("sgmv_tc.cu", "ptx.cuh")}
 
 
 def source_hash(kernel: str) -> str:
-    """Hash of the device sources of `kernel` (its .cu file and the PTX helpers)."""
+    """Hash of the device sources of `kernel` (its .cu file and the device headers it includes)."""
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "adapter_gemm_02_b300", "csrc", name), "rb") as fh:

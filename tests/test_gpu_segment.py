@@ -27,6 +27,8 @@ def test_segment_every_workload(name):
 
 CASES = [
     (0, 4, 0.0), (1, 1, 0.0), (2, 3, 0.0), (31, 64, 0.0), (32, 64, 0.0), (33, 5, 0.0), (64, 1, 0.0),
+    # up to 256 tokens: the rank sort, whatever the pool
+    (100, 1000, 0.05), (200, 3, 0.2), (255, 1000, 0.0), (256, 1000, 0.1), (256, 70000, 0.0),
     (257, 1000, 0.05), (1000, 7, 0.0), (6224, 32, 0.0), (20000, 300, 0.01), (70000, 100, 0.0),
     (5000, 25000, 0.0),   # largest pool whose histograms stay in shared memory
     (3000, 60000, 0.02),  # histograms in the workspace
@@ -55,6 +57,8 @@ def test_segment_skewed_and_degenerate():
         (np.repeat(np.arange(5, dtype=np.int32), 100)[::-1].copy(), 5),
         (rng.choice(1000, 4096, p=(lambda p: p / p.sum())(np.arange(1, 1001) ** -1.2)).astype(np.int32), 1000),
         (np.full(77, 99, np.int32), 100),                      # only the last adapter
+        (np.full(50, -1, np.int32), 8),                        # every id invalid: no segment
+        (np.arange(256, dtype=np.int32)[::-1].copy(), 256),   # 256 tokens, 256 segments, reversed
     ]:
         _run(ids, P)
 

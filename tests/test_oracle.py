@@ -91,3 +91,16 @@ def test_tiny_workload_end_to_end_cpu():
     assert np.all(np.abs(y - y64) <= 1e-5 + 1e-5 * np.abs(y64))
     seg = oracle.lora_segment_ref(inp.ids.numpy(), 4)
     assert seg["seg_offsets"].tolist() == [0, 1, 4, 9, 16]
+
+
+def test_compact_pool_twins_have_the_same_segments():
+    """The compact-pool twins of the 70B decode batches relabel the ids in
+    order: the oracle's permutation and segment offsets are unchanged."""
+    for r in (8, 16):
+        full, comp = WORKLOADS[f"70b_decode_r{r}"], WORKLOADS[f"70b_decode_r{r}_compact"]
+        a = oracle.lora_segment_ref(full.ids(), full.P)
+        b = oracle.lora_segment_ref(comp.ids(), comp.P)
+        S = a["num_segments"]
+        assert S == b["num_segments"] == comp.P
+        assert np.array_equal(a["perm"], b["perm"])
+        assert np.array_equal(a["seg_offsets"][:S + 1], b["seg_offsets"][:S + 1])

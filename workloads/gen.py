@@ -96,6 +96,12 @@ def zipf_ids(n: int, P: int, alpha: float, seed: int = 0) -> np.ndarray:
     return np.random.default_rng(seed).choice(P, n, p=p).astype(np.int32)
 
 
+def compact_ids(ids: np.ndarray) -> np.ndarray:
+    """Ids relabelled 0..k-1 in increasing order of the original ids (the
+    stable sort by adapter and its segments are unchanged)."""
+    return np.unique(ids, return_inverse=True)[1].astype(np.int32)
+
+
 def prefill_ids(n_requests: int = 8, P: int = 32, lo: int = 128, hi: int = 2048,
                 seed: int = 0, interleave: bool = False) -> np.ndarray:
     """Prefill batch: request i has a prompt of L_i ~ U{lo..hi} tokens and its
@@ -166,6 +172,14 @@ def _build_workloads() -> Dict[str, Workload]:
         nm = f"70b_decode_r{r}"
         w[nm] = _mk(nm, llama_projs("70b"), r, 1000, 256, 1.0, lambda: zipf_ids(256, 1000, 0.8),
                     f"Llama2-70B decode, 7 projections, r={r}, 256 tokens, pool 1000, Zipf(0.8)")
+    # the same launches over a pool of only the adapters the batch uses (the
+    # ids relabelled in order, so segments and bytes moved are unchanged): a
+    # device footprint small enough for a profiler capture
+    n_used = int(np.unique(zipf_ids(256, 1000, 0.8)).size)
+    for r in (8, 16):
+        nm = f"70b_decode_r{r}_compact"
+        w[nm] = _mk(nm, llama_projs("70b"), r, n_used, 256, 1.0, lambda: compact_ids(zipf_ids(256, 1000, 0.8)),
+                    f"the 70b_decode_r{r} batch over a pool of its {n_used} adapters (ids relabelled in order)")
     return w
 
 
