@@ -97,6 +97,20 @@ constexpr int kExStages = LSG_TC_EX_STAGES;
 #ifndef LSG_TC_GATHER4
 #define LSG_TC_GATHER4 1
 #endif
+// 1: the expand's A operand (v as a bf16 hi / lo pair) lives in TMEM, which
+// frees its shared memory for expand ring stages; 0: in shared memory.  The
+// cluster variant keeps it in shared memory (peers write it there).
+#ifndef LSG_TC_VOP_TMEM
+#define LSG_TC_VOP_TMEM 1
+#endif
+// most expand ring stages (the ring takes what shared memory is left, up to this)
+#ifndef LSG_TC_EX_STAGES_MAX
+#define LSG_TC_EX_STAGES_MAX 8
+#endif
+// 1: heavy item slots (see TcSched) go to the groups with one item fewer.
+#ifndef LSG_TC_HEAVY_FIRST
+#define LSG_TC_HEAVY_FIRST 1
+#endif
 // 1: an expand slot goes back as soon as this block's y stores have read it;
 // 0: one block later (after the next block's stores are issued).
 #ifndef LSG_TC_RELEASE_EARLY
@@ -106,6 +120,7 @@ constexpr int kExStages = LSG_TC_EX_STAGES;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemV = 0;      // v accumulator: columns [0, r)
 constexpr uint32_t kTmemAcc = 128;  // expand accumulators: [128, 256), [256, 384)
+constexpr uint32_t kTmemVop = 384;  // (operand in TMEM) v as bf16 hi [384, 384 + r/2), lo [.., 384 + r)
 constexpr int kChunkCols = LSG_TC_CHUNK;  // expand columns per item, about
 constexpr int kMaxItemsPerTile = 64;
 constexpr int kMaxC = 8;  // CTAs per cluster (portable limit)
@@ -133,6 +148,8 @@ struct TcTail {
   TcProj proj[kMaxProj];
   int8_t item_proj[kMaxItemsPerTile];
   int8_t item_chunk[kMaxItemsPerTile];
+  int8_t slot_order[kMaxItemsPerTile];  // a tile's item slots, the n_heavy heavy ones first
+  int32_t n_heavy;                      // heavy item slots per tile (0: plain round robin)
   const int32_t* perm;
   const int32_t* seg_offsets;
   const int32_t* seg_adapter;
@@ -186,14 +203,22 @@ struct TcCfg {
 // buffer and takes one stage from each ring to make room for it.
 template <int R, bool CL>
 struct TcSmem {
+  static constexpr bool kVopT = LSG_TC_VOP_TMEM && !CL;  // operand pair in TMEM
+  static constexpr int kVopBytes = kVopT ? 1024 : 2 * TcCfg<R>::kVop;
   static constexpr int kSh = CL ? LSG_TC_SH_STAGES_CL : kShStages;
-  static constexpr int kEx = CL ? LSG_TC_EX_STAGES_CL : kExStages;
+  // non-cluster: as many expand stages as the rest of 227 KB holds (8 KB for
+  // the tail and barriers), at least LSG_TC_EX_STAGES
+  static constexpr int kExFit =
+      (227 * 1024 - kSh * TcCfg<R>::kShBytes - kVopBytes - 8192) / TcCfg<R>::kExBytes;
+  static constexpr int kEx = CL ? LSG_TC_EX_STAGES_CL
+                                : (LSG_TC_VOP_TMEM ? (kExFit < LSG_TC_EX_STAGES_MAX ? kExFit : LSG_TC_EX_STAGES_MAX)
+                                                   : kExStages);
   // the epilogue hands a slot back one block late, so each ring needs two
   // stages (an expand block of 128 columns leaves the cluster variant one)
   static_assert(kSh >= 2 && kEx >= 2, "ring depth");
   alignas(1024) uint8_t sh[kSh][TcCfg<R>::kShBytes];
   alignas(1024) uint8_t ex[kEx][TcCfg<R>::kExBytes];
-  alignas(1024) uint8_t vop[2][TcCfg<R>::kVop];  // hi, lo
+  alignas(1024) uint8_t vop[kVopT ? 1 : 2][kVopT ? 1024 : TcCfg<R>::kVop];  // hi, lo (in shared memory)
   alignas(16) float rbuf[CL ? 128 * R : 4];      // partial v rows this CTA owns: [source rank][row][r]
   alignas(16) TcTail t;
   alignas(8) uint64_t sh_full[kSh];
@@ -269,6 +294,11 @@ struct TcCursor {
   }
 
   __device__ bool find(const TcTail& q, int lane, int tile, TcTile& out) {
+    if (tile < tiles_before) {  // an earlier tile: walk again from the first segment
+      base = 0;
+      tiles_before = 0;
+      load(q, lane);
+    }
     while (base < S) {
       const int tl = (len + 127) >> 7;
       int inc = tl;
@@ -312,6 +342,55 @@ struct TcCursor {
   }
 };
 
+// The order of the launch's items.  Items are (tile, slot) pairs; group g
+// takes the positions g, g + G, g + 2G, ... of a sequence.  Without heavy
+// slots the sequence is the items in tile-major order (plain round robin).
+// A tile's heavy slots (about twice the median item: a projection with a long
+// shrink, such as the MLP down projection) weigh two positions: heavy item j
+// takes position (2 (j / G)) G + j mod G and the one a round later in the
+// same group, so a group with a heavy item takes one light item fewer.  The
+// light items fill the remaining positions in tile order.
+struct TcSched {
+  int L = 0x7fffffff, H = 0, G = 1, hr = 0, hrem = 0, nh = 0, nl = 0;
+  __device__ TcSched(const TcTail& q, TcCursor& cur, int lane, int groups) {
+    G = groups;
+    nh = q.n_heavy;
+    if (nh == 0) return;
+    TcTile t;
+    (void)cur.find(q, lane, 0x7fffffff, t);  // walks every segment: the tile count
+    const int nt = cur.tiles_before;
+    nl = q.ipt - nh;
+    H = nt * nh;
+    L = nt * nl;
+    hr = H / G;
+    hrem = H - hr * G;
+  }
+  // 0: position pos is item (tile, is); 1: pos is the second half of a heavy
+  // item (nothing to do); 2: no item at pos or later in this group.
+  __device__ int map(const TcTail& q, int pos, int& tile, int& is) const {
+    if (nh == 0) {
+      tile = pos / q.ipt;
+      is = pos - tile * q.ipt;
+      return 0;
+    }
+    const int k = pos / G, g = pos - k * G;
+    const int occ = k < 2 * hr ? G : (k < 2 * hr + 2 ? hrem : 0);  // heavy groups of round k
+    if (g < occ) {
+      if (k & 1) return 1;
+      const int j = (k >> 1) * G + g;
+      tile = j / nh;
+      is = q.slot_order[j - tile * nh];
+      return 0;
+    }
+    const int before = G * min(k, 2 * hr) + hrem * min(max(k - 2 * hr, 0), 2) + min(g, occ);
+    const int j = pos - before;  // light item index
+    if (j >= L) return 2;
+    tile = j / nl;
+    is = q.slot_order[nh + j - tile * nl];
+    return 0;
+  }
+};
+
 // x / y rows of tile rows 4*lane .. 4*lane+3 of a gathered tile; -1 for rows
 // past the tile or with a permutation entry outside [0, n) (zero-filled,
 // never stored).
@@ -344,6 +423,35 @@ __device__ __forceinline__ void gather_rows_cp_async(uint8_t* tile, const uint16
     }
   }
   cp_async_mbar_arrive(bar);
+}
+
+// This warp's 32 TMEM lanes x N 32-bit columns from registers (column c of
+// lane l: r[c] of lane l).
+template <int N>
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t (&r)[N]);
+template <>
+__device__ __forceinline__ void tmem_st<8>(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]) : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_st<16>(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]) : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_st<32>(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]) : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// D[tmem] (+)= A[tmem] . B[smem], issued by one thread: A is M rows (TMEM
+// lanes) x K bf16, two consecutive K elements per 32-bit column (the lower
+// K index in the lower half).
+__device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u));
 }
 
 // Bounded wait by lane 0, result broadcast to the warp; a time-out sets the
@@ -406,8 +514,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
   if constexpr (R < RP) {
     // rank 8: the v operand's columns 8..15 and the B tiles' rows 8..15 stay
     // zero (no copy or store writes them)
-    for (int i = tid; i < 2 * Cfg::kVop / 16; i += kTcThreads)
-      reinterpret_cast<uint4*>(&sm.vop[0][0])[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (!TcSmem<R, CL>::kVopT)
+      for (int i = tid; i < 2 * Cfg::kVop / 16; i += kTcThreads)
+        reinterpret_cast<uint4*>(&sm.vop[0][0])[i] = make_uint4(0u, 0u, 0u, 0u);
     for (int s = 0; s < kEx; ++s)
       for (int i = tid; i < (Cfg::kExB - Cfg::kExBCopy) / 16; i += kTcThreads)
         reinterpret_cast<uint4*>(sm.ex[s] + Cfg::kExY + Cfg::kExBCopy)[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -455,8 +564,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
     uint32_t ph = 0, filled = 0, fill_par = 0;
     TcCursor cur;
     cur.init(q, lane);
-    for (int item = group;; item += ngroups) {
-      const int tile = item / q.ipt, is = item - tile * q.ipt;
+    const TcSched sc(q, cur, lane, ngroups);
+    for (int pos = group;; pos += ngroups) {
+      int tile, is;
+      const int step = sc.map(q, pos, tile, is);
+      if (step == 2) break;
+      if (step == 1) continue;
       TcTile t;
       if (!cur.find(q, lane, tile, t)) break;
       if (t.a < 0 || t.a >= q.n_slabs) continue;
@@ -509,8 +622,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
     uint32_t ph = 0, filled = 0, fill_par = 0;
     TcCursor cur;
     cur.init(q, lane);
-    for (int item = group;; item += ngroups) {
-      const int tile = item / q.ipt, is = item - tile * q.ipt;
+    const TcSched sc(q, cur, lane, ngroups);
+    for (int pos = group;; pos += ngroups) {
+      int tile, is;
+      const int step = sc.map(q, pos, tile, is);
+      if (step == 2) break;
+      if (step == 1) continue;
       TcTile t;
       if (!cur.find(q, lane, tile, t)) break;
       if (t.a < 0 || t.a >= q.n_slabs) continue;
@@ -576,8 +693,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
     uint32_t sph = 0;
     TcCursor cur;
     cur.init(q, lane);
-    for (int item = group;; item += ngroups) {
-      const int tile = item / q.ipt, is = item - tile * q.ipt;
+    const TcSched sc(q, cur, lane, ngroups);
+    for (int pos = group;; pos += ngroups) {
+      int tile, is;
+      const int step = sc.map(q, pos, tile, is);
+      if (step == 2) break;
+      if (step == 1) continue;
       TcTile t;
       if (!cur.find(q, lane, tile, t)) break;
       if (t.a < 0 || t.a >= q.n_slabs) continue;
@@ -632,8 +753,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
     uint32_t xph = 0;
     TcCursor cur;
     cur.init(q, lane);
-    for (int item = group;; item += ngroups) {
-      const int tile = item / q.ipt, is = item - tile * q.ipt;
+    const TcSched sc(q, cur, lane, ngroups);
+    for (int pos = group;; pos += ngroups) {
+      int tile, is;
+      const int step = sc.map(q, pos, tile, is);
+      if (step == 2) break;
+      if (step == 1) continue;
       TcTile t;
       if (!cur.find(q, lane, tile, t)) break;
       if (t.a < 0 || t.a >= q.n_slabs) continue;
@@ -663,8 +788,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
             const uint64_t bd = umma_desc(bs + k * 16 * 128, RP * 128, 1024, 2);
 #pragma unroll
             for (int hl = 0; hl < 2; ++hl) {
-              const uint64_t ad = umma_desc(smem_u32(sm.vop[hl]) + k * 32, 16, 8 * RP * 2, umma_layout(RP * 2));
-              umma_bf16(tmem + kTmemAcc + buf * kBN, ad, bd, kIdEx, k > 0 || hl > 0);
+              if constexpr (TcSmem<R, CL>::kVopT) {
+                // the pair in TMEM: 8 columns (16 bf16) per k-step
+                umma_bf16_ta(tmem + kTmemAcc + buf * kBN, tmem + kTmemVop + hl * (RP / 2) + k * 8, bd, kIdEx,
+                             k > 0 || hl > 0);
+              } else {
+                const uint64_t ad = umma_desc(smem_u32(sm.vop[hl]) + k * 32, 16, 8 * RP * 2, umma_layout(RP * 2));
+                umma_bf16(tmem + kTmemAcc + buf * kBN, ad, bd, kIdEx, k > 0 || hl > 0);
+              }
             }
           }
           if (!(withhold(3) && ae == 0)) umma_commit(&sm.acc_full[buf]);
@@ -728,8 +859,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
                      : "memory");
       }
     };
-    for (int item = group;; item += ngroups) {
-      const int tile = item / q.ipt, is = item - tile * q.ipt;
+    const TcSched sc(q, cur, lane, ngroups);
+    for (int pos = group;; pos += ngroups) {
+      int tile, is;
+      const int step = sc.map(q, pos, tile, is);
+      if (step == 2) break;
+      if (step == 1) continue;
       TcTile t;
       if (!cur.find(q, lane, tile, t)) break;
       if (t.a < 0 || t.a >= q.n_slabs) {
@@ -806,6 +941,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
           }
           ++it;
           continue;
+        } else if constexpr (!CL && TcSmem<R, CL>::kVopT) {
+          // ---- v -> bf16 hi / lo pairs in this lane's TMEM row (the expand's A
+          // operand); ranks past r are zero (the shrink's N = 16 columns past
+          // rank 8 hold products that are never used)
+          uint32_t hw[RP / 2], lw[RP / 2];
+#pragma unroll
+          for (int j = 0; j < RP / 2; ++j) {
+            const float f0 = 2 * j < R ? __uint_as_float(v[2 * j]) : 0.f;
+            const float f1 = 2 * j + 1 < R ? __uint_as_float(v[2 * j + 1]) : 0.f;
+            const __nv_bfloat162 h = __floats2bfloat162_rn(f0, f1);
+            const float2 hf = __bfloat1622float2(h);
+            const __nv_bfloat162 l = __floats2bfloat162_rn(f0 - hf.x, f1 - hf.y);
+            hw[j] = *reinterpret_cast<const uint32_t*>(&h);
+            lw[j] = *reinterpret_cast<const uint32_t*>(&l);
+          }
+          tmem_st<RP / 2>(tq + kTmemVop, hw);
+          tmem_st<RP / 2>(tq + kTmemVop + RP / 2, lw);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.vop_ready);
         } else if constexpr (!CL) {
           // ---- v -> bf16 operands hi, lo (K-major, 2*RP-byte swizzle)
           put_operand_row(v);
@@ -995,6 +1151,7 @@ lora_status tc_groups(int C, int& groups) {
   }
   if (groups > 0) return LORA_OK;
   auto kern = sgmv_tc_kernel<R, CL, MODE>;
+  static_assert(sizeof(TcSmem<R, CL>) <= 227 * 1024, "shared memory per CTA");
   const size_t smem = sizeof(TcSmem<R, CL>);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
@@ -1026,6 +1183,7 @@ lora_status launch_tc_rc(TcParams& prm, const SgmvCall& call, int tiles_bound, c
   constexpr bool kHasShrink = (MODE & kModeShrink) != 0;
   constexpr bool kHasExpand = (MODE & kModeExpand) != 0;
   auto kern = sgmv_tc_kernel<R, CL, MODE>;
+  static_assert(sizeof(TcSmem<R, CL>) <= 227 * 1024, "shared memory per CTA");
   const size_t smem = sizeof(TcSmem<R, CL>);
   const int C = prm.t.csplit;
   const uint64_t n = static_cast<uint64_t>(call.seg.n_tokens);
@@ -1172,6 +1330,31 @@ lora_status plan_and_launch(const SgmvCall& call, cudaStream_t stream) {
       prm.t.item_chunk[ipt] = static_cast<int8_t>(c);
       ++ipt;
     }
+  }
+  // Heavy item slots: an item's time is about max(its shrink k-blocks x 0.7,
+  // its expand blocks x 0.95) (us per block measured on B300: the shrink and
+  // the expand of consecutive items overlap); a slot of at least 1.5x the
+  // median item takes the positions of the groups with one item fewer.
+  {
+    double cost[kMaxItemsPerTile], sorted[kMaxItemsPerTile];
+    for (int k = 0; k < ipt; ++k) {
+      const ProjArgs& a = call.proj[prm.t.item_proj[k]];
+      const TcProj& t = prm.t.proj[prm.t.item_proj[k]];
+      const int kb = kHasShrink ? ceil_div(a.h_in, 64) : 0;
+      const int cols = kHasExpand ? std::min(t.chunk, a.h_out - prm.t.item_chunk[k] * t.chunk) : 0;
+      cost[k] = sorted[k] = std::max(0.7 * kb, 0.95 * ceil_div(cols, kBN));
+    }
+    std::sort(sorted, sorted + ipt);
+    const double median = sorted[(ipt - 1) / 2];
+    int nh = 0;
+    for (int k = 0; k < ipt; ++k)
+      if (cost[k] >= 1.5 * median) prm.t.slot_order[nh++] = static_cast<int8_t>(k);
+    int nl = nh;
+    for (int k = 0; k < ipt; ++k)
+      if (!(cost[k] >= 1.5 * median)) prm.t.slot_order[nl++] = static_cast<int8_t>(k);
+    prm.t.n_heavy = LSG_TC_HEAVY_FIRST ? nh : 0;
+    if (!LSG_TC_HEAVY_FIRST)
+      for (int k = 0; k < ipt; ++k) prm.t.slot_order[k] = static_cast<int8_t>(k);
   }
   prm.t.csplit = best.C;
   prm.t.slot_of = call.slot_of;
