@@ -41,9 +41,10 @@
 // x / y (a prefill request, or a run of one inside a segment of several
 // requests) moves with 2-D tensor copies; any other tile (tokens of one
 // adapter spread over the batch) gathers its rows through the permutation:
-// each producer lane loads four rows per stage by a tile::gather4 tensor copy
-// into the swizzled tile, and the updated y rows go back by tile::scatter4
-// tensor stores (rows of an incomplete group of four by 16-byte stores).
+// the producer lanes copy x rows with 16-byte cp.async copies and load y rows
+// four at a time by tile::gather4 tensor copies into the swizzled tile, and
+// the updated y rows go back by tile::scatter4 tensor stores (rows of an
+// incomplete group of four by 16-byte stores).
 // Gathered tiles run at about half the rate of contiguous ones: every 128-byte
 // row piece is its own request, against one 16 KB box.
 //
@@ -91,11 +92,24 @@ constexpr int kExStages = LSG_TC_EX_STAGES;
 #ifndef LSG_TC_EX_STAGES_CL
 #define LSG_TC_EX_STAGES_CL 3
 #endif
-// Gathered tiles' x and y rows: 1 = four-row tensor gathers (one per lane and
-// stage), 0 = 16-byte cp.async copies by the producer's lanes (the full 13B
-// prefill layer with interleaved requests: 795 against 849 us).
-#ifndef LSG_TC_GATHER4
-#define LSG_TC_GATHER4 1
+// Gathered tiles' rows, for the shrink's x and the expand's y apart: 1 =
+// four-row tensor gathers (one per lane and stage), 0 = 16-byte cp.async
+// copies by the producer's lanes.  The full 13B prefill layer with
+// interleaved requests: x by cp.async and y by gathers 755 us, both by
+// gathers 805 us, x by gathers and y by cp.async 800 us, both by cp.async
+// 849 us (the tensor-copy unit issues every 128-byte row piece of a gather
+// as its own request; the copies split the pieces between it and the
+// load/store units).
+#ifndef LSG_TC_GATHER4_X
+#define LSG_TC_GATHER4_X 0
+#endif
+#ifndef LSG_TC_GATHER4_Y
+#define LSG_TC_GATHER4_Y 1
+#endif
+// Gathered tiles' updated y rows: 1 = four-row tensor scatters, 0 = 16-byte
+// stores by the epilogue threads.
+#ifndef LSG_TC_SCATTER4
+#define LSG_TC_SCATTER4 1
 #endif
 // 1: the expand's A operand (v as a bf16 hi / lo pair) lives in TMEM, which
 // frees its shared memory for expand ring stages; 0: in shared memory.  The
@@ -110,6 +124,10 @@ constexpr int kExStages = LSG_TC_EX_STAGES;
 // 1: heavy item slots (see TcSched) go to the groups with one item fewer.
 #ifndef LSG_TC_HEAVY_FIRST
 #define LSG_TC_HEAVY_FIRST 1
+#endif
+// 1: heavy items start at round 1 (after each group's first light item).
+#ifndef LSG_TC_HEAVY_LATE
+#define LSG_TC_HEAVY_LATE 1
 #endif
 // 1: an expand slot goes back as soon as this block's y stores have read it;
 // 0: one block later (after the next block's stores are issued).
@@ -347,11 +365,14 @@ struct TcCursor {
 // slots the sequence is the items in tile-major order (plain round robin).
 // A tile's heavy slots (about twice the median item: a projection with a long
 // shrink, such as the MLP down projection) weigh two positions: heavy item j
-// takes position (2 (j / G)) G + j mod G and the one a round later in the
-// same group, so a group with a heavy item takes one light item fewer.  The
-// light items fill the remaining positions in tile order.
+// takes position (h0 + 2 (j / G)) G + j mod G and the one a round later in
+// the same group, so a group with a heavy item takes one light item fewer.
+// The light items fill the remaining positions in tile order.  The heavy
+// rounds start at round h0 = 1 when every group has a light item for round
+// 0: a heavy item's long shrink then overlaps the expand of the group's first
+// item instead of delaying the group's first expand.
 struct TcSched {
-  int L = 0x7fffffff, H = 0, G = 1, hr = 0, hrem = 0, nh = 0, nl = 0;
+  int L = 0x7fffffff, H = 0, G = 1, hr = 0, hrem = 0, h0 = 0, nh = 0, nl = 0;
   __device__ TcSched(const TcTail& q, TcCursor& cur, int lane, int groups) {
     G = groups;
     nh = q.n_heavy;
@@ -364,6 +385,7 @@ struct TcSched {
     L = nt * nl;
     hr = H / G;
     hrem = H - hr * G;
+    h0 = LSG_TC_HEAVY_LATE && L >= G ? 1 : 0;
   }
   // 0: position pos is item (tile, is); 1: pos is the second half of a heavy
   // item (nothing to do); 2: no item at pos or later in this group.
@@ -373,16 +395,16 @@ struct TcSched {
       is = pos - tile * q.ipt;
       return 0;
     }
-    const int k = pos / G, g = pos - k * G;
-    const int occ = k < 2 * hr ? G : (k < 2 * hr + 2 ? hrem : 0);  // heavy groups of round k
+    const int k = pos / G, g = pos - k * G, kh = k - h0;  // kh: round among the heavy rounds
+    const int occ = kh < 0 ? 0 : (kh < 2 * hr ? G : (kh < 2 * hr + 2 ? hrem : 0));  // heavy groups of round k
     if (g < occ) {
-      if (k & 1) return 1;
-      const int j = (k >> 1) * G + g;
+      if (kh & 1) return 1;
+      const int j = (kh >> 1) * G + g;
       tile = j / nh;
       is = q.slot_order[j - tile * nh];
       return 0;
     }
-    const int before = G * min(k, 2 * hr) + hrem * min(max(k - 2 * hr, 0), 2) + min(g, occ);
+    const int before = G * min(max(kh, 0), 2 * hr) + hrem * min(max(kh - 2 * hr, 0), 2) + min(g, occ);
     const int j = pos - before;  // light item index
     if (j >= L) return 2;
     tile = j / nl;
@@ -502,7 +524,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
   }
   if (warp == 4 && lane < kMaxProj) {
     prefetch_tmap(&p.tmX[lane]);
-    if (LSG_TC_GATHER4) prefetch_tmap(&p.tmXg[lane]);
+    if (LSG_TC_GATHER4_X) prefetch_tmap(&p.tmXg[lane]);
     prefetch_tmap(&p.tmA[lane]);
   }
   if (warp == 5 && lane < kMaxProj) {
@@ -585,10 +607,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
         uint8_t* st = sm.sh[slot];
         // gathered rows: every lane copies its four rows and arrives (before
         // the producer's own arrival, so the phase waits for them)
-        if (t.row < 0 && !LSG_TC_GATHER4)
+        if (t.row < 0 && !LSG_TC_GATHER4_X)
           gather_rows_cp_async(st, q.proj[pj].x, q.proj[pj].ldx, q.proj[pj].h_in, kb * 64, rr, lane, &sm.sh_full[slot]);
         __syncwarp();
-        if (LSG_TC_GATHER4 && t.row < 0) {
+        if (LSG_TC_GATHER4_X && t.row < 0) {
           // every byte of the stage arrives by tensor copies (rows past the
           // tile read as zeros): expected before any is issued
           if (lane == 0) mbar_arrive_expect_tx(&sm.sh_full[slot], 16384u + Cfg::kShA);
@@ -656,7 +678,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
             mbar_arrive_expect_tx(&sm.ey_full[slot], static_cast<uint32_t>(Cfg::kExY));
             tma_load_2d(st, &p.tmYl[pj], c, t.row, &sm.ey_full[slot]);
           }
-        } else if (LSG_TC_GATHER4) {
+        } else if (LSG_TC_GATHER4_Y) {
           // every y byte arrives by tensor gathers (rows of -1 read past the
           // tensor's last row: zeros), expected before any is issued
           if (lane == 0) mbar_arrive_expect_tx(&sm.ey_full[slot], static_cast<uint32_t>(Cfg::kExY));
@@ -1035,11 +1057,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
         // gathered tile: rows in a group of four valid rows go out by one
         // four-row scatter (lane j of the quarter's warp: rows 4j .. 4j+3)
         const unsigned vmask = __ballot_sync(0xffffffffu, yrow >= 0);
-        const bool by_tensor_store = contig ? m < full_rows : ((vmask >> (lane & ~3)) & 0xFu) == 0xFu;
+        const bool by_tensor_store =
+            contig ? m < full_rows : (LSG_TC_SCATTER4 && ((vmask >> (lane & ~3)) & 0xFu) == 0xFu);
         int yr4[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) yr4[k] = __shfl_sync(0xffffffffu, yrow, (4 * lane + k) & 31);
-        const bool scatter_lane = !contig && lane < 8 && ((vmask >> (4 * lane)) & 0xFu) == 0xFu;
+        const bool scatter_lane = LSG_TC_SCATTER4 && !contig && lane < 8 && ((vmask >> (4 * lane)) & 0xFu) == 0xFu;
         for (int b = b0; b < b1 && ok; ++b) {
           const int buf = ae & 1;
           ok = warp_wait(sm, &sm.acc_full[buf], (ae >> 1) & 1, lane) && warp_wait(sm, &sm.ey_full[xslot], xph, lane);
@@ -1195,7 +1218,7 @@ lora_status launch_tc_rc(TcParams& prm, const SgmvCall& call, int tiles_bound, c
       const uint64_t str[1] = {static_cast<uint64_t>(a.ldx) * 2};
       const uint32_t box[2] = {64, 128};
       if ((s = encode_tmap_bf16(&prm.tmX[i], a.x, 2, dims, str, box, 128)) != LORA_OK) return s;
-      if (LSG_TC_GATHER4) {
+      if (LSG_TC_GATHER4_X) {
         const uint32_t box_g[2] = {64, 1};
         if ((s = encode_tmap_bf16(&prm.tmXg[i], a.x, 2, dims, str, box_g, 128)) != LORA_OK) return s;
       }
