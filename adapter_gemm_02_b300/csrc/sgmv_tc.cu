@@ -68,8 +68,12 @@ namespace lsg {
 
 constexpr int kTcThreads = 384;
 constexpr int kTcEpiThreads = 128;  // one epilogue group: 4 warps, one per TMEM lane quarter
+// Shrink ring depth: the shrink streams from L2 (and DRAM) with a latency of
+// microseconds, so its ring sets its rate.  Rank 64, 13B layer: 4 / 5 / 6 / 7
+// shrink stages (the expand ring takes the rest: 5 / 4 / 3 / 2) 415 / 393 /
+// 391 / 508 us.
 #ifndef LSG_TC_SH_STAGES
-#define LSG_TC_SH_STAGES 4
+#define LSG_TC_SH_STAGES 6
 #endif
 #ifndef LSG_TC_CHUNK
 #define LSG_TC_CHUNK 5120
@@ -124,6 +128,18 @@ constexpr int kExStages = LSG_TC_EX_STAGES;
 // 1: heavy item slots (see TcSched) go to the groups with one item fewer.
 #ifndef LSG_TC_HEAVY_FIRST
 #define LSG_TC_HEAVY_FIRST 1
+#endif
+// Item cost model: us per shrink k-block and per expand block.  Fitted to
+// the 4-stage shrink ring (50-57 us of shrink over 80 k-blocks, 137-141 us
+// over 216, 67-78 us of expand over 72-80 blocks) and kept, by measurement:
+// with the 6-stage ring the items measure 38-40 / 103 / 77-98 us, but a fit
+// to those (0.48, 1.05) no longer marks the 13B down projection heavy and the
+// layer takes 415 instead of 390 us (the 2-request batch 244 instead of 216).
+#ifndef LSG_TC_COST_KB
+#define LSG_TC_COST_KB 0.7
+#endif
+#ifndef LSG_TC_COST_BLK
+#define LSG_TC_COST_BLK 0.95
 #endif
 // 1: heavy items start at round 1 (after each group's first light item).
 #ifndef LSG_TC_HEAVY_LATE
@@ -1354,10 +1370,10 @@ lora_status plan_and_launch(const SgmvCall& call, cudaStream_t stream) {
       ++ipt;
     }
   }
-  // Heavy item slots: an item's time is about max(its shrink k-blocks x 0.7,
-  // its expand blocks x 0.95) (us per block measured on B300: the shrink and
-  // the expand of consecutive items overlap); a slot of at least 1.5x the
-  // median item takes the positions of the groups with one item fewer.
+  // Heavy item slots: an item's time is about max(its shrink k-blocks x
+  // LSG_TC_COST_KB, its expand blocks x LSG_TC_COST_BLK) (us per block
+  // measured on B300; the shrink and the expand of consecutive items
+  // overlap); a slot of at least 1.5x the median item weighs two positions.
   {
     double cost[kMaxItemsPerTile], sorted[kMaxItemsPerTile];
     for (int k = 0; k < ipt; ++k) {
@@ -1365,7 +1381,7 @@ lora_status plan_and_launch(const SgmvCall& call, cudaStream_t stream) {
       const TcProj& t = prm.t.proj[prm.t.item_proj[k]];
       const int kb = kHasShrink ? ceil_div(a.h_in, 64) : 0;
       const int cols = kHasExpand ? std::min(t.chunk, a.h_out - prm.t.item_chunk[k] * t.chunk) : 0;
-      cost[k] = sorted[k] = std::max(0.7 * kb, 0.95 * ceil_div(cols, kBN));
+      cost[k] = sorted[k] = std::max(LSG_TC_COST_KB * kb, LSG_TC_COST_BLK * ceil_div(cols, kBN));
     }
     std::sort(sorted, sorted + ipt);
     const double median = sorted[(ipt - 1) / 2];
