@@ -13,13 +13,16 @@
 // One CTA per SM, persistent, twelve warps with fixed roles:
 //   warps 0-3, 8-11  epilogue, two groups of four (warp w: TMEM lane quarter
 //              w % 4).  Group 0 turns v (fp32, TMEM) into the expand's bf16
-//              operand pair v = hi + lo in shared memory; both groups then add
-//              s * acc to their 32 columns of each 64-column y block in shared
-//              memory, and group 0 stores the block (one TMA box per quarter)
+//              operand pair v = hi + lo, written back into TMEM (in shared
+//              memory for the cluster variant, whose peers write it there);
+//              both groups then add s * acc to their 32 columns of each
+//              64-column y block in shared memory, and group 0 stores the
+//              block (one TMA box per quarter)
 //   warp 4     shrink producer: TMA x tiles [128][64] (K-major, 128 B swizzle)
-//              and A tiles [64][r] (MN-major, 2r-byte swizzle), 4 stages
-//   warp 5     expand producer: TMA y tiles [128][64] (128 B swizzle) and B
-//              tiles [r][64] (MN-major), 4 stages
+//              and A tiles [64][r] (MN-major, 2r-byte swizzle), 6 stages
+//   warp 5     expand producer: TMA B tiles [r][64] (MN-major) and y tiles
+//              [128][64] (128 B swizzle) on separate barriers, in the stages
+//              the rest of shared memory holds (3 at r = 64)
 //   warp 6     TMEM allocation; one thread issues the shrink MMAs
 //   warp 7     one thread issues the expand MMAs
 //              (tcgen05.mma kind::f16, fp32 accumulators in TMEM: v in columns
@@ -32,9 +35,9 @@
 //              of item i completed.
 //
 // Work item = (128-token tile of a segment, projection, column chunk of
-// h_out), round robin over the CTAs (or over clusters of C CTAs that share an
-// item: split-K shrink, split-N expand, partial v summed through distributed
-// shared memory).  Each item recomputes its tile's shrink (x is re-read from
+// h_out), dealt to the CTAs (or to clusters of C CTAs that share an item:
+// split-K shrink, split-N expand, partial v summed through distributed
+// shared memory) in a weighted round robin (TcSched).  Each item recomputes its tile's shrink (x is re-read from
 // L2 by the items of the same tile), which keeps items of similar size for
 // load balance.  Every segment of at least kLongSeg tokens is taken here (the
 // decode kernel skips exactly these).  A tile whose rows are contiguous in

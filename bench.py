@@ -25,6 +25,7 @@ import glob
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -133,13 +134,21 @@ def hbm_peak():
 KERNEL_SOURCES = {"sgmv_cc_kernel": ("sgmv_cc.cu", "seg_warp.cuh", "ptx.cuh"), "sgmv_tc_kernel": ("sgmv_tc.cu", "ptx.cuh")}
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and with whitespace collapsed (a comment
+    edit leaves the kernel, and so its recorded counters, unchanged)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def source_hash(kernel: str) -> str:
-    """Hash of the device sources of `kernel` (its .cu file and the device headers it includes)."""
+    """Hash of the device code of `kernel` (its .cu file and the device headers it includes)."""
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "adapter_gemm_02_b300", "csrc", name), "rb") as fh:
+        with open(os.path.join(ROOT, "adapter_gemm_02_b300", "csrc", name), encoding="utf-8") as fh:
             h.update(name.encode())
-            h.update(fh.read())
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
