@@ -93,6 +93,9 @@ LORA_API int lora_abi_version(void);
  *                              last segment.
  *   num_segments               device scalar: number of non-empty segments.
  *   max_segments               min(n_tokens, n_adapters) (capacity of the arrays).
+ * A record built by the caller must keep perm ascending within each segment,
+ * as lora_segment's does: the tensor-tile kernel takes a 128-token tile
+ * whose first and last rows are 127 apart as contiguous rows.
  */
 typedef struct {
   const int32_t* perm;
@@ -331,8 +334,8 @@ typedef struct {
  * for all projections; several ranks: each launch takes the projections
  * whose (projection, rank) pairs fit 8, i.e. 8 / popcount(rank_mask)
  * projections.  Prefill-like batches also run the tensor-tile kernel once
- * per rank of the mask among 16, 32 and 64, for the long contiguous segments
- * of that rank.
+ * per rank of the mask, for the segments of at least 64 tokens of that rank
+ * (rows contiguous or gathered through perm).
  * Host errors as sgmv_multi, plus: table NULL, a table pointer NULL or not
  * 4-byte aligned, n_slots < 1, r_max or rank_mask invalid
  * (LORA_ERR_INVALID_ARG / LORA_ERR_UNSUPPORTED), n_slots*r_max*max(h_in,
