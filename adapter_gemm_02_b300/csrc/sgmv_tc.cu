@@ -144,7 +144,8 @@ constexpr int kExStages = LSG_TC_EX_STAGES;
 #ifndef LSG_TC_COST_BLK
 #define LSG_TC_COST_BLK 0.95
 #endif
-// 1: heavy items start at round 1 (after each group's first light item).
+// 1: heavy items start at pass 1 of the round robin (after each group's
+// first light item).
 #ifndef LSG_TC_HEAVY_LATE
 #define LSG_TC_HEAVY_LATE 1
 #endif
@@ -384,11 +385,11 @@ struct TcCursor {
 // slots the sequence is the items in tile-major order (plain round robin).
 // A tile's heavy slots (about twice the median item: a projection with a long
 // shrink, such as the MLP down projection) weigh two positions: heavy item j
-// takes position (h0 + 2 (j / G)) G + j mod G and the one a round later in
+// takes position (h0 + 2 (j / G)) G + j mod G and the one a pass later in
 // the same group, so a group with a heavy item takes one light item fewer.
 // The light items fill the remaining positions in tile order.  The heavy
-// rounds start at round h0 = 1 when every group has a light item for round
-// 0: a heavy item's long shrink then overlaps the expand of the group's first
+// passes start at pass h0 = 1 when every group has a light item for pass 0:
+// a heavy item's long shrink then overlaps the expand of the group's first
 // item instead of delaying the group's first expand.
 struct TcSched {
   int L = 0x7fffffff, H = 0, G = 1, hr = 0, hrem = 0, h0 = 0, nh = 0, nl = 0;
@@ -414,8 +415,8 @@ struct TcSched {
       is = pos - tile * q.ipt;
       return 0;
     }
-    const int k = pos / G, g = pos - k * G, kh = k - h0;  // kh: round among the heavy rounds
-    const int occ = kh < 0 ? 0 : (kh < 2 * hr ? G : (kh < 2 * hr + 2 ? hrem : 0));  // heavy groups of round k
+    const int k = pos / G, g = pos - k * G, kh = k - h0;  // k: pass of the round robin; kh: among the heavy passes
+    const int occ = kh < 0 ? 0 : (kh < 2 * hr ? G : (kh < 2 * hr + 2 ? hrem : 0));  // heavy groups of pass k
     if (g < occ) {
       if (kh & 1) return 1;
       const int j = (kh >> 1) * G + g;
@@ -1290,10 +1291,10 @@ lora_status launch_tc_rc(TcParams& prm, const SgmvCall& call, int tiles_bound, c
 
 // Work plan: items are (tile, projection, column chunk) taken by groups of C
 // CTAs.  For each C in {1, 2, 4, 8} the columns are cut into enough chunks
-// for one round of items over the co-resident groups (at least one chunk of
+// for one pass of items over the co-resident groups (at least one chunk of
 // about kChunkCols columns per projection; each extra chunk re-reads the
 // tile's x and the A slab for its own shrink); the plan with the fewest bytes
-// per CTA over all rounds wins (ties: the smaller C).  The shrink and expand
+// per CTA over all passes wins (ties: the smaller C).  The shrink and expand
 // modes run one CTA per item; the shrink mode has one item per tile.
 template <int R, int MODE>
 lora_status plan_and_launch(const SgmvCall& call, cudaStream_t stream) {
