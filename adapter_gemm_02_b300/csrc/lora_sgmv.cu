@@ -286,15 +286,17 @@ lora_status sgmv_multi_host(const lora_proj* projs, int32_t n_proj, int32_t n_ad
   int32_t* ids = reinterpret_cast<int32_t*>(at(h.ids));
   const size_t n = static_cast<size_t>(n_tokens);
   if (cudaMemcpyAsync(ids, ids_host, n * 4, cudaMemcpyDefault, st) != cudaSuccess) return LORA_ERR_CUDA;
+  // rows of width w with leading dimension ld: one flat copy when they are
+  // contiguous (ld == w), else a 2-D copy
+  auto copy_rows = [&](void* dst, size_t dld, const void* src, size_t sld, size_t w) {
+    if (dld == w && sld == w) return cudaMemcpyAsync(dst, src, w * n, cudaMemcpyDefault, st);
+    return cudaMemcpy2DAsync(dst, dld, src, sld, w, n, cudaMemcpyDefault, st);
+  };
   for (int i = 0; i < n_proj; ++i) {
     const lora_proj& q = projs[i];
-    if (h.x_of[i] == i &&
-        cudaMemcpy2DAsync(at(h.x[i]), q.h_in * 2, q.x, q.ldx * 2, q.h_in * 2, n, cudaMemcpyDefault, st) !=
-            cudaSuccess)
+    if (h.x_of[i] == i && copy_rows(at(h.x[i]), q.h_in * 2, q.x, q.ldx * 2, q.h_in * 2) != cudaSuccess)
       return LORA_ERR_CUDA;
-    if (cudaMemcpy2DAsync(at(h.y[i]), q.h_out * 2, q.y, q.ldy * 2, q.h_out * 2, n, cudaMemcpyDefault, st) !=
-        cudaSuccess)
-      return LORA_ERR_CUDA;
+    if (copy_rows(at(h.y[i]), q.h_out * 2, q.y, q.ldy * 2, q.h_out * 2) != cudaSuccess) return LORA_ERR_CUDA;
   }
   lora_segments seg{};
   seg.perm = reinterpret_cast<int32_t*>(at(h.perm));
@@ -322,9 +324,7 @@ lora_status sgmv_multi_host(const lora_proj* projs, int32_t n_proj, int32_t n_ad
   if (s != LORA_OK) return s;
   for (int i = 0; i < n_proj; ++i) {
     const lora_proj& q = projs[i];
-    if (cudaMemcpy2DAsync(q.y, q.ldy * 2, at(h.y[i]), q.h_out * 2, q.h_out * 2, n, cudaMemcpyDefault, st) !=
-        cudaSuccess)
-      return LORA_ERR_CUDA;
+    if (copy_rows(q.y, q.ldy * 2, at(h.y[i]), q.h_out * 2, q.h_out * 2) != cudaSuccess) return LORA_ERR_CUDA;
   }
   return LORA_OK;
 }

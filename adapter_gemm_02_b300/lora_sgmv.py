@@ -445,9 +445,10 @@ def sgmv_multi_host(projs: Sequence, ids_host: torch.Tensor, *, workspace: Optio
     arr = c_projs if c_projs is not None else make_host_projs(projs)
     P, _, r = projs[0][1].shape
     n = ids_host.shape[0]
-    need = sgmv_multi_host_workspace_bytes(arr, n, P)
-    if workspace is None or workspace.numel() < need:
+    if workspace is None:
+        need = sgmv_multi_host_workspace_bytes(arr, n, P)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=projs[0][1].device)
+    # (a given workspace that is too small: LORA_ERR_WORKSPACE from the library)
     _check(lib.sgmv_multi_host(arr, len(arr), P, r, _ptr(ids_host), n, _ptr(workspace), workspace.numel(),
                                _ptr(err_flag), _stream(stream)), "sgmv_multi_host")
     return workspace
