@@ -69,6 +69,10 @@ struct SgmvCall {
   // else with lora_segment first, using seg_hist as its workspace).
   const int32_t* ids;
   int32_t* seg_hist;
+  // (sgmv_multi_host) the ids in host memory: they travel in the launch's
+  // parameters when the batch is segmented inside the launch (ids above is
+  // then not written), else they are copied to ids first
+  const int32_t* ids_host;
   // The long segments were handled by another launch (the backbone GEMM with
   // the fused expand): this call skips them and launches no tensor-tile kernel.
   int32_t long_done;

@@ -285,7 +285,6 @@ lora_status sgmv_multi_host(const lora_proj* projs, int32_t n_proj, int32_t n_ad
   auto at = [&](size_t off) { return ws + off; };
   int32_t* ids = reinterpret_cast<int32_t*>(at(h.ids));
   const size_t n = static_cast<size_t>(n_tokens);
-  if (cudaMemcpyAsync(ids, ids_host, n * 4, cudaMemcpyDefault, st) != cudaSuccess) return LORA_ERR_CUDA;
   // rows of width w with leading dimension ld: one flat copy when they are
   // contiguous (ld == w), else a 2-D copy
   auto copy_rows = [&](void* dst, size_t dld, const void* src, size_t sld, size_t w) {
@@ -308,6 +307,7 @@ lora_status sgmv_multi_host(const lora_proj* projs, int32_t n_proj, int32_t n_ad
   // segmentation inside the SGMV launch when the batch is small (else its own kernel first)
   SgmvCall c{};
   c.ids = ids;
+  c.ids_host = ids_host;  // in the launch's parameters, or copied to ids, as the launch needs them
   c.seg_hist = seg_plan(n_tokens, n_adapters).gmem ? reinterpret_cast<int32_t*>(at(h.hist)) : nullptr;
   c.mode = kModeFused;
   for (int i = 0; i < n_proj; ++i) {

@@ -51,6 +51,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 #include <type_traits>
 
@@ -190,10 +191,15 @@ struct CCTail {
 // storage as 2-D rows of r elements ([n_slots*h_in*rmax/r][r], box {r, BA}:
 // slot s starts at row s*h_in*rmax/r), tmB views its B storage as
 // [n_slots*rmax][h_out] (box {bw, r}: slot s starts at row s*rmax).
+// ids of a one-launch step that come from host memory travel in the
+// parameters (read by the producer warp from the constant bank)
+constexpr int kIdsInParamsMax = 128;
 struct CCParams {
   CUtensorMap tmA[kMaxProj];
   CUtensorMap tmB[kMaxProj];
   CCTail t;
+  int32_t n_ids_in_params;  // > 0: the one-launch step's ids are ids_in_params[0 .. n)
+  int32_t ids_in_params[kIdsInParamsMax];
 };
 
 // Rank R's stage contents in a ring shaped for rank RM >= R.
@@ -440,9 +446,10 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
       int32_t* adap_s = offs_s + ms + 1;
       int32_t* count_s = adap_s + max(ms, 1);
       // up to 64 tokens: ranks in registers; more: counting sort in shared memory
-      so = n <= 32   ? warp_segment_rank<1>(q.ids, n, P, perm_s, offs_s, adap_s, lane)
-           : n <= 64 ? warp_segment_rank<2>(q.ids, n, P, perm_s, offs_s, adap_s, lane)
-                     : warp_segment(q.ids, n, P, ids_s, cnt, perm_s, offs_s, adap_s, lane);
+      const int32_t* ids = p.n_ids_in_params > 0 ? p.ids_in_params : q.ids;
+      so = n <= 32   ? warp_segment_rank<1>(ids, n, P, perm_s, offs_s, adap_s, lane)
+           : n <= 64 ? warp_segment_rank<2>(ids, n, P, perm_s, offs_s, adap_s, lane)
+                     : warp_segment(ids, n, P, ids_s, cnt, perm_s, offs_s, adap_s, lane);
       fence_proxy_async_smem();  // stage 0 is next written by the tensor copies
       if (lane == 0) *count_s = so.S;
       __syncwarp();
@@ -1282,7 +1289,16 @@ lora_status launch_sgmv_cc(const SgmvCall& call, cudaStream_t stream) {
         call.n_adapters <= kSegInKernelMaxAdapters) {
       prm.t.ids = call.ids;
       extra = seg_extra_bytes(n, call.n_adapters);
+      if (call.ids_host != nullptr) {
+        static_assert(kIdsInParamsMax >= LSG_SEG_IN_KERNEL_MAX_TOKENS, "ids in the parameters");
+        std::memcpy(prm.ids_in_params, call.ids_host, static_cast<size_t>(n) * sizeof(int32_t));
+        prm.n_ids_in_params = n;
+      }
     } else {
+      if (call.ids_host != nullptr &&
+          cudaMemcpyAsync(const_cast<int32_t*>(call.ids), call.ids_host, static_cast<size_t>(n) * sizeof(int32_t),
+                          cudaMemcpyDefault, stream) != cudaSuccess)
+        return LORA_ERR_CUDA;
       const lora_status s = launch_segment(call.ids, n, call.n_adapters, const_cast<int32_t*>(call.seg.perm),
                                            const_cast<int32_t*>(call.seg.seg_offsets),
                                            const_cast<int32_t*>(call.seg.seg_adapter),

@@ -251,11 +251,13 @@ LORA_API lora_status sgmv_multi_segment(const lora_proj* projs, int32_t n_proj, 
 /*
  * The whole step from host memory: token ids, x and y0 rows in host memory
  * (pinned for an asynchronous call), adapter pools on the device.  Copies
- * ids, every distinct x and every y to the device workspace, segments the
- * ids and runs sgmv_multi on them (one launch for small batches, as
+ * every distinct x and every y to the device workspace, segments the ids and
+ * runs sgmv_multi on them (one launch for small batches, as
  * sgmv_multi_segment) and copies every y back, all ordered on `stream` with
- * one cudaMemcpyAsync / cudaMemcpy2DAsync per buffer; the caller
- * synchronises before reading y.  projs[i].x / .y are HOST pointers
+ * one cudaMemcpyAsync (contiguous rows) or cudaMemcpy2DAsync per buffer; the
+ * ids of a batch segmented inside the launch travel in the launch's
+ * parameters (read from ids_host when the call is made), larger batches copy
+ * them to the workspace first.  The caller synchronises before reading y.  projs[i].x / .y are HOST pointers
  * here (x [n][ldx], y [n][ldy]); A_pool / B_pool are device pointers.
  * Projections that name the same host x share one device copy.  The
  * workspace (device, 256-byte aligned, caller-owned) must hold
