@@ -383,9 +383,10 @@ def run_ours(args) -> None:
     # (measured before the clock sampler starts: once nvidia-smi has run in
     # this process's lifetime, host-side CUDA calls were measured to cost
     # 2-4x more, which this host-bound loop would inherit).
-    # Two pipelines (stream, pinned host buffers, device workspace) take the
-    # steps in turn, so one step's uploads overlap the previous step's kernels
-    # and download; every step still copies its own inputs in and its y out.
+    # E2E_STREAMS pipelines (stream, pinned host buffers, device workspace)
+    # take the steps in turn, so one step's uploads overlap the previous
+    # steps' kernels and downloads; every step still copies its own inputs in
+    # and its y out.
     e2e = None
     if not args.no_e2e:
         inp0 = copies[0][0]
