@@ -70,3 +70,31 @@ def test_layer_with_shared_inputs_and_workspace_reuse():
     torch.cuda.synchronize()
     for i, ((x, A, B, y, s), y0) in enumerate(zip(projs, refs2)):
         assert_within_tol(y, oracle.sgmv_ref(x, A.cpu(), B.cpu(), ids, s, y0, threads=THREADS), f"step 2 proj {i}")
+
+
+@pytest.mark.parametrize("n", [1, 127, 128, 129, 300])
+def test_ids_in_the_launch_or_copied(n):
+    """Batches of up to 128 tokens are segmented inside the launch and take
+    their ids from the launch's parameters, read when the call is made (so the
+    host ids may be rewritten as soon as it returns); larger ones copy the ids
+    to the workspace on the stream and segment them first.  Both sides of the
+    limit, with an invalid id, against the oracle."""
+    rng = np.random.default_rng(40 + n)
+    P, h_in, h_out, r = 24, 512, 768, 16
+    ids = rng.integers(0, P, n).astype(np.int32)
+    ids[n // 2] = -1  # invalid: row untouched, flagged
+    x = _host(rng.standard_normal((n, h_in)))
+    A = _dev(rng.standard_normal((P, h_in, r)) / np.sqrt(h_in))
+    B = _dev(rng.standard_normal((P, r, h_out)) / np.sqrt(r))
+    y = _host(rng.standard_normal((n, h_out)))
+    y0 = y.clone()
+    ids_h = torch.from_numpy(ids.copy()).pin_memory()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lsg.sgmv_multi_host([(x, A, B, y, 0.75)], ids_h, err_flag=err)
+    if n <= 128:
+        ids_h.fill_(0)  # the launch carries its own copy of the ids
+    torch.cuda.synchronize()
+    assert int(err.item()) == -4
+    assert torch.equal(y[n // 2], y0[n // 2])
+    ref = oracle.sgmv_ref(x, A.cpu(), B.cpu(), ids, 0.75, y0, threads=THREADS)
+    assert_within_tol(y, ref)
