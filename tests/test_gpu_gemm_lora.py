@@ -87,6 +87,29 @@ def test_interleaved_short_and_invalid_every_row(r):
     assert_within_tol(y, _ref(x, W, A, B, ids, 1.25))
 
 
+@pytest.mark.parametrize("n,interleave,r", [(2100, False, 64), (2100, True, 16), (3072, True, 32)])
+def test_units_of_two_token_tiles_every_row(n, interleave, r):
+    """Batches large enough for units of two token tiles (256 tokens x 256
+    columns) on every SM.  2100 tokens over 20 column tiles: 17 tiles, 180
+    pairs, so one whole wave of pairs and the 32 pairs left over split into
+    single tiles, the last tile ragged and without a partner; 3072 tokens: 240
+    pairs, the 92 left over fill more than half a wave and stay pairs.
+    Requests sorted (contiguous rows) or interleaved (gathered rows), with
+    short segments and an invalid id; every row against the oracle."""
+    rng = np.random.default_rng(n + r)
+    lens = [n // 3, n // 4, n // 5, n // 8]
+    lens.append(n - 31 - sum(lens))
+    ids = np.concatenate([_requests(lens, [4, 1, 7, 2, 5], interleave),
+                          rng.integers(0, 9, 30).astype(np.int32), np.array([-1], np.int32)])
+    if interleave:
+        ids = ids[rng.permutation(ids.size)]
+    P, h_in, h_out = 9, 512, 5120
+    x, W, A, B = _problem(f"gl_pairs_{n}_{r}", ids, P, h_in, h_out, r)
+    y, err = _run(x, W, A, B, ids, P, 0.75)
+    assert err == -4
+    assert_within_tol(y, _ref(x, W, A, B, ids, 0.75))
+
+
 def test_decode_batch_every_row():
     """A decode batch (every segment short): the GEMM writes x . W and the
     split-K kernel adds every token's delta."""
