@@ -89,6 +89,7 @@ struct GlParams {
   CUtensorMap tmXg;  // x, box {64, 1} (four-row gathers)
   CUtensorMap tmW;   // W [h_in][h_out], box {64, 64}, 128 B swizzle
   CUtensorMap tmB;   // B pool [P][r][h_out], box {64, RP, 1} (rows past r read zeros), 128 B swizzle
+  CUtensorMap tmY;   // y [n][h_out], box {64, 32}, 128 B swizzle (stores of 32 contiguous rows)
   GlTail t;
 };
 
@@ -100,6 +101,8 @@ struct GlCfg {
   static constexpr int kStage = kGlMT * kX + kW;
   static constexpr int kB = RP * 512;         // B tile [RP][256] (in the W part of a stage)
   static constexpr int kVop = 128 * RP * 2;   // one bf16 operand [128][RP]
+  static constexpr int kStg = 4 * 2 * 4096;   // y staging: per epilogue warp two [32][64] bf16 boxes
+  static constexpr int kOpSt = 2 * kVop > kStg ? 2 * kVop : kStg;  // operand pair, or y staging
   static constexpr uint32_t kSwM = (RP * 2) / 16 - 1;
   static_assert(kB <= kW, "B tile fits a stage");
 };
@@ -107,7 +110,9 @@ struct GlCfg {
 template <int R>
 struct GlSmem {
   alignas(1024) uint8_t st[kGlStages][GlCfg<R>::kStage];
-  alignas(1024) uint8_t vop[2][GlCfg<R>::kVop];  // hi, lo
+  // the operand pair (hi at 0, lo at kVop) while a unit's long segments are
+  // expanded; the epilogue's y staging after its accumulators are complete
+  alignas(1024) uint8_t opst[GlCfg<R>::kOpSt];
   alignas(16) GlTail t;
   alignas(8) uint64_t full[kGlStages];
   uint64_t empty[kGlStages];
@@ -241,6 +246,7 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
     prefetch_tmap(&p.tmXg);
     prefetch_tmap(&p.tmW);
     prefetch_tmap(&p.tmB);
+    prefetch_tmap(&p.tmY);
   }
   if (tid == 0) {
     for (int s = 0; s < kGlStages; ++s) {
@@ -425,7 +431,7 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
 #pragma unroll
               for (int hl = 0; hl < 2; ++hl) {
                 const uint64_t ad =
-                    umma_desc(smem_u32(sm.vop[hl]) + k * 32, 16, 8 * RP * 2, umma_layout(RP * 2));
+                    umma_desc(smem_u32(sm.opst + hl * Cfg::kVop) + k * 32, 16, 8 * RP * 2, umma_layout(RP * 2));
                 umma_bf16(acc, ad, bd, kId, true);
               }
             }
@@ -455,7 +461,7 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
     // ============================== epilogue: thread = tile row m
     const int m = warp * 32 + lane;
     const uint32_t tq = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    int ui = 0, nop = 0, cur_m = -1, cur_l = 0, op_m = -1, op_j = -1;
+    int ui = 0, nop = 0, cur_m = -1, cur_l = 0, op_m = -1, op_j = -1, nstg = 0;
     bool any = false;
     GlTile t[kGlMT];
     int yrow[kGlMT];
@@ -495,24 +501,31 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
 #pragma unroll
         for (int j = 0; j < kGlMaxRuns; ++j) {
           if (j >= t[mi].nrun || !ok) break;
+          const int tm = un.mt + mi;
+          const bool build = op_m != tm || op_j != j;
+          // this row's v (zero outside the segment), loaded before the wait
+          // for the previous operand's MMAs so the loads overlap them
+          float4 vv[R / 4];
+          if (build) {
+            const bool mine = yrow[mi] >= 0 && m >= t[mi].lo[j] && m < t[mi].hi[j];
+            const float4* vr = reinterpret_cast<const float4*>(q.v + static_cast<int64_t>(mine ? yrow[mi] : 0) * R);
+#pragma unroll
+            for (int e = 0; e < R / 4; ++e) vv[e] = mine ? vr[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
           if (nop > 0) {
             ok = gl_wait(sm, &sm.op_empty, (nop - 1) & 1, lane);
             if (!ok) break;
           }
-          const int tm = un.mt + mi;
-          if (op_m != tm || op_j != j) {
-            const bool mine = yrow[mi] >= 0 && m >= t[mi].lo[j] && m < t[mi].hi[j];
-            const float* vr = q.v + static_cast<int64_t>(mine ? yrow[mi] : 0) * R;
-            const uint32_t hrow = smem_u32(sm.vop[0]) + static_cast<uint32_t>(m) * (RP * 2);
-            const uint32_t lrow = smem_u32(sm.vop[1]) + static_cast<uint32_t>(m) * (RP * 2);
+          if (build) {
+            const uint32_t hrow = smem_u32(sm.opst) + static_cast<uint32_t>(m) * (RP * 2);
+            const uint32_t lrow = smem_u32(sm.opst + Cfg::kVop) + static_cast<uint32_t>(m) * (RP * 2);
 #pragma unroll
             for (int c = 0; c < RP / 8; ++c) {
               float f[8];
 #pragma unroll
               for (int e = 0; e < 8; ++e) f[e] = 0.f;
-              if (mine && c < R / 8) {
-                const float4 v0 = reinterpret_cast<const float4*>(vr)[2 * c];
-                const float4 v1 = reinterpret_cast<const float4*>(vr)[2 * c + 1];
+              if (c < R / 8) {
+                const float4 v0 = vv[2 * c], v1 = vv[2 * c + 1];
                 f[0] = s * v0.x;
                 f[1] = s * v0.y;
                 f[2] = s * v0.z;
@@ -549,45 +562,70 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
         }
       }
       if (!ok) break;
-      // ---- y = bf16(acc), 32 columns at a time, 16-byte stores of this row
+      // ---- y = bf16(acc), 64 columns at a time.  A warp whose 32 rows are
+      // contiguous rows of the tile stages them in shared memory (128 B
+      // swizzle) and stores one TMA box; other rows go out as 16-byte stores.
       ok = gl_wait(sm, &sm.acc_full[buf], use & 1u, lane);
       if (!ok) break;
       tc_fence_after();
-      const int c0 = un.nt * kGlBN;
+      const int c0 = un.nt * kGlBN, nstg0 = nstg;
 #pragma unroll
       for (int mi = 0; mi < kGlMT; ++mi) {
         if (t[mi].tlen <= 0) continue;  // the same for every lane
+        const bool box = t[mi].row >= 0 && warp * 32 + 32 <= t[mi].tlen;  // the same for every lane
         uint16_t* yp = yrow[mi] >= 0 ? q.y + static_cast<int64_t>(yrow[mi]) * q.ldy : nullptr;
 #pragma unroll 1
-        for (int c = 0; c < kGlBN / 32; ++c) {
-          const int col = c0 + c * 32;
+        for (int c = 0; c < kGlBN / 64; ++c) {
+          const int col = c0 + c * 64;
           if (col >= q.h_out) break;  // the same for every lane
-          uint32_t a32[32];
-          tmem_ld32(tq + static_cast<uint32_t>((buf + mi) * kGlBN + c * 32), a32);
+          uint32_t a0[32], a1[32];
+          tmem_ld32(tq + static_cast<uint32_t>((buf + mi) * kGlBN + c * 64), a0);
+          tmem_ld32(tq + static_cast<uint32_t>((buf + mi) * kGlBN + c * 64 + 32), a1);
           tmem_ld_wait();
-          if (yp != nullptr) {
+          uint32_t w[32];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              if (col + i * 8 < q.h_out) {
-                uint32_t w[4];
+          for (int e = 0; e < 16; ++e) {
+            const __nv_bfloat162 o0 = __floats2bfloat162_rn(__uint_as_float(a0[2 * e]), __uint_as_float(a0[2 * e + 1]));
+            const __nv_bfloat162 o1 = __floats2bfloat162_rn(__uint_as_float(a1[2 * e]), __uint_as_float(a1[2 * e + 1]));
+            w[e] = *reinterpret_cast<const uint32_t*>(&o0);
+            w[16 + e] = *reinterpret_cast<const uint32_t*>(&o1);
+          }
+          if (box) {
+            uint8_t* sb = sm.opst + warp * 8192 + (nstg & 1) * 4096;
+            if (lane == 0) bulk_wait_read1();  // the store that last read this buffer is done with it
+            __syncwarp();
+            const uint32_t rowa = smem_u32(sb) + static_cast<uint32_t>(lane) * 128;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const __nv_bfloat162 o = __floats2bfloat162_rn(__uint_as_float(a32[i * 8 + 2 * e]),
-                                                                 __uint_as_float(a32[i * 8 + 2 * e + 1]));
-                  w[e] = *reinterpret_cast<const uint32_t*>(&o);
-                }
-                *reinterpret_cast<uint4*>(yp + col + i * 8) = make_uint4(w[0], w[1], w[2], w[3]);
-              }
+            for (int i = 0; i < 8; ++i)
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(swz<7>(rowa + i * 16)), "r"(w[4 * i]),
+                           "r"(w[4 * i + 1]), "r"(w[4 * i + 2]), "r"(w[4 * i + 3])
+                           : "memory");
+            fence_proxy_async_smem();  // read by the tensor copy
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&p.tmY, col, t[mi].row + warp * 32, sb);
+              bulk_commit();
             }
+            ++nstg;
+          } else if (yp != nullptr) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (col + i * 8 < q.h_out)
+                *reinterpret_cast<uint4*>(yp + col + i * 8) =
+                    make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
           }
         }
       }
+      if (lane == 0) bulk_wait_read0();  // the staging area holds the next unit's operand
+      __syncwarp();
+      if (nstg != nstg0) op_m = -1;  // the cached operand was overwritten
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.acc_empty[buf]);
       ++ui;
     }
   }
+  if (aligned && warp < 4 && lane == 0) bulk_wait0();  // y stores complete before the CTA leaves
   tc_fence_before();
   __syncthreads();
   if (warp == 5) {
@@ -623,6 +661,12 @@ lora_status launch_gemm_lora_r(GlParams& prm, const void* x, int64_t ldx, const 
     const uint64_t str[2] = {static_cast<uint64_t>(t.h_out) * 2, static_cast<uint64_t>(t.h_out) * R * 2};
     const uint32_t box[3] = {64, static_cast<uint32_t>(GlCfg<R>::RP), 1};
     if ((s = encode_tmap_bf16(&prm.tmB, B_pool, 3, dims, str, box, 128)) != LORA_OK) return s;
+  }
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(t.h_out), n};
+    const uint64_t str[1] = {static_cast<uint64_t>(t.ldy) * 2};
+    const uint32_t box[2] = {64, 32};
+    if ((s = encode_tmap_bf16(&prm.tmY, t.y, 2, dims, str, box, 128)) != LORA_OK) return s;
   }
   auto kern = gemm_lora_kernel<R>;
   const size_t smem = sizeof(GlSmem<R>);
