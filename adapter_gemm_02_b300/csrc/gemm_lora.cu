@@ -62,6 +62,23 @@ constexpr int kGlMaxRuns = 3;  // long segments (>= 64 tokens) a 128-token windo
 #ifndef LSG_GL_PAIR
 #define LSG_GL_PAIR 1
 #endif
+// Fewer, larger tensor copies per stage (1): a pair of adjacent contiguous
+// tiles as one 256-row x box, and W as one 3-D box of its four 64-column
+// blocks when h_out is a multiple of 64; else a box per tile and per block.
+// LSG_GL_PREFETCH > 0: the producer also prefetches into L2 the boxes of the
+// stage that many k-blocks ahead.
+#ifndef LSG_GL_WIDE
+#define LSG_GL_WIDE 1
+#endif
+#ifndef LSG_GL_PREFETCH
+#define LSG_GL_PREFETCH 0
+#endif
+// k-partial slices the shrink launch may split each long tile into (at most
+// kGlVParts), so that its items cover more SMs.  Measured on the 13B layer
+// (6224 tokens, 49 tiles): at most 1 / 2 / 3 parts 3723 / 3652 / 3717 us.
+#ifndef LSG_GL_SHRINK_PARTS
+#define LSG_GL_SHRINK_PARTS 2
+#endif
 constexpr int kGlMT = LSG_GL_PAIR ? 2 : 1;       // token tiles per unit, at most
 constexpr int kGlStages = kGlMT == 2 ? 3 : 4;    // ring stages (64 KB / 48 KB)
 constexpr int kGlBufs = kGlMT == 2 ? 1 : 2;      // accumulator sets in the 512 TMEM columns
@@ -72,22 +89,27 @@ struct GlTail {
   const int32_t* seg_offsets;
   const int32_t* seg_adapter;
   const int32_t* num_segments;
-  const float* v;  // [n][r] fp32: rows of long-segment tokens
+  const float* v;  // [vparts][n][r] fp32: k-partial sums of v, rows of long-segment tokens
   uint16_t* y;
   int64_t ldy;
+  int64_t vslice;  // floats between the partial slices of v (n * r)
   int32_t* err_flag;
   int32_t n_tokens, max_segments, n_adapters, h_in, h_out;
   int32_t m_tiles, n_tiles, k_blocks;
   int32_t units;       // units of the launch
   int32_t pair_units;  // units [0, pair_units) take two token tiles, the rest one
   int32_t use_runs;    // long segments' expands are fused here (their v was computed)
+  int32_t vparts;      // partial slices of v to sum
+  int32_t w3d;         // W tiles as one 3-D box (tmW3)
   float scale;
 };
 
 struct GlParams {
   CUtensorMap tmX;   // x [n][h_in], box {64, 128}, 128 B swizzle
   CUtensorMap tmXg;  // x, box {64, 1} (four-row gathers)
+  CUtensorMap tmX2;  // x, box {64, 256} (two adjacent contiguous tiles)
   CUtensorMap tmW;   // W [h_in][h_out], box {64, 64}, 128 B swizzle
+  CUtensorMap tmW3;  // W as [h_out / 64][h_in][64], box {64, 64, 4}, 128 B swizzle (w3d)
   CUtensorMap tmB;   // B pool [P][r][h_out], box {64, RP, 1} (rows past r read zeros), 128 B swizzle
   CUtensorMap tmY;   // y [n][h_out], box {64, 32}, 128 B swizzle (stores of 32 contiguous rows)
   GlTail t;
@@ -244,7 +266,9 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
   if (warp == 4 && lane == 0) {
     prefetch_tmap(&p.tmX);
     prefetch_tmap(&p.tmXg);
+    prefetch_tmap(&p.tmX2);
     prefetch_tmap(&p.tmW);
+    prefetch_tmap(&p.tmW3);
     prefetch_tmap(&p.tmB);
     prefetch_tmap(&p.tmY);
   }
@@ -320,19 +344,46 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
 #pragma unroll
       for (int mi = 0; mi < kGlMT; ++mi) xbytes += t[mi].tlen > 0 ? Cfg::kX : 0;
       const int c0 = un.nt * kGlBN;
+      // both tiles' rows as one box: two contiguous tiles, the second right after the first
+      const bool xpair = LSG_GL_WIDE && kGlMT == 2 && t[0].tlen > 0 && t[0].row >= 0 &&
+                         t[kGlMT - 1].tlen > 0 && t[kGlMT - 1].row == t[0].row + 128;
       for (int kb = 0; kb < q.k_blocks && ok; ++kb) {
         ok = gl_wait(sm, &sm.empty[slot], ph ^ 1u, lane);
         if (!ok) break;
         uint8_t* st = sm.st[slot];
         if (lane == 0) {
           mbar_arrive_expect_tx(&sm.full[slot], xbytes + static_cast<uint32_t>(Cfg::kW));
+          if (xpair) {
+            tma_load_2d(st, &p.tmX2, kb * 64, t[0].row, &sm.full[slot]);
+          } else {
 #pragma unroll
-          for (int mi = 0; mi < kGlMT; ++mi)
-            if (t[mi].tlen > 0 && t[mi].row >= 0)
-              tma_load_2d(st + mi * Cfg::kX, &p.tmX, kb * 64, t[mi].row, &sm.full[slot]);
+            for (int mi = 0; mi < kGlMT; ++mi)
+              if (t[mi].tlen > 0 && t[mi].row >= 0)
+                tma_load_2d(st + mi * Cfg::kX, &p.tmX, kb * 64, t[mi].row, &sm.full[slot]);
+          }
+          if (q.w3d) {
+            tma_load_3d(st + kGlMT * Cfg::kX, &p.tmW3, 0, kb * 64, c0 / 64, &sm.full[slot]);
+          } else {
 #pragma unroll
-          for (int h = 0; h < 4; ++h)
-            tma_load_2d(st + kGlMT * Cfg::kX + h * 8192, &p.tmW, c0 + h * 64, kb * 64, &sm.full[slot]);
+            for (int h = 0; h < 4; ++h)
+              tma_load_2d(st + kGlMT * Cfg::kX + h * 8192, &p.tmW, c0 + h * 64, kb * 64, &sm.full[slot]);
+          }
+          if (LSG_GL_PREFETCH > 0 && kb + LSG_GL_PREFETCH < q.k_blocks) {
+            const int kp = kb + LSG_GL_PREFETCH;
+            if (xpair) {
+              tma_prefetch_2d(&p.tmX2, kp * 64, t[0].row);
+            } else {
+#pragma unroll
+              for (int mi = 0; mi < kGlMT; ++mi)
+                if (t[mi].tlen > 0 && t[mi].row >= 0) tma_prefetch_2d(&p.tmX, kp * 64, t[mi].row);
+            }
+            if (q.w3d) {
+              tma_prefetch_3d(&p.tmW3, 0, kp * 64, c0 / 64);
+            } else {
+#pragma unroll
+              for (int h = 0; h < 4; ++h) tma_prefetch_2d(&p.tmW, c0 + h * 64, kp * 64);
+            }
+          }
         }
         __syncwarp();  // the stage's byte count is registered before the gathers land
 #pragma unroll
@@ -511,6 +562,18 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
             const float4* vr = reinterpret_cast<const float4*>(q.v + static_cast<int64_t>(mine ? yrow[mi] : 0) * R);
 #pragma unroll
             for (int e = 0; e < R / 4; ++e) vv[e] = mine ? vr[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+            // the shrink's k-partial slices, summed in slice order
+            for (int pp = 1; pp < q.vparts && mine; ++pp) {
+              const float4* vp = vr + pp * (q.vslice / 4);
+#pragma unroll
+              for (int e = 0; e < R / 4; ++e) {
+                const float4 u = vp[e];
+                vv[e].x += u.x;
+                vv[e].y += u.y;
+                vv[e].z += u.z;
+                vv[e].w += u.w;
+              }
+            }
           }
           if (nop > 0) {
             ok = gl_wait(sm, &sm.op_empty, (nop - 1) & 1, lane);
@@ -648,12 +711,24 @@ lora_status launch_gemm_lora_r(GlParams& prm, const void* x, int64_t ldx, const 
     const uint32_t box[2] = {64, 128}, box_g[2] = {64, 1};
     if ((s = encode_tmap_bf16(&prm.tmX, x, 2, dims, str, box, 128)) != LORA_OK) return s;
     if ((s = encode_tmap_bf16(&prm.tmXg, x, 2, dims, str, box_g, 128)) != LORA_OK) return s;
+    const uint32_t box2[2] = {64, 256};
+    if ((s = encode_tmap_bf16(&prm.tmX2, x, 2, dims, str, box2, 128)) != LORA_OK) return s;
   }
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(t.h_out), static_cast<uint64_t>(t.h_in)};
     const uint64_t str[1] = {static_cast<uint64_t>(t.h_out) * 2};
     const uint32_t box[2] = {64, 64};
     if ((s = encode_tmap_bf16(&prm.tmW, W, 2, dims, str, box, 128)) != LORA_OK) return s;
+  }
+  // W viewed as [h_out / 64][h_in][64] (a 64-column block's rows h_out apart,
+  // the blocks 128 bytes apart): a [4][64][64] box is one W tile in the
+  // stage's layout.  Only when every block is whole, so no box reads past W.
+  t.w3d = 0;
+  if (LSG_GL_WIDE && t.h_out % 64 == 0) {
+    const uint64_t dims[3] = {64, static_cast<uint64_t>(t.h_in), static_cast<uint64_t>(t.h_out / 64)};
+    const uint64_t str[2] = {static_cast<uint64_t>(t.h_out) * 2, 128};
+    const uint32_t box[3] = {64, 64, 4};
+    t.w3d = encode_tmap_bf16(&prm.tmW3, W, 3, dims, str, box, 128) == LORA_OK ? 1 : 0;
   }
   {
     const uint64_t dims[3] = {static_cast<uint64_t>(t.h_out), static_cast<uint64_t>(R),
@@ -729,6 +804,9 @@ lora_status launch_gemm_lora(const GemmLoraCall& c, cudaStream_t stream) {
   sh.seg = c.seg;
   sh.v_out = c.v;
   sh.err_flag = c.err_flag;
+  int32_t vparts = 1;
+  sh.v_parts_max = std::min(LSG_GL_SHRINK_PARTS, kGlVParts);
+  sh.v_parts = &vparts;
   const bool runs = sgmv_tc_applicable(sh);
   if (runs) {
     const lora_status s = launch_sgmv_tc(sh, stream);
@@ -754,6 +832,8 @@ lora_status launch_gemm_lora(const GemmLoraCall& c, cudaStream_t stream) {
   t.n_tiles = ceil_div(c.h_out, kGlBN);
   t.k_blocks = ceil_div(c.h_in, 64);
   t.use_runs = runs ? 1 : 0;
+  t.vparts = runs ? vparts : 1;
+  t.vslice = static_cast<int64_t>(n) * c.r;
   t.scale = c.scale;
   lora_status s;
   switch (c.r) {

@@ -54,6 +54,13 @@ struct SgmvCall {
   int n_adapters;
   lora_segments seg;
   float* v_out;       // shrink output [n][r]
+  // Shrink mode: v_out may hold up to v_parts_max slices [n][r]; the
+  // tensor-tile kernel then splits each long tile's k-blocks into that many
+  // parts at most, slice p holding the partial sum of part p (the sum over
+  // the slices is v).  The number of slices written goes to *v_parts
+  // (host memory) when v_parts is not null.  0 or 1: v_out is v itself.
+  int32_t v_parts_max;
+  int32_t* v_parts;
   const float* v_in;  // expand input [n][r]
   int32_t* err_flag;
   // Slot arenas (null slot_of: each pool is contiguous, [n_adapters] slabs of
@@ -89,6 +96,7 @@ bool sgmv_tc_applicable(const SgmvCall& call);
 lora_status launch_sgmv_tc(const SgmvCall& call, cudaStream_t stream);
 
 // ---- backbone GEMM with the LoRA expand fused into its epilogue
+constexpr int kGlVParts = 4;  // k-partial slices of v the shrink may write
 struct GemmLoraCall {
   const uint16_t* x;
   int64_t ldx;
@@ -100,7 +108,7 @@ struct GemmLoraCall {
   lora_segments seg;
   uint16_t* y;
   int64_t ldy;
-  float* v;  // workspace [n][r]
+  float* v;  // workspace [kGlVParts][n][r]: the shrink's k-partial slices
   int32_t* err_flag;
 };
 lora_status launch_gemm_lora(const GemmLoraCall& call, cudaStream_t stream);

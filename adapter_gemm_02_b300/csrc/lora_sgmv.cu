@@ -366,7 +366,7 @@ lora_status sgmv_multi_segment(const lora_proj* projs, int32_t n_proj, int32_t n
 
 size_t gemm_lora_workspace_bytes(int32_t n_tokens, int32_t r) {
   if (n_tokens < 0 || !rank_ok(r)) return 0;
-  return static_cast<size_t>(n_tokens) * r * sizeof(float);
+  return static_cast<size_t>(kGlVParts) * n_tokens * r * sizeof(float);
 }
 
 lora_status gemm_lora(const lora_bf16* x, int64_t ldx, const lora_bf16* W, const lora_bf16* A_pool,

@@ -201,6 +201,8 @@ struct TcTail {
   int32_t max_segments;
   int32_t n_adapters;
   int32_t csplit;  // CTAs per item (cluster size C): split-K shrink, split-N expand
+  int32_t kparts;  // shrink mode: items per (tile, projection), each a part of the k-blocks;
+                   // part p writes its partial v to v_out + p * n * r
   // Slot arenas (null slot_of: contiguous pool, slab = adapter id): a long
   // segment is taken when its adapter's slot is valid and its rank is this
   // kernel's rank; the slab index is then the slot.
@@ -535,6 +537,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
     lo = min(n, crank * per);
     hi = min(n, lo + per);
   };
+  // the k-blocks of item slot `is`: the cluster's share, or (shrink mode
+  // with k-parts) the part the slot's chunk index names
+  auto krange = [&](int n, int is, int& lo, int& hi) {
+    if (!kHasExpand && sm.t.kparts > 1) {
+      const int per = (n + sm.t.kparts - 1) / sm.t.kparts;
+      lo = min(n, sm.t.item_chunk[is] * per);
+      hi = min(n, lo + per);
+    } else {
+      split(n, lo, hi);
+    }
+  };
 
   {
     static_assert(sizeof(TcTail) % 4 == 0, "tail size");
@@ -617,7 +630,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       if (t.a < 0 || t.a >= q.n_slabs) continue;
       const int pj = q.item_proj[is];
       int kb0, kb1;
-      split((q.proj[pj].h_in + 63) >> 6, kb0, kb1);
+      krange((q.proj[pj].h_in + 63) >> 6, is, kb0, kb1);
       int rr[4] = {0, 0, 0, 0};
       if (t.row < 0) tile_rows4(q, t, lane, rr);
       bool ok = true;
@@ -746,7 +759,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
       if (t.a < 0 || t.a >= q.n_slabs) continue;
       const TcProj& pr = q.proj[q.item_proj[is]];
       int kb0, kb1;
-      split((pr.h_in + 63) >> 6, kb0, kb1);
+      krange((pr.h_in + 63) >> 6, is, kb0, kb1);
       // the epilogue has read the previous item's v out of TMEM
       bool ok = it == 0 || warp_wait(sm, &sm.v_read, (it - 1) & 1, lane);
       if (!ok) break;
@@ -926,7 +939,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
         }
       }
       int kb0 = 0, kb1 = 0;
-      if (kHasShrink) split((pr.h_in + 63) >> 6, kb0, kb1);
+      if (kHasShrink) krange((pr.h_in + 63) >> 6, is, kb0, kb1);
       bool ok = true;
       if (eg == 0) {
         uint32_t v[RP];
@@ -975,7 +988,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) sgmv_tc_kernel(const __grid_con
         if constexpr (!kHasExpand) {
           // ---- shrink mode: v rows to device memory (fp32, token order)
           if (yrow >= 0) {
-            float4* dst = reinterpret_cast<float4*>(q.v_out + static_cast<int64_t>(yrow) * R);
+            float4* dst = reinterpret_cast<float4*>(
+                q.v_out + (static_cast<int64_t>(q.kparts > 1 ? ch : 0) * q.n_tokens + yrow) * R);
 #pragma unroll
             for (int j = 0; j < R / 4; ++j)
               dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
@@ -1356,6 +1370,22 @@ lora_status plan_and_launch(const SgmvCall& call, cudaStream_t stream) {
     if (best.C == 0 || pl.cost < best.cost * 0.999) best = pl;
   }
   if (best.C == 0) return LORA_ERR_UNSUPPORTED;
+  // Shrink mode into k-partial slices: a batch of few tiles splits each
+  // tile's k-blocks over up to v_parts_max items, so that about one item per
+  // co-resident CTA streams its part of x (one item per tile would leave most
+  // SMs idle and each item a long serial stream).
+  int kparts = 1;
+  if constexpr (MODE == kModeShrink) {
+    if (call.v_parts_max > 1) {
+      int G = 0;
+      const lora_status st = tc_groups<R, false, MODE>(1, G);
+      if (st != LORA_OK) return st;
+      kparts = std::clamp(G / (tiles_est * call.n_proj), 1,
+                          std::min({call.v_parts_max, min_kb, kMaxItemsPerTile / call.n_proj}));
+      for (int i = 0; i < call.n_proj; ++i) best.nch[i] = kparts;
+    }
+  }
+  if (call.v_parts != nullptr) *call.v_parts = kparts;
   int ipt = 0;
   for (int i = 0; i < call.n_proj; ++i) {
     const ProjArgs& a = call.proj[i];
@@ -1400,6 +1430,7 @@ lora_status plan_and_launch(const SgmvCall& call, cudaStream_t stream) {
       for (int k = 0; k < ipt; ++k) prm.t.slot_order[k] = static_cast<int8_t>(k);
   }
   prm.t.csplit = best.C;
+  prm.t.kparts = kparts;
   prm.t.slot_of = call.slot_of;
   prm.t.rank_of = call.rank_of;
   prm.t.n_slabs = call.slot_of ? call.n_slots : call.n_adapters;

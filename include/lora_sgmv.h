@@ -289,8 +289,10 @@ LORA_API lora_status sgmv_multi_host(const lora_proj* projs, int32_t n_proj, int
  *   W [h_in][h_out] row-major bf16 (device), shared by every token,
  *     16-byte aligned.
  *   A_pool, B_pool, seg, r: as sgmv_fused.
- *   workspace: device memory of gemm_lora_workspace_bytes(n, r) bytes (v,
- *     fp32 [n][r]), 16-byte aligned; contents on exit unspecified.
+ *   workspace: device memory of gemm_lora_workspace_bytes(n, r) bytes (v as
+ *     up to four fp32 [n][r] slices of partial sums over parts of h_in,
+ *     which the GEMM launch adds in slice order), 16-byte aligned; contents
+ *     on exit unspecified.
  * A token whose adapter id is invalid (outside every segment) gets
  * y = x . W; err_flag as for lora_segment.  Errors: as sgmv_fused, plus W
  * NULL (LORA_ERR_INVALID_ARG) or misaligned, workspace missing or too small
