@@ -65,13 +65,8 @@ constexpr int kGlMaxRuns = 3;  // long segments (>= 64 tokens) a 128-token windo
 // Fewer, larger tensor copies per stage (1): a pair of adjacent contiguous
 // tiles as one 256-row x box, and W as one 3-D box of its four 64-column
 // blocks when h_out is a multiple of 64; else a box per tile and per block.
-// LSG_GL_PREFETCH > 0: the producer also prefetches into L2 the boxes of the
-// stage that many k-blocks ahead.
 #ifndef LSG_GL_WIDE
 #define LSG_GL_WIDE 1
-#endif
-#ifndef LSG_GL_PREFETCH
-#define LSG_GL_PREFETCH 0
 #endif
 // k-partial slices the shrink launch may split each long tile into (at most
 // kGlVParts), so that its items cover more SMs.  Measured on the 13B layer
@@ -367,22 +362,6 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
 #pragma unroll
             for (int h = 0; h < 4; ++h)
               tma_load_2d(st + kGlMT * Cfg::kX + h * 8192, &p.tmW, c0 + h * 64, kb * 64, &sm.full[slot]);
-          }
-          if (LSG_GL_PREFETCH > 0 && kb + LSG_GL_PREFETCH < q.k_blocks) {
-            const int kp = kb + LSG_GL_PREFETCH;
-            if (xpair) {
-              tma_prefetch_2d(&p.tmX2, kp * 64, t[0].row);
-            } else {
-#pragma unroll
-              for (int mi = 0; mi < kGlMT; ++mi)
-                if (t[mi].tlen > 0 && t[mi].row >= 0) tma_prefetch_2d(&p.tmX, kp * 64, t[mi].row);
-            }
-            if (q.w3d) {
-              tma_prefetch_3d(&p.tmW3, 0, kp * 64, c0 / 64);
-            } else {
-#pragma unroll
-              for (int h = 0; h < 4; ++h) tma_prefetch_2d(&p.tmW, c0 + h * 64, kp * 64);
-            }
           }
         }
         __syncwarp();  // the stage's byte count is registered before the gathers land

@@ -201,13 +201,6 @@ __device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int32_t c0, in
                : "memory");
 }
 
-__device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int32_t c0, int32_t c1, int32_t c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(tmap)),
-               "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
-
 // This CTA's shared memory -> global, tracked as a bulk async-group of the
 // executing thread.  dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
