@@ -74,6 +74,16 @@ constexpr int kGlMaxRuns = 3;  // long segments (>= 64 tokens) a 128-token windo
 #ifndef LSG_GL_SHRINK_PARTS
 #define LSG_GL_SHRINK_PARTS 2
 #endif
+// Clusters of LSG_GL_CM CTAs (1 or 2): the CTAs of a cluster take the same
+// column tile of different token tiles, each loads a 1/CM share of the W
+// tile and multicasts it to every CTA of the cluster, so each SM reads
+// 1/CM of the W bytes from L2.  A ring slot is refilled only after every CTA
+// of the cluster has consumed it.
+#ifndef LSG_GL_CM
+#define LSG_GL_CM 1
+#endif
+constexpr int kGlCM = LSG_GL_CM;
+static_assert(kGlCM == 1 || kGlCM == 2, "cluster size");
 constexpr int kGlMT = LSG_GL_PAIR ? 2 : 1;       // token tiles per unit, at most
 constexpr int kGlStages = kGlMT == 2 ? 3 : 4;    // ring stages (64 KB / 48 KB)
 constexpr int kGlBufs = kGlMT == 2 ? 1 : 2;      // accumulator sets in the 512 TMEM columns
@@ -194,21 +204,26 @@ __device__ __forceinline__ void gl_tile(const GlTail& q, int S, int mt, int lane
   }
 }
 
-// Unit u: token tiles [mt, mt + ntl) x column tile nt.  Units below
-// pair_units are pairs (2p, 2p + 1), column tiles inner; the units after them
-// split the remaining pairs into their two tiles, in the same order.
+// Unit u of a cluster, for its CTA `crank`: token tiles [mt, mt + ntl) x
+// column tile nt.  A unit takes a group of kGlCM pairs, pair (g kGlCM + crank)
+// for CTA crank.  Units below pair_units are whole pairs (2p, 2p + 1), column
+// tiles inner; the units after them split the remaining groups into their
+// first and second tiles, in the same order.
 struct GlUnit {
   int mt, ntl, nt;
 };
 
-__device__ __forceinline__ GlUnit gl_unit(const GlTail& q, int u) {
-  if (kGlMT == 1) return GlUnit{u / q.n_tiles, 1, u % q.n_tiles};
-  if (u < q.pair_units) {
-    const int pr = u / q.n_tiles;
-    return GlUnit{2 * pr, 2, u - pr * q.n_tiles};
+__device__ __forceinline__ GlUnit gl_unit(const GlTail& q, int u, int crank) {
+  if (kGlMT == 1) {
+    const int g = u / q.n_tiles;
+    return GlUnit{g * kGlCM + crank, 1, u - g * q.n_tiles};
   }
-  const int s = u - q.pair_units, w = q.pair_units + (s >> 1), pr = w / q.n_tiles;
-  return GlUnit{2 * pr + (s & 1), 1, w - pr * q.n_tiles};
+  if (u < q.pair_units) {
+    const int g = u / q.n_tiles;
+    return GlUnit{2 * (g * kGlCM + crank), 2, u - g * q.n_tiles};
+  }
+  const int s = u - q.pair_units, w = q.pair_units + (s >> 1), g = w / q.n_tiles;
+  return GlUnit{2 * (g * kGlCM + crank) + (s & 1), 1, w - g * q.n_tiles};
 }
 
 // The unit's tiles (a full warp); a tile index past the unit gets no rows.
@@ -229,6 +244,32 @@ __device__ __forceinline__ bool gl_tiles(const GlTail& q, int S, const GlUnit& u
   return any;
 }
 
+// A unit seen from one CTA of its cluster (a full warp): its own tiles, and
+// whether any CTA of the cluster has rows; nslot[mi]: the long segments'
+// expand slots of tile mi, the most any CTA of the cluster has (a CTA with
+// fewer fills the rest with empty slots, so the rings stay in step).
+struct GlView {
+  bool own, all;
+  int nslot[kGlMT];
+};
+
+__device__ __forceinline__ GlView gl_view(const GlTail& q, int S, int u, int crank, int lane, GlTile (&t)[kGlMT]) {
+  GlView v;
+  v.own = gl_tiles(q, S, gl_unit(q, u, crank), lane, t);
+  v.all = v.own;
+#pragma unroll
+  for (int mi = 0; mi < kGlMT; ++mi) v.nslot[mi] = t[mi].nrun;
+#pragma unroll
+  for (int k = 0; k < kGlCM; ++k) {
+    if (k == crank) continue;
+    GlTile tk[kGlMT];
+    v.all |= gl_tiles(q, S, gl_unit(q, u, k), lane, tk);
+#pragma unroll
+    for (int mi = 0; mi < kGlMT; ++mi) v.nslot[mi] = max(v.nslot[mi], tk[mi].nrun);
+  }
+  return v;
+}
+
 template <typename SM>
 __device__ __forceinline__ bool gl_wait(SM& sm, uint64_t* bar, uint32_t parity, int lane) {
   bool ok = true;
@@ -247,6 +288,7 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
   using Cfg = GlCfg<R>;
   using SM = GlSmem<R>;
   constexpr int RP = Cfg::RP;
+  constexpr uint16_t kMask = static_cast<uint16_t>((1u << kGlCM) - 1u);  // every CTA of the cluster
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   auto& sm = *reinterpret_cast<SM*>(smem_raw);
   const GlTail& q = sm.t;
@@ -270,7 +312,7 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
   if (tid == 0) {
     for (int s = 0; s < kGlStages; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 1);
+      mbar_init(&sm.empty[s], kGlCM);  // every CTA of the cluster has consumed the slot
     }
     for (int b = 0; b < kGlBufs; ++b) {
       mbar_init(&sm.acc_full[b], 1);
@@ -286,13 +328,18 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (kGlCM > 1) {  // every CTA's barriers exist before a peer copies or commits into them
+    cluster_arrive_relaxed();
+    cluster_wait_acquire();
+  }
   const uint32_t tmem = sm.tmem_base;
   pdl_launch_dependents();
   pdl_wait();  // v (and the segmentation) come from the launches before
   const bool aligned = (smem_u32(sm.st) & 1023u) == 0;
   if (!aligned && tid == 0) set_err(q.err_flag, LORA_ERR_UNSUPPORTED);
 
-  const int u0 = static_cast<int>(blockIdx.x), ustep = static_cast<int>(gridDim.x);
+  const int crank = static_cast<int>(blockIdx.x) % kGlCM;
+  const int u0 = static_cast<int>(blockIdx.x) / kGlCM, ustep = static_cast<int>(gridDim.x) / kGlCM;
   const int S = min(max(*q.num_segments, 0), q.max_segments);
 
   if (aligned && warp == 4) {
@@ -300,7 +347,7 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
     int slot = 0;
     uint32_t ph = 0, filled = 0, fill_par = 0;
     int cur_m = -1, cur_l = 0;
-    bool any = false;
+    GlView v{};
     GlTile t[kGlMT];
     int rr[kGlMT][4];
     auto advance = [&]() {
@@ -313,9 +360,9 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
     };
     bool ok = true;
     for (int u = u0; u < q.units && ok; u += ustep) {
-      const GlUnit un = gl_unit(q, u);
+      const GlUnit un = gl_unit(q, u, crank);
       if (un.mt != cur_m || un.ntl != cur_l) {
-        any = gl_tiles(q, S, un, lane, t);
+        v = gl_view(q, S, u, crank, lane, t);
         cur_m = un.mt;
         cur_l = un.ntl;
 #pragma unroll
@@ -334,7 +381,7 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
           }
         }
       }
-      if (!any) continue;  // the empty half of the last pair: no work in any role
+      if (!v.all) continue;  // the empty half of the last pairs: no work in any role of the cluster
       uint32_t xbytes = 0;
 #pragma unroll
       for (int mi = 0; mi < kGlMT; ++mi) xbytes += t[mi].tlen > 0 ? Cfg::kX : 0;
@@ -356,7 +403,12 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
               if (t[mi].tlen > 0 && t[mi].row >= 0)
                 tma_load_2d(st + mi * Cfg::kX, &p.tmX, kb * 64, t[mi].row, &sm.full[slot]);
           }
-          if (q.w3d) {
+          if constexpr (kGlCM > 1) {
+            // this CTA's share of the W tile, into every CTA of the cluster
+#pragma unroll
+            for (int h = crank * (4 / kGlCM); h < (crank + 1) * (4 / kGlCM); ++h)
+              tma_load_2d_mc(st + kGlMT * Cfg::kX + h * 8192, &p.tmW, c0 + h * 64, kb * 64, &sm.full[slot], kMask);
+          } else if (q.w3d) {
             tma_load_3d(st + kGlMT * Cfg::kX, &p.tmW3, 0, kb * 64, c0 / 64, &sm.full[slot]);
           } else {
 #pragma unroll
@@ -377,15 +429,19 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
       for (int mi = 0; mi < kGlMT; ++mi) {
 #pragma unroll
         for (int j = 0; j < kGlMaxRuns; ++j) {
-          if (j >= t[mi].nrun || !ok) break;
+          if (j >= v.nslot[mi] || !ok) break;
           ok = gl_wait(sm, &sm.empty[slot], ph ^ 1u, lane);
           if (!ok) break;
           uint8_t* st = sm.st[slot] + kGlMT * Cfg::kX;
           if (lane == 0) {
-            mbar_arrive_expect_tx(&sm.full[slot], static_cast<uint32_t>(Cfg::kB));
+            if (j < t[mi].nrun) {
+              mbar_arrive_expect_tx(&sm.full[slot], static_cast<uint32_t>(Cfg::kB));
 #pragma unroll
-            for (int h = 0; h < 4; ++h)
-              tma_load_3d(st + h * RP * 128, &p.tmB, c0 + h * 64, 0, t[mi].a[j], &sm.full[slot]);
+              for (int h = 0; h < 4; ++h)
+                tma_load_3d(st + h * RP * 128, &p.tmB, c0 + h * 64, 0, t[mi].a[j], &sm.full[slot]);
+            } else {
+              mbar_arrive(&sm.full[slot]);  // an empty slot: keeps the cluster's rings in step
+            }
           }
           __syncwarp();
           advance();
@@ -402,22 +458,30 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
     constexpr uint32_t kId = umma_idesc_bf16(128, kGlBN, 0, 1);
     int slot = 0, ui = 0, nop = 0, cur_m = -1, cur_l = 0;
     uint32_t ph = 0;
-    bool any = false;
+    GlView v{};
     GlTile t[kGlMT];
     bool ok = true;
+    // a consumed slot goes back to the producers of every CTA of the cluster
+    auto release = [&](int sl) {
+      if constexpr (kGlCM > 1) umma_commit_mc(&sm.empty[sl], kMask);
+      else umma_commit(&sm.empty[sl]);
+    };
     for (int u = u0; u < q.units && ok; u += ustep) {
-      const GlUnit un = gl_unit(q, u);
+      const GlUnit un = gl_unit(q, u, crank);
       if (un.mt != cur_m || un.ntl != cur_l) {
-        any = gl_tiles(q, S, un, lane, t);
+        v = gl_view(q, S, u, crank, lane, t);
         cur_m = un.mt;
         cur_l = un.ntl;
       }
-      if (!any) continue;
+      if (!v.all) continue;
+      const bool mine = v.own;  // no rows here: the cluster's slots are consumed, no MMAs
       const int buf = ui % kGlBufs;
       const uint32_t use = static_cast<uint32_t>(ui / kGlBufs);
-      ok = gl_wait(sm, &sm.acc_empty[buf], (use & 1u) ^ 1u, lane);
-      if (!ok) break;
-      tc_fence_after();
+      if (mine) {
+        ok = gl_wait(sm, &sm.acc_empty[buf], (use & 1u) ^ 1u, lane);
+        if (!ok) break;
+        tc_fence_after();
+      }
       for (int kb = 0; kb < q.k_blocks && ok; ++kb) {
         ok = gl_wait(sm, &sm.full[slot], ph, lane);
         if (!ok) break;
@@ -436,7 +500,7 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
               umma_bf16(acc, ad, bd, kId, kb > 0 || k > 0);
             }
           }
-          umma_commit(&sm.empty[slot]);
+          release(slot);
         }
         __syncwarp();
         if (++slot == kGlStages) {
@@ -449,11 +513,12 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
         const uint32_t acc = tmem + static_cast<uint32_t>((buf + mi) * kGlBN);
 #pragma unroll
         for (int j = 0; j < kGlMaxRuns; ++j) {
-          if (j >= t[mi].nrun || !ok) break;
-          ok = gl_wait(sm, &sm.op_full, nop & 1, lane) && gl_wait(sm, &sm.full[slot], ph, lane);
+          if (j >= v.nslot[mi] || !ok) break;
+          const bool run = j < t[mi].nrun;
+          ok = (!run || gl_wait(sm, &sm.op_full, nop & 1, lane)) && gl_wait(sm, &sm.full[slot], ph, lane);
           if (!ok) break;
           tc_fence_after();
-          if (lane == 0) {
+          if (lane == 0 && run) {
             const uint32_t bs = smem_u32(sm.st[slot]) + kGlMT * Cfg::kX;
 #pragma unroll
             for (int k = 0; k < RP / 16; ++k) {
@@ -465,11 +530,11 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
                 umma_bf16(acc, ad, bd, kId, true);
               }
             }
-            umma_commit(&sm.empty[slot]);
             umma_commit(&sm.op_empty);
           }
+          if (lane == 0) release(slot);
           __syncwarp();
-          ++nop;
+          if (run) ++nop;
           if (++slot == kGlStages) {
             slot = 0;
             ph ^= 1u;
@@ -477,9 +542,11 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
         }
       }
       if (!ok) break;
-      if (lane == 0) umma_commit(&sm.acc_full[buf]);
-      __syncwarp();
-      ++ui;
+      if (mine) {
+        if (lane == 0) umma_commit(&sm.acc_full[buf]);
+        __syncwarp();
+        ++ui;
+      }
     }
     // every MMA issued here has completed before TMEM is released
     if (lane == 0) {
@@ -499,7 +566,7 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
     bool ok = true;
     const float s = q.scale;
     for (int u = u0; u < q.units && ok; u += ustep) {
-      const GlUnit un = gl_unit(q, u);
+      const GlUnit un = gl_unit(q, u, crank);
       if (un.mt != cur_m || un.ntl != cur_l) {
         any = gl_tiles(q, S, un, lane, t);
         cur_m = un.mt;
@@ -670,6 +737,10 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
   if (aligned && warp < 4 && lane == 0) bulk_wait0();  // y stores complete before the CTA leaves
   tc_fence_before();
   __syncthreads();
+  if (kGlCM > 1) {  // no CTA leaves while a peer may still copy or commit into it
+    cluster_arrive_relaxed();
+    cluster_wait_acquire();
+  }
   if (warp == 5) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -726,46 +797,66 @@ lora_status launch_gemm_lora_r(GlParams& prm, const void* x, int64_t ldx, const 
   const size_t smem = sizeof(GlSmem<R>);
   static_assert(sizeof(GlSmem<R>) <= 227 * 1024, "shared memory of one CTA");
   static std::mutex mu;
-  static int sms_cache[64];
+  static int groups_cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
-  int sms = 0;
+  int clusters = 0;  // co-resident clusters of kGlCM CTAs (one CTA per SM)
   {
     std::lock_guard<std::mutex> lk(mu);
-    sms = sms_cache[dev & 63];
+    clusters = groups_cache[dev & 63];
   }
-  if (sms == 0) {
+  cudaLaunchAttribute at[2];
+  auto cluster_attr = [&](cudaLaunchAttribute& a) {
+    a.id = cudaLaunchAttributeClusterDimension;
+    a.val.clusterDim.x = kGlCM;
+    a.val.clusterDim.y = 1;
+    a.val.clusterDim.z = 1;
+  };
+  if (clusters == 0) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess)
       return LORA_ERR_CUDA;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return LORA_ERR_CUDA;
-    sms = std::max(1, sms);
+    if (kGlCM > 1) {
+      cudaLaunchConfig_t occ{};
+      occ.gridDim = dim3(kGlCM * 64);
+      occ.blockDim = dim3(kGlThreads);
+      occ.dynamicSmemBytes = smem;
+      cluster_attr(at[0]);
+      occ.attrs = at;
+      occ.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&clusters, kern, &occ) != cudaSuccess) return LORA_ERR_CUDA;
+    } else if (cudaDeviceGetAttribute(&clusters, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      return LORA_ERR_CUDA;
+    }
+    clusters = std::max(1, clusters);
     std::lock_guard<std::mutex> lk(mu);
-    sms_cache[dev & 63] = sms;
+    groups_cache[dev & 63] = clusters;
   }
-  // Whole waves of pairs run as pairs.  Pairs left over run as pairs too when
-  // they fill more than half a wave (one more wave of pairs is shorter than
-  // two waves of single tiles), else as single tiles in one short wave.
+  // Whole waves of groups run as pairs.  Groups left over run as pairs too
+  // when they fill more than half a wave (one more wave of pairs is shorter
+  // than two waves of single tiles), else as single tiles in one short wave.
   if (kGlMT == 2) {
-    const int pairs = ceil_div(t.m_tiles, 2) * t.n_tiles;
-    int whole = (pairs / sms) * sms;
-    if (2 * (pairs - whole) > sms) whole = pairs;
+    const int groups = ceil_div(ceil_div(t.m_tiles, 2), kGlCM) * t.n_tiles;
+    int whole = (groups / clusters) * clusters;
+    if (2 * (groups - whole) > clusters) whole = groups;
     t.pair_units = whole;
-    t.units = whole + 2 * (pairs - whole);
+    t.units = whole + 2 * (groups - whole);
   } else {
     t.pair_units = 0;
-    t.units = t.m_tiles * t.n_tiles;
+    t.units = ceil_div(t.m_tiles, kGlCM) * t.n_tiles;
   }
-  cudaLaunchAttribute at[1];
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(std::max(1, std::min(sms, t.units)));
+  int na = 0;
+  cfg.gridDim = dim3(std::max(1, std::min(clusters, t.units)) * kGlCM);
   cfg.blockDim = dim3(kGlThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
+  if (kGlCM > 1) cluster_attr(at[na++]);
+  at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = na;
   return cuda_status(cudaLaunchKernelEx(&cfg, kern, prm));
 }
 
