@@ -89,6 +89,16 @@ constexpr int kGlStages = kGlMT == 2 ? 3 : 4;    // ring stages (64 KB / 48 KB)
 constexpr int kGlBufs = kGlMT == 2 ? 1 : 2;      // accumulator sets in the 512 TMEM columns
 constexpr uint64_t kGlWaitNs = LSG_WAIT_LIMIT_NS;
 
+#ifdef LSG_TEST_HOOKS
+__device__ int g_test_withhold_gl;
+__device__ __forceinline__ bool gl_withhold(int what) { return *(volatile int*)&g_test_withhold_gl == what; }
+lora_status test_withhold_gl(int what) {
+  return cuda_status(cudaMemcpyToSymbol(g_test_withhold_gl, &what, sizeof(int)));
+}
+#else
+__device__ __forceinline__ bool gl_withhold(int) { return false; }
+#endif
+
 struct GlTail {
   const int32_t* perm;
   const int32_t* seg_offsets;
@@ -543,7 +553,7 @@ __global__ void __launch_bounds__(kGlThreads, 1) gemm_lora_kernel(const __grid_c
       }
       if (!ok) break;
       if (mine) {
-        if (lane == 0) umma_commit(&sm.acc_full[buf]);
+        if (lane == 0 && !(gl_withhold(4) && ui == 0)) umma_commit(&sm.acc_full[buf]);
         __syncwarp();
         ++ui;
       }

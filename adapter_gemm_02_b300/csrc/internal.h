@@ -124,10 +124,12 @@ lora_status cuda_status(cudaError_t e);
 #ifdef LSG_TEST_HOOKS
 // Test builds only: the kernels withhold one signal (1: the decode kernel's
 // end-of-work marker, 2: the partial v that CTA 1 of each decode cluster
-// pushes, 3: the tensor-tile kernel's first expand accumulator), so a bounded
-// wait runs out; 0: none.
+// pushes, 3: the tensor-tile kernel's first expand accumulator, 4: the
+// backbone GEMM's first completed accumulator pair), so a bounded wait runs
+// out; 0: none.
 lora_status test_withhold_cc(int what);
 lora_status test_withhold_tc(int what);
+lora_status test_withhold_gl(int what);
 #endif
 
 }  // namespace lsg

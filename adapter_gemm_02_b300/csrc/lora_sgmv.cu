@@ -74,8 +74,9 @@ int lora_abi_version(void) { return LORA_SGMV_ABI_VERSION; }
 // Test builds only (not declared in the public header): which signal the
 // kernels withhold, so that a bounded wait runs out (see internal.h).
 LORA_API lora_status lora_test_withhold(int what) {
-  const lora_status s = test_withhold_cc(what);
-  return s != LORA_OK ? s : test_withhold_tc(what);
+  lora_status s = test_withhold_cc(what);
+  if (s == LORA_OK) s = test_withhold_tc(what);
+  return s != LORA_OK ? s : test_withhold_gl(what);
 }
 #endif
 
