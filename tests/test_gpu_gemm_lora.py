@@ -135,6 +135,29 @@ def test_padded_rows_and_partial_column_tiles(h_out):
     assert_within_tol(y, _ref(x, W, A, B, ids, 1.5))
 
 
+@pytest.mark.parametrize("interleave", [False, True])
+def test_many_long_segments_per_unit_every_row(interleave):
+    """Segments of 64-130 tokens: each 128-token window overlaps two or three
+    of them, so a unit of two tiles carries four to six long-segment expands
+    (each with its own operand and B tile slot) after its main loop; 2048
+    tokens over 20 column tiles make 160 units of two tiles (one whole wave
+    and single tiles after it).  Every row against the oracle."""
+    rng = np.random.default_rng(11 + int(interleave))
+    lens, total = [], 0
+    while total < 2048 - 130:
+        lens.append(int(rng.integers(64, 131)))
+        total += lens[-1]
+    lens.append(2048 - total)
+    P = len(lens) + 2
+    adapters = rng.permutation(P)[:len(lens)]
+    ids = _requests(lens, adapters, interleave)
+    h_in, h_out, r = 512, 5120, 16
+    x, W, A, B = _problem(f"gl_many_{int(interleave)}", ids, P, h_in, h_out, r)
+    y, err = _run(x, W, A, B, ids, P, 0.8)
+    assert err == 0
+    assert_within_tol(y, _ref(x, W, A, B, ids, 0.8))
+
+
 def test_decode_batch_every_row():
     """A decode batch (every segment short): the GEMM writes x . W and the
     split-K kernel adds every token's delta."""
