@@ -105,8 +105,9 @@ __device__ inline WarpSegOut warp_segment(const int32_t* ids, int n, int P, int3
 // starts a segment; a segment's index is the number of segment-starting
 // tokens with a smaller id.  Ids outside [0, P) sort as P (after every valid
 // token, in token order).  perm_s[n], offs_s[S+1], adap_s[S] in shared memory.
+// idv[e]: the id of token e*32 + lane, already loaded by the caller.
 template <int E>
-__device__ __forceinline__ WarpSegOut warp_segment_rank(const int32_t* ids, int n, int P, int32_t* perm_s,
+__device__ __forceinline__ WarpSegOut warp_segment_rank(const int (&idv)[2], int n, int P, int32_t* perm_s,
                                                         int32_t* offs_s, int32_t* adap_s, int lane) {
   constexpr int kPad = 0x7fffffff;  // lanes past n: after every token
   int key[E];
@@ -116,7 +117,7 @@ __device__ __forceinline__ WarpSegOut warp_segment_rank(const int32_t* ids, int 
     const int i = e * 32 + lane;
     key[e] = kPad;
     if (i < n) {
-      const int id = ids[i];
+      const int id = idv[e];
       const bool ok = id >= 0 && id < P;
       key[e] = ok ? id : P;
       bad |= !ok;

@@ -107,6 +107,10 @@ constexpr int kCThreads = kCW * 32;    // consumer threads
 constexpr int kThreads = kCThreads + 32;
 constexpr int kMaxC = 8;               // CTAs per cluster (portable limit)
 constexpr int kXB = 2;                 // partial-v exchange buffers
+// 1: a one-launch step's ids (up to 64) are loaded at the kernel's entry
+#ifndef LSG_CC_IDS_EARLY
+#define LSG_CC_IDS_EARLY 1
+#endif
 constexpr uint64_t kWaitLimitNs = LSG_WAIT_LIMIT_NS;  // per wait (2 s)
 
 #ifdef LSG_TEST_HOOKS
@@ -370,6 +374,20 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
   const int ngroups = static_cast<int>(gridDim.x) / C;
   const bool xchg = kHasShrink && C > 1;
 
+  // One-launch step of up to 64 tokens: the producer's lanes load the ids
+  // first, so that their latency overlaps the prologue below (the ids are
+  // read before the dependency wait, as the header states).
+  int id_pre[2] = {0, 0};
+  auto load_ids = [&]() {
+    const int32_t* ids = p.n_ids_in_params > 0 ? p.ids_in_params : p.t.ids;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int i = e * 32 + lane;
+      if (i < p.t.n_tokens) id_pre[e] = ids[i];
+    }
+  };
+  if (LSG_CC_IDS_EARLY && warp == kCW && p.t.ids != nullptr && p.t.n_tokens <= 64) load_ids();
+
   // Per-call parameters to shared memory: every word in flight at once.
   {
     static_assert(sizeof(CCTail) % 4 == 0, "tail size");
@@ -447,8 +465,9 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
       int32_t* count_s = adap_s + max(ms, 1);
       // up to 64 tokens: ranks in registers; more: counting sort in shared memory
       const int32_t* ids = p.n_ids_in_params > 0 ? p.ids_in_params : q.ids;
-      so = n <= 32   ? warp_segment_rank<1>(ids, n, P, perm_s, offs_s, adap_s, lane)
-           : n <= 64 ? warp_segment_rank<2>(ids, n, P, perm_s, offs_s, adap_s, lane)
+      if (!LSG_CC_IDS_EARLY && n <= 64) load_ids();
+      so = n <= 32   ? warp_segment_rank<1>(id_pre, n, P, perm_s, offs_s, adap_s, lane)
+           : n <= 64 ? warp_segment_rank<2>(id_pre, n, P, perm_s, offs_s, adap_s, lane)
                      : warp_segment(ids, n, P, ids_s, cnt, perm_s, offs_s, adap_s, lane);
       fence_proxy_async_smem();  // stage 0 is next written by the tensor copies
       if (lane == 0) *count_s = so.S;
