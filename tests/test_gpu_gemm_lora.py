@@ -110,20 +110,22 @@ def test_units_of_two_token_tiles_every_row(n, interleave, r):
     assert_within_tol(y, _ref(x, W, A, B, ids, 0.75))
 
 
-@pytest.mark.parametrize("h_out", [576, 1000])
-def test_padded_rows_and_partial_column_tiles(h_out):
+@pytest.mark.parametrize("h_in,h_out", [(768, 576), (1000, 1000)])
+def test_padded_rows_and_partial_column_tiles(h_in, h_out):
     """x and y with row strides past their widths (y's padding must stay
     untouched by the box stores), and a last column tile that runs past h_out:
     576 = 9 x 64 (W as one 3-D box per stage, its blocks past h_out read as
-    zeros) or 1000 (W by 64-column boxes, the last one partly past h_out)."""
+    zeros) or 1000 (W by 64-column boxes, the last one partly past h_out).
+    h_in = 1000: the last k-block is partial (x columns and W rows past h_in
+    read as zeros, in the GEMM and in the shrink)."""
     ids = _requests([300, 200, 100, 40], [2, 0, 3, 1])
-    n, P, h_in, r = ids.size, 4, 768, 32
+    n, P, r = ids.size, 4, 32
     ldx, ldy = h_in + 64, h_out + 136
-    x_full = normal_bf16((n, ldx), 1.0, seed_for(f"gl_pad_{h_out}", "x"), "cuda")
+    x_full = normal_bf16((n, ldx), 1.0, seed_for(f"gl_pad_{h_in}_{h_out}", "x"), "cuda")
     x = x_full[:, :h_in]
-    W = normal_bf16((h_in, h_out), 1.0 / h_in, seed_for(f"gl_pad_{h_out}", "W"), "cuda")
-    A = normal_bf16((P, h_in, r), 1.0 / h_in, seed_for(f"gl_pad_{h_out}", "A"), "cuda")
-    B = normal_bf16((P, r, h_out), 1.0 / r, seed_for(f"gl_pad_{h_out}", "B"), "cuda")
+    W = normal_bf16((h_in, h_out), 1.0 / h_in, seed_for(f"gl_pad_{h_in}_{h_out}", "W"), "cuda")
+    A = normal_bf16((P, h_in, r), 1.0 / h_in, seed_for(f"gl_pad_{h_in}_{h_out}", "A"), "cuda")
+    B = normal_bf16((P, r, h_out), 1.0 / r, seed_for(f"gl_pad_{h_in}_{h_out}", "B"), "cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     seg = lsg.lora_segment(torch.from_numpy(ids).cuda(), P, err_flag=err)
     y_full = torch.full((n, ldy), 7.0, dtype=torch.bfloat16, device="cuda")
