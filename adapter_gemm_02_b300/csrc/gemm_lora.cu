@@ -32,17 +32,23 @@
 // CTAs, so the units in flight together cover a few token tiles and all of W:
 // both stay in L2.  Only whole waves of pairs are dealt as pairs; when the
 // pairs left over fill at most half a wave they are dealt as single tiles
-// (twice as many units, each half as long), so the last wave is short.  Six
-// warps:
+// (twice as many units, each about a fifth shorter than a pair), so the last
+// wave is shorter.  Six warps:
 //   warps 0-3  epilogue (warp w: TMEM lane quarter w; thread = tile row): the
-//              v operand of each long segment, then y from the accumulators
-//   warp 4     producer: TMA x tiles [128][64] (2-D box, or four-row gathers
-//              through the permutation), W tiles [64][256] (four [64][64]
-//              boxes, MN-major, 128 B swizzle), B tiles [r][256]
+//              operand (s v as bf16 hi + lo) of each long segment, then y
+//              from the accumulators (a warp's 32 contiguous rows through a
+//              swizzled staging box and one TMA store, other rows by 16-byte
+//              stores)
+//   warp 4     producer: TMA x tiles [128][64] (a 2-D box, one 256-row box
+//              for two adjacent contiguous tiles, or four-row gathers through
+//              the permutation), W tiles [64][256] (one 3-D box of four
+//              [64][64] blocks, or four boxes; MN-major, 128 B swizzle), B
+//              tiles [r][256]
 //   warp 5     TMEM allocation; one thread issues the MMAs (M = 128, N = 256)
-// The ring's stages hold the unit's x tiles and one W tile.  Single-tile
-// builds (LSG_GL_PAIR=0) keep two accumulators that alternate between units
-// instead, so the epilogue of one unit overlaps the main loop of the next.
+// The ring's stages (3 of 64 KB) hold the unit's x tiles and one W tile.
+// TMEM holds no second pair of accumulators, so the issuer starts the next
+// unit once the epilogue has read both.  Single-tile builds (LSG_GL_PAIR=0)
+// keep two accumulators that alternate between units instead.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -78,7 +84,8 @@ constexpr int kGlMaxRuns = 3;  // long segments (>= 64 tokens) a 128-token windo
 // column tile of different token tiles, each loads a 1/CM share of the W
 // tile and multicasts it to every CTA of the cluster, so each SM reads
 // 1/CM of the W bytes from L2.  A ring slot is refilled only after every CTA
-// of the cluster has consumed it.
+// of the cluster has consumed it.  Measured no faster on the 13B layer (each
+// SM still receives the whole stage), so CTAs run alone.
 #ifndef LSG_GL_CM
 #define LSG_GL_CM 1
 #endif
