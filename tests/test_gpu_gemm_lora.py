@@ -87,7 +87,7 @@ def test_interleaved_short_and_invalid_every_row(r):
     assert_within_tol(y, _ref(x, W, A, B, ids, 1.25))
 
 
-@pytest.mark.parametrize("n,interleave,r", [(2100, False, 64), (2100, True, 16), (3072, True, 32)])
+@pytest.mark.parametrize("n,interleave,r", [(2100, False, 64), (2100, True, 16), (3072, True, 32), (2100, False, 8)])
 def test_units_of_two_token_tiles_every_row(n, interleave, r):
     """Batches large enough for units of two token tiles (256 tokens x 256
     columns) on every SM.  2100 tokens over 20 column tiles: 17 tiles, 180
